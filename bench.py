@@ -1,0 +1,383 @@
+#!/usr/bin/env python
+"""Benchmark of the fused SwiGLU + MXFP8 cast on GB300.
+
+One step = the six fused cells of the pages' headline shape M=131072,
+N=8192 ("Add swiglu + MXFP8 fused CuTe DSL kernel", section "Performance"):
+forward rowwise / colwise / both and backward rowwise / colwise / both, each
+one launch of libmxfp8 over the same resident bf16 inputs (gate, up, dh:
+3 x 2 GiB, far larger than L2, so no L2 flush is needed between steps).
+
+The metric is algorithmic GB/s = (bytes read + bytes written) / time with
+GB = 1e9: fwd reads 4MN and writes k(MN + MN/32), bwd reads 6MN and writes
+2k(MN + MN/32), k = 1 (row or col) or 2 (both).  ``value`` is the whole
+step's bytes over its time, summed over ranks (weak scaling: every rank casts
+its own batch; no collective on the data path).
+
+Prints one JSON line.  ``--impl reference`` instead times the CPU oracle on a
+bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+M_LARGE, N_LARGE = 131072, 8192
+CELLS = [("fwd", 1), ("fwd", 2), ("fwd", 3), ("bwd", 1), ("bwd", 2), ("bwd", 3)]
+MODE_NAME = {1: "row", 2: "col", 3: "both"}
+METRIC = "fused SwiGLU+MXFP8 cast GB/s (fwd/bwd, row/col/both) and % of GB300 HBM peak"
+WORKLOAD = "swiglu_mxfp8_fwd_bwd_row_col_both_131072x8192"
+# the pages' own figures for these six cells at (131072, 8192), GB200 with
+# clocks pinned at 2062 MHz (context, another machine): microseconds per cell
+PAGES_US = {("fwd", 1): 904.19, ("fwd", 2): 1022.98, ("fwd", 3): 1216.08,
+            ("bwd", 1): 1321.98, ("bwd", 2): 1710.08, ("bwd", 3): 1859.09}
+
+
+def cell_bytes(kind: str, mode: int, M: int, N: int) -> int:
+    k = 2 if mode == 3 else 1
+    mn = M * N
+    cast = mn + mn // 32
+    return 4 * mn + k * cast if kind == "fwd" else 6 * mn + 2 * k * cast
+
+
+def step_bytes(M=M_LARGE, N=N_LARGE) -> int:
+    return sum(cell_bytes(k, m, M, N) for k, m in CELLS)
+
+
+def pages_step_gbs() -> float:
+    return step_bytes() / (sum(PAGES_US.values()) * 1e-6) / 1e9
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def base_config(extra=None):
+    c = {"workload": WORKLOAD, "M": M_LARGE, "N": N_LARGE,
+         "cells": ["%s_%s" % (k, MODE_NAME[m]) for k, m in CELLS],
+         "inputs": "gate, up, dh bf16 N(0,1), seed 3 (+rank), resident in HBM",
+         "l2": "no flush: 6 GiB of inputs per step, far above the 129 MB L2"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+                 "-i", str(gpu_index), "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.flush()
+        with open(self.f.name) as fh:
+            lines = [ln.strip() for ln in fh if ln.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- CPU oracle
+def oracle_step(gate_b, up_b, dh_b, threads=None):
+    """The six cells of one step through the CPU oracle (plain definitions)."""
+    import oracle as O
+    for kind, mode in CELLS:
+        if kind == "fwd":
+            O.swiglu_fwd(gate_b, up_b, mode, threads=threads)
+        else:
+            O.swiglu_bwd(dh_b, gate_b, up_b, mode, threads=threads)
+
+
+def cpu_sample(rows: int, seed: int = 3):
+    """A (rows, 8192) sample of the workload drawn on the host (same recipe)."""
+    import numpy as np
+    import torch
+    from mxfp8_quantization_moe_gb300 import synthetic
+    g = torch.Generator().manual_seed(seed)
+    t = [synthetic.normal_bf16((rows, N_LARGE), 1.0, g, "cpu") for _ in range(3)]
+    return [x.view(torch.int16).numpy().view(np.uint16) for x in t]
+
+
+def time_oracle(target_s: float, threads: int):
+    """Grow a sample of 32-row blocks until one oracle step takes ~target_s."""
+    rows = 32
+    while True:
+        gate, up, dh = cpu_sample(rows)
+        t0 = time.perf_counter()
+        oracle_step(gate, up, dh, threads=threads)
+        dt = time.perf_counter() - t0
+        if dt >= target_s * 0.5 or rows >= 4096:
+            return rows, dt
+        rows = min(4096, max(rows * 2, int(rows * target_s / max(dt, 1e-3)) // 32 * 32))
+
+
+def cpu_baseline(target_s: float):
+    threads = os.cpu_count() or 1
+    rows, dt = time_oracle(target_s, threads)
+    b = step_bytes(rows, N_LARGE)
+    return {"value": b / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": "%d of 131072 rows (%d 32-row blocks) x 8192, all six cells, one pass, "
+                      "%.1f s on %d threads" % (rows, rows // 32, dt, threads)}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    threads = os.cpu_count() or 1
+    rows = 32 * max(1, args.ref_blocks)
+    gate, up, dh = cpu_sample(rows)
+    for _ in range(args.warmup):
+        oracle_step(gate, up, dh, threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(gate, up, dh, threads=threads)
+    dt = time.perf_counter() - t0
+    b = step_bytes(rows, N_LARGE)
+    val = b * args.steps / dt / 1e9
+    sample = "%d of 131072 rows x 8192 per step, all six cells, %d threads" % (rows, threads)
+    line = {"metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": base_config({"sample_rows": rows}), "impl": "reference",
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# -------------------------------------------------------------------- GPU
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mx", choices=["mx", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--ref-blocks", type=int, default=2)
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import torch
+    import torch.distributed as dist
+
+    # the CPU oracle's thread pool is started before any GPU work
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        cpu = cpu_baseline(args.cpu_seconds)
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    import mxfp8_quantization_moe_gb300 as mx
+    from mxfp8_quantization_moe_gb300 import synthetic
+
+    mx.init()
+    gate, up, dh = synthetic.large(device="cuda", seed=synthetic.SEEDS["large_131072x8192"] + rank)
+    M, N = gate.shape
+    fwd_out = {m: mx._alloc(M, N, m, gate.device) for m in (1, 2, 3)}
+    bwd_out = {}
+    for m in (1, 2, 3):
+        o = mx.SwiGLUGrads()
+        if m & 1:
+            o.q_row = torch.empty((M, 2 * N), dtype=torch.uint8, device="cuda")
+            o.s_row = torch.empty((M, 2 * N // 32), dtype=torch.uint8, device="cuda")
+        if m & 2:
+            o.q_col = torch.empty((2 * N, M), dtype=torch.uint8, device="cuda")
+            o.s_col = torch.empty((M // 32, 2 * N), dtype=torch.uint8, device="cuda")
+        bwd_out[m] = o
+    stream = torch.cuda.current_stream()
+
+    def launch(kind, mode):
+        if kind == "fwd":
+            mx.swiglu_fwd(gate, up, mode, out=fwd_out[mode])
+        else:
+            mx.swiglu_bwd(dh, gate, up, mode, out=bwd_out[mode])
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        for c in CELLS:
+            launch(*c)
+    barrier()
+    mx.device_status(reset=True)
+
+    K = args.steps
+    ev = {c: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)] for c in CELLS}
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    barrier()
+    t_start.record(stream)
+    for k in range(K):
+        for c in CELLS:
+            ev[c][k][0].record(stream)
+            launch(*c)
+            ev[c][k][1].record(stream)
+    t_end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    if world > 1:
+        t = torch.tensor([elapsed], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    flags, fallbacks = mx.device_status()
+    if flags:
+        raise SystemExit("device status flags %#x after the timed region" % flags)
+
+    peak, peak_kind = peaks()
+    per_cell = {}
+    for c in CELLS:
+        us = statistics.mean(a.elapsed_time(b) for a, b in ev[c]) * 1e3
+        b = cell_bytes(c[0], c[1], M, N)
+        per_cell["%s_%s" % (c[0], MODE_NAME[c[1]])] = {
+            "us": round(us, 2), "GBps": round(b / us / 1e3, 1), "frac_of_peak": round(b / us / 1e3 / peak, 4),
+            "bytes": b}
+    dom = max(per_cell, key=lambda k: per_cell[k]["us"])
+    dom_achieved = per_cell[dom]["GBps"]
+
+    total_bytes = step_bytes(M, N) * K * world
+    value = total_bytes / elapsed / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, mx, gate, up, dh, fwd_out, bwd_out, launch, barrier, world)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(elapsed / K * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": round(value / world / pages_step_gbs(), 4),
+        "dtype": "f32", "data": "synthetic",
+        "config": base_config({"parallelism": "replicas%d" % world if world > 1 else "single",
+                               "vs_baseline_note": "pages' six-cell aggregate %.1f GB/s on GB200 "
+                                                   "(another machine; context)" % pages_step_gbs()}),
+        "frac_of_peak": round(value / world / peak, 4),
+        "per_cell": per_cell,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": dom_achieved, "peak": peak,
+                     "peak_kind": "%s hbm_gbs (copy)" % peak_kind, "unit": "GB/s",
+                     "frac": round(dom_achieved / peak, 4), "traffic": None},
+        "gpu_launches": K * len(CELLS),
+        "fallback_elements": fallbacks,
+        "clocks": clk,
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if cpu:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, mx, gate, up, dh, fwd_out, bwd_out, launch, barrier, world):
+    """Same metric through the public API with host buffers: every step copies
+    the inputs host->device from pinned memory, runs the six cells, and
+    copies every cast output back to pinned host memory."""
+    import torch
+    h_in = [t.cpu().pin_memory() for t in (gate, up, dh)]
+    outs = []
+    for m in (1, 2, 3):
+        o = fwd_out[m]
+        outs += [t for t in (o.q_row, o.s_row, o.q_col, o.s_col) if t is not None]
+        o = bwd_out[m]
+        outs += [t for t in (o.q_row, o.s_row, o.q_col, o.s_col) if t is not None]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for d, h in zip((gate, up, dh), h_in):
+            d.copy_(h, non_blocking=True)
+        for c in CELLS:
+            launch(*c)
+        for d, h in zip(outs, h_out):
+            h.copy_(d, non_blocking=True)
+
+    step()
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(1, args.e2e_steps)
+    a.record(stream)
+    for _ in range(n):
+        step()
+    b.record(stream)
+    barrier()
+    el = a.elapsed_time(b) / 1e3
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([el], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        el = float(t.item())
+    val = step_bytes() * n * world / el / 1e9
+    return {"value": round(val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": n, "ms_per_step": round(el / n * 1e3, 3)}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

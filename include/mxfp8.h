@@ -1,0 +1,171 @@
+/*
+ * mxfp8.h -- C ABI of libmxfp8: MXFP8 casts for MoE training on GB300 (sm_103a).
+ *
+ * MXFP8 here means: E4M3 (fn) data plus one E8M0 scale byte per block of 32
+ * consecutive elements along the blocking axis.  The scale byte is RCEIL:
+ * e = ceil(log2(amax / 448)) clamped to [-127, 127], byte = e + 127, and 0
+ * for an all-zero block; a block whose amax is NaN or Inf gets byte 255 and
+ * 32 NaN codes (0x7F).  Data codes are x * 2^-e rounded to nearest, ties to
+ * even, saturating at +-448, sign of zero kept (a byte-0 scale multiplies by
+ * 2^127).  Sources: "Add swiglu + MXFP8 fused CuTe DSL kernel" (torchao fork
+ * PR #2), sections "Summary", "API" and "Numerics and tests" and its commit
+ * message; "[mxfp8 moe training] update 3d quant colwise scaling kernel to use
+ * single input/output TMA descriptors" (pytorch/ao PR #3034), "Summary".
+ *
+ * Conventions shared by every entry point:
+ *  - bf16 tensors are passed as pointers to their 16-bit patterns.
+ *  - All tensor pointers are DEVICE pointers on the current CUDA device; the
+ *    caller owns every buffer.  The library never allocates a buffer for a
+ *    call, never frees one and never synchronizes; work is enqueued on
+ *    `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *  - Sizes and leading dimensions are int64_t, in ELEMENTS (bf16 elements for
+ *    inputs, bytes for E4M3/E8M0 outputs).  Indexing is 64-bit.
+ *  - Rowwise (1x32 blocks along a row): data (M, N) row-major, element (r, c)
+ *    at q_row[r * ld_qrow + c]; scales (M, N/32) row-major, s_row[r * ld_srow
+ *    + c/32].  Needs N % 32 == 0.
+ *  - Colwise (32x1 blocks down a column): data (M, N) COLUMN-major, element
+ *    (r, c) at q_col[c * ld_qcol + r]; scales (M/32, N) row-major,
+ *    s_col[(r/32) * ld_scol + c].  Needs M % 32 == 0.
+ *  - Pointers of a disabled direction are ignored (pass NULL).
+ *  - M == 0 or N == 0 (or E == 0) is an empty call: MXFP8_OK, nothing runs.
+ *  - Errors are returned, never thrown; every argument check runs on the host
+ *    before anything is enqueued, so a rejected call leaves the stream and
+ *    the device untouched.
+ *  - Alignment: input pointers 16-byte aligned and ld * 2 a multiple of 16
+ *    bytes (TMA tiles); E4M3 data pointers 16-byte aligned with leading
+ *    dimensions multiples of 16.  Scale pointers have no alignment rule.
+ *  - No output may overlap an input or another output (strided regions with
+ *    equal leading dimensions are checked exactly, so interleaved layouts
+ *    such as [dGate | dUp] halves of one buffer are accepted).
+ *  - Calls are thread-safe.  The first call on a device builds a 512 KB
+ *    read-only sigmoid table in device memory (see mxfp8_init); do that
+ *    before capturing a CUDA graph.
+ */
+#ifndef MXFP8_H
+#define MXFP8_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MXFP8_ROWWISE = 1, /* 1x32 blocks, row-major data + (M, N/32) scales     */
+    MXFP8_COLWISE = 2, /* 32x1 blocks, column-major data + (M/32, N) scales  */
+    MXFP8_BOTH = 3     /* both sets from one read of the input               */
+} mxfp8_scale_mode;
+
+typedef enum {
+    MXFP8_OK = 0,
+    MXFP8_ERR_NULL = 1,     /* a required pointer is NULL                        */
+    MXFP8_ERR_SHAPE = 2,    /* negative size, or N % 32 (rowwise) / M % 32
+                               (colwise, 3D N) not zero, or a size overflows      */
+    MXFP8_ERR_ALIGN = 3,    /* pointer or leading dimension misaligned           */
+    MXFP8_ERR_LD = 4,       /* leading dimension smaller than the row it spans   */
+    MXFP8_ERR_MODE = 5,     /* scale mode not 1, 2 or 3                          */
+    MXFP8_ERR_OVERLAP = 6,  /* an output overlaps an input or another output     */
+    MXFP8_ERR_LAUNCH = 7,   /* the CUDA runtime refused the launch               */
+    MXFP8_ERR_DEVICE = 8,   /* no usable device, or device set-up failed         */
+    MXFP8_ERR_CAPTURE = 9   /* first call on a device made during stream capture */
+} mxfp8_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *mxfp8_status_str(mxfp8_status s);
+
+/* Version of this library: major * 10000 + minor * 100 + patch. */
+int mxfp8_version(void);
+
+/*
+ * One-time set-up of the current device: fills the library's read-only table
+ * of sigmoid(g) in double for every bf16 g (used by the exact-rounding path of
+ * the SwiGLU kernels) and waits for it on `stream`.  Every entry point calls it
+ * on its first use on a device; call it yourself before capturing a graph.
+ * Returns MXFP8_ERR_CAPTURE if it would have to run inside a capture.
+ */
+mxfp8_status mxfp8_init(void *stream);
+
+/*
+ * Standalone 2D quantizer: bf16 x (M, N), element (r, c) at x[r * ld_x + c],
+ * to MXFP8 rowwise, colwise or both, in one pass over x.
+ * ("Add swiglu + MXFP8 fused CuTe DSL kernel", sections "Summary" and
+ * "Numerics and tests": the standalone MXFP8 quantizers.)
+ */
+mxfp8_status mxfp8_quant_2d(const uint16_t *x, int64_t ld_x, int64_t M, int64_t N,
+                            int mode,
+                            uint8_t *q_row, int64_t ld_qrow, uint8_t *s_row, int64_t ld_srow,
+                            uint8_t *q_col, int64_t ld_qcol, uint8_t *s_col, int64_t ld_scol,
+                            void *stream);
+
+/*
+ * Fused SwiGLU forward + MXFP8 cast.  h = silu(gate) * up, evaluated at fp32
+ * precision and rounded once to bf16 (never written to memory), is cast as
+ * mxfp8_quant_2d would cast a stored h.  gate and up are (M, N) with the same
+ * leading dimension ld_in; the packed [gate | up] buffer of a fused w13
+ * projection is gate = buf, up = buf + N, ld_in = 2N.
+ * ("Add swiglu + MXFP8 fused CuTe DSL kernel", sections "Summary" and "API".)
+ */
+mxfp8_status mxfp8_swiglu_fwd(const uint16_t *gate, const uint16_t *up, int64_t ld_in,
+                              int64_t M, int64_t N, int mode,
+                              uint8_t *q_row, int64_t ld_qrow, uint8_t *s_row, int64_t ld_srow,
+                              uint8_t *q_col, int64_t ld_qcol, uint8_t *s_col, int64_t ld_scol,
+                              void *stream);
+
+/*
+ * Fused SwiGLU backward + MXFP8 cast.  From dh (M, N), gate and up:
+ *   dgate = dh * up * sigmoid(gate) * (1 + gate * (1 - sigmoid(gate)))
+ *   dup   = dh * gate * sigmoid(gate)
+ * each evaluated at fp32 precision, rounded once to bf16, then cast like
+ * mxfp8_quant_2d.  dgate and dup share the leading dimensions of their
+ * direction, so the concatenated [dGate | dUp] outputs are: rowwise
+ * du_row = dg_row + N with ld_qrow = 2N (scales du_srow = dg_srow + N/32,
+ * ld_srow = N/16); colwise du_col = dg_col + N * ld_qcol and
+ * du_scol = dg_scol + N with ld_scol = 2N.
+ * ("Add swiglu + MXFP8 fused CuTe DSL kernel", sections "API" and "Numerics
+ * and tests".)
+ */
+mxfp8_status mxfp8_swiglu_bwd(const uint16_t *dh, int64_t ld_dh,
+                              const uint16_t *gate, const uint16_t *up, int64_t ld_in,
+                              int64_t M, int64_t N, int mode,
+                              uint8_t *dg_row, uint8_t *du_row, int64_t ld_qrow,
+                              uint8_t *dg_srow, uint8_t *du_srow, int64_t ld_srow,
+                              uint8_t *dg_col, uint8_t *du_col, int64_t ld_qcol,
+                              uint8_t *dg_scol, uint8_t *du_scol, int64_t ld_scol,
+                              void *stream);
+
+/*
+ * Per-expert 3D colwise quantizer: x (E, N, K) bf16 row-major (element
+ * (e, n, k) at x[(e*N + n)*K + k]) -> E4M3 data column-major per expert,
+ * element (e, n, k) at q[e*N*K + k*N + n], and E8M0 scales (E, N/32, K)
+ * row-major, s[e*(N/32)*K + (n/32)*K + k]; blocks of 32 along N.  One launch
+ * covers every expert.  Needs N % 32 == 0 and K % 8 == 0.
+ * ("[mxfp8 moe training] update 3d quant colwise scaling kernel to use
+ * single input/output TMA descriptors", sections "Summary" and "Performance".)
+ */
+mxfp8_status mxfp8_quant_3d_colwise(const uint16_t *x, int64_t E, int64_t N, int64_t K,
+                                    uint8_t *q, uint8_t *s, void *stream);
+
+/*
+ * Sticky device-side status of the current device.  Kernels never trap: a
+ * pipeline wait that exceeds its limit (about a second) makes the kernel set
+ * a flag bit and return.  flags: bit 0 consumer wait, bit 1 producer wait,
+ * bit 2 drain wait, bit 3 self-test wait.  fallbacks: number of SwiGLU
+ * elements whose bf16 rounding was settled by the double-precision path.
+ * Synchronizes `stream`; with reset != 0 clears both afterwards.
+ * Either output pointer (host memory) may be NULL.
+ */
+mxfp8_status mxfp8_device_status(uint32_t *flags, uint64_t *fallbacks, int reset, void *stream);
+
+/*
+ * Failure-detection self-test: launches one thread that waits on a shared
+ * memory barrier nobody arrives on, giving up after `limit_cycles` SM clock
+ * cycles; it then sets status bit 3 and returns.  Used by the tests to show
+ * that a stuck wait ends with a readable error instead of a hang.
+ */
+mxfp8_status mxfp8_selftest_wait_timeout(uint64_t limit_cycles, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP8_H */

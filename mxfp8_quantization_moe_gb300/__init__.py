@@ -1,0 +1,199 @@
+"""mxfp8_quantization_moe_gb300 -- MXFP8 casts for MoE training on GB300.
+
+The compute lives in ``libmxfp8.so`` (hand-written CUDA for sm_103a, C ABI in
+``include/mxfp8.h``).  ``capi`` binds that ABI one-to-one; the helpers below
+allocate outputs with PyTorch and call it.  Nothing here computes a cast on
+the host: without the built library the import fails.
+
+Layouts of the returned tensors (uint8):
+  q_row (M, N) row-major,  s_row (M, N/32)
+  q_col (N, M): q_col[c, r] is element (r, c) -- the column-major (M, N) data
+  s_col (M/32, N)
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import capi
+from .capi import MXFP8_BOTH, MXFP8_COLWISE, MXFP8_ROWWISE, MXFP8Error, check
+
+__all__ = ["capi", "MXFP8Cast", "quant_2d", "swiglu_fwd", "swiglu_bwd", "quant_3d_colwise",
+           "init", "device_status", "MXFP8_ROWWISE", "MXFP8_COLWISE", "MXFP8_BOTH", "MXFP8Error"]
+
+
+@dataclass
+class MXFP8Cast:
+    q_row: Optional[torch.Tensor] = None
+    s_row: Optional[torch.Tensor] = None
+    q_col: Optional[torch.Tensor] = None
+    s_col: Optional[torch.Tensor] = None
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _check_bf16_2d(t: torch.Tensor, name: str):
+    if t.dtype != torch.bfloat16 or t.dim() != 2 or not t.is_cuda:
+        raise ValueError("%s must be a 2D bf16 CUDA tensor" % name)
+    if t.stride(1) != 1:
+        raise ValueError("%s must have unit column stride" % name)
+
+
+def _alloc(M: int, N: int, mode: int, device, ld_row: Optional[int] = None) -> MXFP8Cast:
+    out = MXFP8Cast()
+    if mode & MXFP8_ROWWISE:
+        out.q_row = torch.empty((M, N), dtype=torch.uint8, device=device)
+        out.s_row = torch.empty((M, N // 32), dtype=torch.uint8, device=device)
+    if mode & MXFP8_COLWISE:
+        out.q_col = torch.empty((N, M), dtype=torch.uint8, device=device)
+        out.s_col = torch.empty((M // 32, N), dtype=torch.uint8, device=device)
+    return out
+
+
+def _lds(o: MXFP8Cast):
+    return (o.q_row.stride(0) if o.q_row is not None else 0,
+            o.s_row.stride(0) if o.s_row is not None else 0,
+            o.q_col.stride(0) if o.q_col is not None else 0,
+            o.s_col.stride(0) if o.s_col is not None else 0)
+
+
+def init(stream=None) -> None:
+    check(capi.mxfp8_init(_stream(stream)), "mxfp8_init")
+
+
+def quant_2d(x: torch.Tensor, mode: int = MXFP8_BOTH, out: Optional[MXFP8Cast] = None,
+             stream=None) -> MXFP8Cast:
+    """Standalone MXFP8 cast of a bf16 (M, N) tensor."""
+    _check_bf16_2d(x, "x")
+    M, N = x.shape
+    o = out if out is not None else _alloc(M, N, mode, x.device)
+    a, b, c, d = _lds(o)
+    check(capi.mxfp8_quant_2d(x.data_ptr(), x.stride(0), M, N, mode,
+                              _ptr(o.q_row), a, _ptr(o.s_row), b,
+                              _ptr(o.q_col), c, _ptr(o.s_col), d, _stream(stream)), "mxfp8_quant_2d")
+    return o
+
+
+def swiglu_fwd(gate: torch.Tensor, up: Optional[torch.Tensor] = None, mode: int = MXFP8_BOTH,
+               out: Optional[MXFP8Cast] = None, stream=None) -> MXFP8Cast:
+    """Fused SwiGLU + MXFP8 cast.  With ``up=None``, ``gate`` is the packed
+    [gate | up] (M, 2N) buffer."""
+    if up is None:
+        _check_bf16_2d(gate, "gate_up")
+        n = gate.shape[1] // 2
+        gate, up = gate[:, :n], gate[:, n:]
+    _check_bf16_2d(gate, "gate")
+    _check_bf16_2d(up, "up")
+    if gate.shape != up.shape or gate.stride() != up.stride():
+        raise ValueError("gate and up must have the same shape and strides")
+    M, N = gate.shape
+    o = out if out is not None else _alloc(M, N, mode, gate.device)
+    a, b, c, d = _lds(o)
+    check(capi.mxfp8_swiglu_fwd(gate.data_ptr(), up.data_ptr(), gate.stride(0), M, N, mode,
+                                _ptr(o.q_row), a, _ptr(o.s_row), b,
+                                _ptr(o.q_col), c, _ptr(o.s_col), d, _stream(stream)),
+          "mxfp8_swiglu_fwd")
+    return o
+
+
+@dataclass
+class SwiGLUGrads:
+    """Packed [dGate | dUp] MXFP8 gradients.
+
+    q_row (M, 2N), s_row (M, N/16); q_col (2N, M) column-major, s_col (M/32, 2N).
+    """
+    q_row: Optional[torch.Tensor] = None
+    s_row: Optional[torch.Tensor] = None
+    q_col: Optional[torch.Tensor] = None
+    s_col: Optional[torch.Tensor] = None
+
+    def dgate(self) -> MXFP8Cast:
+        n = self._n()
+        return MXFP8Cast(*self._halves(0, n))
+
+    def dup(self) -> MXFP8Cast:
+        n = self._n()
+        return MXFP8Cast(*self._halves(1, n))
+
+    def _n(self):
+        return (self.q_row.shape[1] if self.q_row is not None else self.q_col.shape[0]) // 2
+
+    def _halves(self, h, n):
+        r = []
+        r.append(None if self.q_row is None else self.q_row[:, h * n:(h + 1) * n])
+        r.append(None if self.s_row is None else self.s_row[:, h * n // 32:(h + 1) * n // 32])
+        r.append(None if self.q_col is None else self.q_col[h * n:(h + 1) * n])
+        r.append(None if self.s_col is None else self.s_col[:, h * n:(h + 1) * n])
+        return r
+
+
+def swiglu_bwd(dh: torch.Tensor, gate: torch.Tensor, up: Optional[torch.Tensor] = None,
+               mode: int = MXFP8_BOTH, out: Optional[SwiGLUGrads] = None, stream=None) -> SwiGLUGrads:
+    """Fused SwiGLU backward + MXFP8 cast of dgate and dup into packed
+    [dGate | dUp] outputs.  With ``up=None``, ``gate`` is the packed input."""
+    if up is None:
+        n = gate.shape[1] // 2
+        gate, up = gate[:, :n], gate[:, n:]
+    for t, nm in ((dh, "dh"), (gate, "gate"), (up, "up")):
+        _check_bf16_2d(t, nm)
+    if gate.shape != up.shape or gate.stride() != up.stride() or dh.shape != gate.shape:
+        raise ValueError("dh, gate and up must have the same shape (gate/up the same strides)")
+    M, N = gate.shape
+    dev = gate.device
+    o = out
+    if o is None:
+        o = SwiGLUGrads()
+        if mode & MXFP8_ROWWISE:
+            o.q_row = torch.empty((M, 2 * N), dtype=torch.uint8, device=dev)
+            o.s_row = torch.empty((M, 2 * N // 32), dtype=torch.uint8, device=dev)
+        if mode & MXFP8_COLWISE:
+            o.q_col = torch.empty((2 * N, M), dtype=torch.uint8, device=dev)
+            o.s_col = torch.empty((M // 32, 2 * N), dtype=torch.uint8, device=dev)
+    qr = o.q_row.data_ptr() if o.q_row is not None else None
+    sr = o.s_row.data_ptr() if o.s_row is not None else None
+    qc = o.q_col.data_ptr() if o.q_col is not None else None
+    sc = o.s_col.data_ptr() if o.s_col is not None else None
+    ld_qrow = o.q_row.stride(0) if o.q_row is not None else 0
+    ld_srow = o.s_row.stride(0) if o.s_row is not None else 0
+    ld_qcol = o.q_col.stride(0) if o.q_col is not None else 0
+    ld_scol = o.s_col.stride(0) if o.s_col is not None else 0
+    check(capi.mxfp8_swiglu_bwd(
+        dh.data_ptr(), dh.stride(0), gate.data_ptr(), up.data_ptr(), gate.stride(0), M, N, mode,
+        qr, None if qr is None else qr + N, ld_qrow,
+        sr, None if sr is None else sr + N // 32, ld_srow,
+        qc, None if qc is None else qc + N * ld_qcol, ld_qcol,
+        sc, None if sc is None else sc + N, ld_scol,
+        _stream(stream)), "mxfp8_swiglu_bwd")
+    return o
+
+
+def quant_3d_colwise(x: torch.Tensor, q: Optional[torch.Tensor] = None,
+                     s: Optional[torch.Tensor] = None, stream=None):
+    """(E, N, K) bf16 -> q (E, K, N) uint8 [per-expert column-major data],
+    s (E, N/32, K) uint8 scales."""
+    if x.dtype != torch.bfloat16 or x.dim() != 3 or not x.is_contiguous() or not x.is_cuda:
+        raise ValueError("x must be a contiguous (E, N, K) bf16 CUDA tensor")
+    E, N, K = x.shape
+    if q is None:
+        q = torch.empty((E, K, N), dtype=torch.uint8, device=x.device)
+    if s is None:
+        s = torch.empty((E, N // 32, K), dtype=torch.uint8, device=x.device)
+    check(capi.mxfp8_quant_3d_colwise(x.data_ptr(), E, N, K, q.data_ptr(), s.data_ptr(),
+                                      _stream(stream)), "mxfp8_quant_3d_colwise")
+    return q, s
+
+
+def device_status(reset: bool = False, stream=None):
+    """(flags, fallbacks) of the current device; synchronizes the stream."""
+    st, flags, n = capi.mxfp8_device_status(reset, _stream(stream))
+    check(st, "mxfp8_device_status")
+    return flags, n

@@ -1,0 +1,482 @@
+// api.cu -- the C ABI of libmxfp8 (declared in include/mxfp8.h): argument
+// validation on the host, TMA descriptor encoding, per-device set-up, launch.
+//
+// Every argument check runs before anything touches the CUDA runtime, so a
+// rejected call returns a status code without side effects (and can be made
+// on a machine without a GPU).
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "launch.cuh"
+#include "mxfp8.h"
+
+namespace {
+
+using mx::KernelArgs;
+
+// ----------------------------------------------------- device-side state
+// Read-only sigmoid table (double, one entry per bf16 bit pattern), sticky
+// status bits and the count of elements settled by the double path.  Each
+// device that loads the library holds its own copy.
+__device__ double g_sig_table[65536];
+__device__ unsigned g_status;
+__device__ unsigned long long g_fallbacks;
+
+__global__ void init_sigmoid_table_kernel(double *table)
+{
+    const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= 65536u) return;
+    const double g = static_cast<double>(__uint_as_float(i << 16));
+    table[i] = __drcp_rn(__dadd_rn(1.0, exp(-g)));  // 1 / (1 + e^-g)
+}
+
+__global__ void selftest_wait_kernel(unsigned *status, long long limit)
+{
+    __shared__ uint64_t bar;
+    const uint32_t b = mx::smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mx::mbar_init(b, 1);
+        mx::fence_barrier_init();
+    }
+    __syncthreads();
+    // nobody ever arrives: phase 0 never completes
+    if (!mx::mbar_wait_bounded(b, 0u, limit)) atomicOr(status, mx::kStatusSelftestWait);
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    std::atomic<bool> ready{false};
+    double *table = nullptr;
+    unsigned *status = nullptr;
+    unsigned long long *fallbacks = nullptr;
+    int sms = 0;
+    long long wait_limit = 0;
+};
+
+DeviceState g_dev[kMaxDevices];
+std::mutex g_init_mutex;
+
+mxfp8_status ensure_device(cudaStream_t stream, int *dev_out, DeviceState **state)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MXFP8_ERR_DEVICE;
+    DeviceState &d = g_dev[dev];
+    *dev_out = dev;
+    *state = &d;
+    if (d.ready.load(std::memory_order_acquire)) return MXFP8_OK;
+    std::lock_guard<std::mutex> lock(g_init_mutex);
+    if (d.ready.load(std::memory_order_acquire)) return MXFP8_OK;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+        return MXFP8_ERR_CAPTURE;
+    int major = 0, minor = 0, sms = 0, clock_khz = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return MXFP8_ERR_DEVICE;
+    if (major != 10 || minor != 3) return MXFP8_ERR_DEVICE;  // built for sm_103a only
+    if (cudaDeviceGetAttribute(&clock_khz, cudaDevAttrClockRate, dev) != cudaSuccess || clock_khz <= 0)
+        clock_khz = 2000000;
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_sig_table) != cudaSuccess) return MXFP8_ERR_DEVICE;
+    d.table = static_cast<double *>(p);
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return MXFP8_ERR_DEVICE;
+    d.status = static_cast<unsigned *>(p);
+    if (cudaGetSymbolAddress(&p, g_fallbacks) != cudaSuccess) return MXFP8_ERR_DEVICE;
+    d.fallbacks = static_cast<unsigned long long *>(p);
+    init_sigmoid_table_kernel<<<256, 256, 0, stream>>>(d.table);
+    if (cudaGetLastError() != cudaSuccess) return MXFP8_ERR_DEVICE;
+    if (cudaMemsetAsync(d.status, 0, sizeof(unsigned), stream) != cudaSuccess ||
+        cudaMemsetAsync(d.fallbacks, 0, sizeof(unsigned long long), stream) != cudaSuccess)
+        return MXFP8_ERR_DEVICE;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MXFP8_ERR_DEVICE;
+    d.sms = sms;
+    d.wait_limit = static_cast<long long>(clock_khz) * 1000;  // about one second of SM clock
+    d.ready.store(true, std::memory_order_release);
+    return MXFP8_OK;
+}
+
+// --------------------------------------------------------- TMA descriptors
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder()
+{
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+// bf16 (rows, cols) with row pitch ld elements, boxes of 128 rows x 64 cols,
+// 128-byte swizzle, zero fill outside the tensor.
+bool make_bf16_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64_t ld)
+{
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(mx::kTileN), static_cast<cuuint32_t>(mx::kTileM)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// --------------------------------------------------------------- checking
+struct Region {        // rows of `width` bytes, `pitch` bytes apart
+    uintptr_t base;
+    int64_t rows, width, pitch;
+    bool used;
+};
+
+Region region(const void *p, int64_t rows, int64_t cols, int64_t ld, int64_t elem)
+{
+    return Region{reinterpret_cast<uintptr_t>(p), rows, cols * elem, ld * elem, p != nullptr};
+}
+
+int64_t floordiv(int64_t a, int64_t b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
+
+// Do two strided byte regions share a byte?  Exact when the pitches are
+// equal, conservative (extent overlap) otherwise.
+bool regions_overlap(const Region &a, const Region &b)
+{
+    if (!a.used || !b.used || a.rows <= 0 || b.rows <= 0) return false;
+    const int64_t a_end = static_cast<int64_t>(a.base) + (a.rows - 1) * a.pitch + a.width;
+    const int64_t b_end = static_cast<int64_t>(b.base) + (b.rows - 1) * b.pitch + b.width;
+    if (a_end <= static_cast<int64_t>(b.base) || b_end <= static_cast<int64_t>(a.base)) return false;
+    if (a.pitch != b.pitch || a.width > a.pitch || b.width > b.pitch) return true;
+    const int64_t L = a.pitch;
+    const int64_t d = static_cast<int64_t>(b.base) - static_cast<int64_t>(a.base);
+    const int64_t k = floordiv(d, L);
+    const int64_t r = d - k * L;  // 0 <= r < L
+    // B row j starts r bytes into A's pitch window j + k
+    const bool same_window = r < a.width && k < a.rows && k + b.rows > 0;
+    const bool next_window = r + b.width > L && k + 1 < a.rows && k + 1 + b.rows > 0;
+    return same_window || next_window;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool mul_ok(int64_t a, int64_t b, int64_t *out) { return !__builtin_mul_overflow(a, b, out); }
+
+// extent check: (rows - 1) * ld + cols fits in int64 (and as bytes * elem)
+bool extent_ok(int64_t rows, int64_t cols, int64_t ld, int64_t elem)
+{
+    int64_t t;
+    if (!mul_ok(rows, ld, &t)) return false;
+    if (__builtin_add_overflow(t, cols, &t)) return false;
+    return mul_ok(t, elem, &t);
+}
+
+constexpr int64_t kMaxDim = 0x7FFFFF00LL;  // TMA coordinates are signed 32-bit
+
+struct Spec {
+    int op;               // mx::kQuant / kFwd / kBwd
+    int mode;
+    int64_t M, N;
+    const void *in[3];
+    int64_t ld_in[3];
+    uint8_t *q_row[2], *s_row[2], *q_col[2], *s_col[2];
+    int64_t ld_qrow, ld_srow, ld_qcol, ld_scol;
+    int64_t group_rows, group_stride;
+};
+
+mxfp8_status validate(const Spec &s)
+{
+    const int nin = s.op == mx::kQuant ? 1 : (s.op == mx::kFwd ? 2 : 3);
+    const int nout = s.op == mx::kBwd ? 2 : 1;
+    if (s.mode < 1 || s.mode > 3) return MXFP8_ERR_MODE;
+    if (s.M < 0 || s.N < 0) return MXFP8_ERR_SHAPE;
+    if (s.M == 0 || s.N == 0) return MXFP8_OK;
+    if (s.M > kMaxDim || s.N > kMaxDim) return MXFP8_ERR_SHAPE;
+    const bool row = s.mode & 1, col = s.mode & 2;
+    if (row && s.N % 32 != 0) return MXFP8_ERR_SHAPE;
+    if (col && s.M % 32 != 0) return MXFP8_ERR_SHAPE;
+    for (int i = 0; i < nin; ++i) {
+        if (!s.in[i]) return MXFP8_ERR_NULL;
+    }
+    for (int o = 0; o < nout; ++o) {
+        if (row && (!s.q_row[o] || !s.s_row[o])) return MXFP8_ERR_NULL;
+        if (col && (!s.q_col[o] || !s.s_col[o])) return MXFP8_ERR_NULL;
+    }
+    for (int i = 0; i < nin; ++i) {
+        if (s.ld_in[i] < s.N) return MXFP8_ERR_LD;
+        if (!extent_ok(s.M, s.N, s.ld_in[i], 2) || s.ld_in[i] > (int64_t(1) << 38)) return MXFP8_ERR_SHAPE;
+        if (!aligned16(s.in[i]) || (s.ld_in[i] * 2) % 16 != 0) return MXFP8_ERR_ALIGN;
+    }
+    if (row) {
+        if (s.ld_qrow < s.N || s.ld_srow < s.N / 32) return MXFP8_ERR_LD;
+        if (!extent_ok(s.M, s.N, s.ld_qrow, 1) || !extent_ok(s.M, s.N / 32, s.ld_srow, 1))
+            return MXFP8_ERR_SHAPE;
+        if (s.ld_qrow % 16 != 0) return MXFP8_ERR_ALIGN;
+        for (int o = 0; o < nout; ++o)
+            if (!aligned16(s.q_row[o])) return MXFP8_ERR_ALIGN;
+    }
+    if (col) {
+        if (s.group_stride == 0) {  // 2D column-major
+            if (s.ld_qcol < s.M || s.ld_scol < s.N) return MXFP8_ERR_LD;
+            if (!extent_ok(s.N, s.M, s.ld_qcol, 1) || !extent_ok(s.M / 32, s.N, s.ld_scol, 1))
+                return MXFP8_ERR_SHAPE;
+        }
+        if (s.ld_qcol % 16 != 0) return MXFP8_ERR_ALIGN;
+        for (int o = 0; o < nout; ++o)
+            if (!aligned16(s.q_col[o])) return MXFP8_ERR_ALIGN;
+    }
+    // overlap: outputs against inputs and against each other
+    Region ins[3], outs[8];
+    int n_outs = 0;
+    for (int i = 0; i < nin; ++i) ins[i] = region(s.in[i], s.M, s.N, s.ld_in[i], 2);
+    for (int o = 0; o < nout; ++o) {
+        if (row) {
+            outs[n_outs++] = region(s.q_row[o], s.M, s.N, s.ld_qrow, 1);
+            outs[n_outs++] = region(s.s_row[o], s.M, s.N / 32, s.ld_srow, 1);
+        }
+        if (col) {
+            if (s.group_stride == 0) {
+                outs[n_outs++] = region(s.q_col[o], s.N, s.M, s.ld_qcol, 1);
+            } else {  // 3D: E * K rows of N bytes
+                const int64_t E = s.M / s.group_rows;
+                outs[n_outs++] = region(s.q_col[o], E * s.N, s.group_rows, s.ld_qcol, 1);
+            }
+            outs[n_outs++] = region(s.s_col[o], s.M / 32, s.N, s.ld_scol, 1);
+        }
+    }
+    for (int a = 0; a < n_outs; ++a) {
+        for (int i = 0; i < nin; ++i)
+            if (regions_overlap(outs[a], ins[i])) return MXFP8_ERR_OVERLAP;
+        for (int b = a + 1; b < n_outs; ++b)
+            if (regions_overlap(outs[a], outs[b])) return MXFP8_ERR_OVERLAP;
+    }
+    return MXFP8_OK;
+}
+
+mxfp8_status run(const Spec &s, void *stream_ptr)
+{
+    mxfp8_status st = validate(s);
+    if (st != MXFP8_OK || s.M == 0 || s.N == 0) return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    int dev = -1;
+    DeviceState *d = nullptr;
+    st = ensure_device(stream, &dev, &d);
+    if (st != MXFP8_OK) return st;
+    if (!get_encoder()) return MXFP8_ERR_DEVICE;
+    const int nin = s.op == mx::kQuant ? 1 : (s.op == mx::kFwd ? 2 : 3);
+    CUtensorMap maps[3];
+    std::memset(maps, 0, sizeof(maps));
+    for (int i = 0; i < 3; ++i) {
+        const int src = i < nin ? i : 0;
+        if (!make_bf16_map(&maps[i], s.in[src], s.M, s.N, s.ld_in[src])) return MXFP8_ERR_ALIGN;
+    }
+    KernelArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.M = s.M;
+    a.N = s.N;
+    a.tiles_n = (s.N + mx::kTileN - 1) / mx::kTileN;
+    a.num_tiles = ((s.M + mx::kTileM - 1) / mx::kTileM) * a.tiles_n;
+    for (int o = 0; o < 2; ++o) {
+        a.q_row[o] = s.q_row[o];
+        a.s_row[o] = s.s_row[o];
+        a.q_col[o] = s.q_col[o];
+        a.s_col[o] = s.s_col[o];
+    }
+    a.ld_qrow = s.ld_qrow;
+    a.ld_srow = s.ld_srow;
+    a.ld_qcol = s.ld_qcol;
+    a.ld_scol = s.ld_scol;
+    a.group_rows = s.group_rows > 0 ? s.group_rows : s.M;
+    a.group_stride = s.group_stride;
+    a.sig_table = d->table;
+    a.status = d->status;
+    a.fallbacks = d->fallbacks;
+    a.wait_limit = d->wait_limit;
+    const int grid = static_cast<int>(a.num_tiles < d->sms ? a.num_tiles : d->sms);
+    cudaError_t e;
+    switch (s.op) {
+    case mx::kQuant: e = mx::launch_quant(s.mode, maps, a, grid, stream, dev); break;
+    case mx::kFwd: e = mx::launch_fwd(s.mode, maps, a, grid, stream, dev); break;
+    default: e = mx::launch_bwd(s.mode, maps, a, grid, stream, dev); break;
+    }
+    return e == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
+}
+
+Spec blank(int op, int mode, int64_t M, int64_t N)
+{
+    Spec s;
+    std::memset(&s, 0, sizeof(s));
+    s.op = op;
+    s.mode = mode;
+    s.M = M;
+    s.N = N;
+    return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *mxfp8_status_str(mxfp8_status s)
+{
+    switch (s) {
+    case MXFP8_OK: return "MXFP8_OK";
+    case MXFP8_ERR_NULL: return "MXFP8_ERR_NULL: a required pointer is NULL";
+    case MXFP8_ERR_SHAPE: return "MXFP8_ERR_SHAPE: invalid or unsupported shape";
+    case MXFP8_ERR_ALIGN: return "MXFP8_ERR_ALIGN: misaligned pointer or leading dimension";
+    case MXFP8_ERR_LD: return "MXFP8_ERR_LD: leading dimension too small";
+    case MXFP8_ERR_MODE: return "MXFP8_ERR_MODE: scale mode must be 1, 2 or 3";
+    case MXFP8_ERR_OVERLAP: return "MXFP8_ERR_OVERLAP: an output overlaps an input or another output";
+    case MXFP8_ERR_LAUNCH: return "MXFP8_ERR_LAUNCH: kernel launch failed";
+    case MXFP8_ERR_DEVICE: return "MXFP8_ERR_DEVICE: no usable sm_103 device or device set-up failed";
+    case MXFP8_ERR_CAPTURE: return "MXFP8_ERR_CAPTURE: first use of a device inside a stream capture";
+    }
+    return "MXFP8_ERR_UNKNOWN";
+}
+
+int mxfp8_version(void) { return 100; }
+
+mxfp8_status mxfp8_init(void *stream)
+{
+    int dev;
+    DeviceState *d;
+    return ensure_device(static_cast<cudaStream_t>(stream), &dev, &d);
+}
+
+mxfp8_status mxfp8_quant_2d(const uint16_t *x, int64_t ld_x, int64_t M, int64_t N, int mode,
+                            uint8_t *q_row, int64_t ld_qrow, uint8_t *s_row, int64_t ld_srow,
+                            uint8_t *q_col, int64_t ld_qcol, uint8_t *s_col, int64_t ld_scol,
+                            void *stream)
+{
+    Spec s = blank(mx::kQuant, mode, M, N);
+    s.in[0] = x;
+    s.ld_in[0] = ld_x;
+    s.q_row[0] = q_row;
+    s.s_row[0] = s_row;
+    s.q_col[0] = q_col;
+    s.s_col[0] = s_col;
+    s.ld_qrow = ld_qrow;
+    s.ld_srow = ld_srow;
+    s.ld_qcol = ld_qcol;
+    s.ld_scol = ld_scol;
+    return run(s, stream);
+}
+
+mxfp8_status mxfp8_swiglu_fwd(const uint16_t *gate, const uint16_t *up, int64_t ld_in, int64_t M,
+                              int64_t N, int mode, uint8_t *q_row, int64_t ld_qrow, uint8_t *s_row,
+                              int64_t ld_srow, uint8_t *q_col, int64_t ld_qcol, uint8_t *s_col,
+                              int64_t ld_scol, void *stream)
+{
+    Spec s = blank(mx::kFwd, mode, M, N);
+    s.in[0] = gate;
+    s.in[1] = up;
+    s.ld_in[0] = s.ld_in[1] = ld_in;
+    s.q_row[0] = q_row;
+    s.s_row[0] = s_row;
+    s.q_col[0] = q_col;
+    s.s_col[0] = s_col;
+    s.ld_qrow = ld_qrow;
+    s.ld_srow = ld_srow;
+    s.ld_qcol = ld_qcol;
+    s.ld_scol = ld_scol;
+    return run(s, stream);
+}
+
+mxfp8_status mxfp8_swiglu_bwd(const uint16_t *dh, int64_t ld_dh, const uint16_t *gate,
+                              const uint16_t *up, int64_t ld_in, int64_t M, int64_t N, int mode,
+                              uint8_t *dg_row, uint8_t *du_row, int64_t ld_qrow, uint8_t *dg_srow,
+                              uint8_t *du_srow, int64_t ld_srow, uint8_t *dg_col, uint8_t *du_col,
+                              int64_t ld_qcol, uint8_t *dg_scol, uint8_t *du_scol, int64_t ld_scol,
+                              void *stream)
+{
+    Spec s = blank(mx::kBwd, mode, M, N);
+    s.in[0] = dh;
+    s.in[1] = gate;
+    s.in[2] = up;
+    s.ld_in[0] = ld_dh;
+    s.ld_in[1] = s.ld_in[2] = ld_in;
+    s.q_row[0] = dg_row;
+    s.q_row[1] = du_row;
+    s.s_row[0] = dg_srow;
+    s.s_row[1] = du_srow;
+    s.q_col[0] = dg_col;
+    s.q_col[1] = du_col;
+    s.s_col[0] = dg_scol;
+    s.s_col[1] = du_scol;
+    s.ld_qrow = ld_qrow;
+    s.ld_srow = ld_srow;
+    s.ld_qcol = ld_qcol;
+    s.ld_scol = ld_scol;
+    return run(s, stream);
+}
+
+mxfp8_status mxfp8_quant_3d_colwise(const uint16_t *x, int64_t E, int64_t N, int64_t K, uint8_t *q,
+                                    uint8_t *s, void *stream)
+{
+    if (E < 0 || N < 0 || K < 0) return MXFP8_ERR_SHAPE;
+    if (E == 0 || N == 0 || K == 0) return MXFP8_OK;
+    if (N % 32 != 0) return MXFP8_ERR_SHAPE;
+    int64_t rows;
+    if (!mul_ok(E, N, &rows) || rows > kMaxDim || K > kMaxDim) return MXFP8_ERR_SHAPE;
+    if (K % 8 != 0) return MXFP8_ERR_ALIGN;
+    int64_t slab;
+    if (!mul_ok(N, K, &slab)) return MXFP8_ERR_SHAPE;
+    Spec sp = blank(mx::kQuant, MXFP8_COLWISE, rows, K);
+    sp.in[0] = x;
+    sp.ld_in[0] = K;
+    sp.q_col[0] = q;
+    sp.s_col[0] = s;
+    sp.ld_qcol = N;       // within an expert: element (n, k) at k * N + n
+    sp.ld_scol = K;       // scales (E * N/32, K) row-major
+    sp.group_rows = N;
+    sp.group_stride = slab;
+    return run(sp, stream);
+}
+
+mxfp8_status mxfp8_device_status(uint32_t *flags, uint64_t *fallbacks, int reset, void *stream)
+{
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int dev;
+    DeviceState *d;
+    mxfp8_status r = ensure_device(st, &dev, &d);
+    if (r != MXFP8_OK) return r;
+    unsigned f = 0;
+    unsigned long long n = 0;
+    if (cudaMemcpyAsync(&f, d->status, sizeof f, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemcpyAsync(&n, d->fallbacks, sizeof n, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return MXFP8_ERR_DEVICE;
+    if (reset) {
+        if (cudaMemsetAsync(d->status, 0, sizeof(unsigned), st) != cudaSuccess ||
+            cudaMemsetAsync(d->fallbacks, 0, sizeof(unsigned long long), st) != cudaSuccess)
+            return MXFP8_ERR_DEVICE;
+    }
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MXFP8_ERR_DEVICE;
+    if (flags) *flags = f;
+    if (fallbacks) *fallbacks = n;
+    return MXFP8_OK;
+}
+
+mxfp8_status mxfp8_selftest_wait_timeout(uint64_t limit_cycles, void *stream)
+{
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int dev;
+    DeviceState *d;
+    mxfp8_status r = ensure_device(st, &dev, &d);
+    if (r != MXFP8_OK) return r;
+    const long long lim = limit_cycles > (1ull << 40) ? (1ll << 40) : static_cast<long long>(limit_cycles);
+    selftest_wait_kernel<<<1, 32, 0, st>>>(d->status, lim);
+    return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
+}
+
+}  // extern "C"

@@ -1,0 +1,7 @@
+// ops_fwd.cu -- instantiations of the tile kernel for the fwd op
+// (rowwise, colwise and both scale modes).
+#include "launch.cuh"
+
+namespace mx {
+MX_DEFINE_LAUNCH(launch_fwd, kFwd)
+}  // namespace mx

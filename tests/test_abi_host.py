@@ -1,0 +1,150 @@
+"""Host-side checks of the C ABI (no GPU needed, nothing is launched).
+
+* the library loads and exports every function include/mxfp8.h declares;
+* every argument error returns its status code before the CUDA runtime is
+  touched ("Add swiglu + MXFP8 fused CuTe DSL kernel", section "Numerics
+  and tests": every launcher error path exercised), with fake pointers;
+* calls that pass validation reach device set-up, which on a machine
+  without a GPU reports MXFP8_ERR_DEVICE (only run where no GPU is present,
+  since there the fake pointers would be launched on).
+"""
+import os
+import re
+
+import pytest
+import torch
+
+from mxfp8_quantization_moe_gb300 import capi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, NULL, SHAPE, ALIGN, LD, MODE, OVERLAP, LAUNCH, DEVICE = range(9)
+NO_GPU = not torch.cuda.is_available()
+
+X = 0x10000000          # fake, 16-byte aligned "device" addresses, far apart
+Q = 0x20000000
+S = 0x30000000
+QC = 0x40000000
+SC = 0x50000000
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "mxfp8.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mxfp8_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("mxfp8_swiglu_fwd", "mxfp8_swiglu_bwd", "mxfp8_quant_2d", "mxfp8_quant_3d_colwise"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = capi.lib()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in capi.SIGNATURES, name
+
+
+def test_status_strings_and_version():
+    for s in range(10):
+        assert capi.mxfp8_status_str(s).startswith("MXFP8_")
+    assert capi.mxfp8_version() >= 100
+
+
+def q2d(x=X, ld_x=256, M=128, N=256, mode=3, q_row=Q, ld_qrow=256, s_row=S, ld_srow=8,
+        q_col=QC, ld_qcol=128, s_col=SC, ld_scol=256):
+    return capi.mxfp8_quant_2d(x, ld_x, M, N, mode, q_row, ld_qrow, s_row, ld_srow,
+                               q_col, ld_qcol, s_col, ld_scol, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(mode=0), MODE), (dict(mode=4), MODE), (dict(mode=-1), MODE),
+    (dict(M=-1), SHAPE), (dict(N=-32), SHAPE),
+    (dict(N=48, ld_x=48, ld_qrow=48, mode=1), SHAPE),          # rowwise needs N % 32
+    (dict(M=100, mode=2), SHAPE),                                # colwise needs M % 32
+    (dict(M=2 ** 31, mode=1), SHAPE),
+    (dict(x=0), NULL), (dict(q_row=0), NULL), (dict(s_row=0), NULL),
+    (dict(q_col=0), NULL), (dict(s_col=0), NULL),
+    (dict(x=X + 2), ALIGN), (dict(ld_x=260), ALIGN), (dict(q_row=Q + 8), ALIGN),
+    (dict(ld_qrow=264), ALIGN), (dict(q_col=QC + 4), ALIGN), (dict(ld_qcol=136), ALIGN),
+    (dict(ld_x=128), LD), (dict(ld_qrow=128), LD), (dict(ld_srow=4), LD),
+    (dict(ld_qcol=96), LD), (dict(ld_scol=128), LD),
+    (dict(q_row=X + 64), OVERLAP),                               # data over the input
+    (dict(s_col=Q + 100), OVERLAP),                              # scales inside q_row
+    (dict(q_col=Q + 4096), OVERLAP),                             # col data over row data
+])
+def test_quant_2d_argument_errors(kw, status):
+    assert q2d(**kw) == status
+
+
+def test_disabled_direction_pointers_are_ignored():
+    # rowwise-only call with garbage colwise arguments still fails only on the
+    # rowwise error it was given
+    assert q2d(mode=1, q_col=3, s_col=0, ld_qcol=-5, ld_scol=-5, x=0) == NULL
+    assert q2d(mode=2, q_row=3, s_row=0, ld_qrow=-5, ld_srow=-5, ld_x=260) == ALIGN
+
+
+@pytest.mark.parametrize("kw", [dict(M=0), dict(N=0), dict(M=0, x=0, q_row=0)])
+def test_empty_calls_succeed_without_device(kw):
+    assert q2d(**kw) == OK
+
+
+def _bwd_rowwise(du_off, base=0x20000000, sb=0x30000000, M=64, N=128):
+    return capi.mxfp8_swiglu_bwd(X, N, X + 0x1000000, X + 0x1000000 + 2 * N, 2 * N, M, N, 1,
+                                 base, base + du_off, 2 * N, sb, sb + N // 32, N // 16,
+                                 None, None, 0, None, None, 0, None)
+
+
+def test_overlap_check_is_exact_for_interleaved_layouts():
+    N = 128
+    # shifting dUp by 16 bytes into dGate's rows is an overlap
+    assert _bwd_rowwise(N - 16) == OVERLAP
+    # dUp's row end wrapping into the next dGate row
+    assert _bwd_rowwise(N + 16) == OVERLAP
+
+
+@pytest.mark.skipif(not NO_GPU, reason="would launch on fake pointers")
+def test_interleaved_dgate_dup_halves_pass_validation():
+    # rowwise outputs of two tensors interleaved in one buffer ([dGate | dUp])
+    assert _bwd_rowwise(128) == DEVICE
+
+
+@pytest.mark.skipif(not NO_GPU, reason="would launch on fake pointers")
+def test_valid_calls_reach_device_setup():
+    assert q2d() == DEVICE
+    assert capi.mxfp8_init(None) == DEVICE
+
+
+def test_fwd_and_bwd_argument_errors():
+    f = capi.mxfp8_swiglu_fwd
+    assert f(X, 0, 512, 64, 256, 1, Q, 256, S, 8, None, 0, None, 0, None) == NULL
+    assert f(X, X + 2, 512, 64, 256, 1, Q, 256, S, 8, None, 0, None, 0, None) == ALIGN
+    assert f(X, X + 256, 200, 64, 256, 1, Q, 256, S, 8, None, 0, None, 0, None) == LD
+    assert f(X, X + 256, 512, 64, 256, 1, X + 1024, 256, S, 8, None, 0, None, 0, None) == OVERLAP
+    b = capi.mxfp8_swiglu_bwd
+    assert b(0, 256, X, X + 256, 512, 64, 256, 1, Q, Q + 256, 512, S, S + 8, 16,
+             None, None, 0, None, None, 0, None) == NULL
+    assert b(X + 0x100000, 256, X, X + 256, 512, 64, 256, 1, Q, 0, 512, S, S + 8, 16,
+             None, None, 0, None, None, 0, None) == NULL
+    # [dGate | dUp] colwise halves, dUp shifted 16 bytes into dGate's last column
+    assert b(X + 0x100000, 256, X, X + 256, 512, 64, 256, 2, None, None, 0, None, None, 0,
+             QC, QC + 256 * 64 - 16, 64, SC, SC + 256, 512, None) == OVERLAP
+    if NO_GPU:   # valid packed layouts pass validation (fake pointers: never on a GPU)
+        assert f(X, X + 256, 512, 64, 256, 1, Q, 256, S, 8, None, 0, None, 0, None) == DEVICE
+        assert b(X + 0x100000, 256, X, X + 256, 512, 64, 256, 2, None, None, 0, None, None, 0,
+                 QC, QC + 256 * 64, 64, SC, SC + 256, 512, None) == DEVICE
+
+
+def test_3d_argument_errors():
+    f = capi.mxfp8_quant_3d_colwise
+    assert f(X, 2, 48, 64, Q, S, None) == SHAPE           # N % 32
+    assert f(X, 2, 64, 60, Q, S, None) == ALIGN           # K * 2 not a multiple of 16
+    assert f(X, -1, 64, 64, Q, S, None) == SHAPE
+    assert f(X, 0, 64, 64, Q, S, None) == OK              # empty
+    assert f(0, 2, 64, 64, Q, S, None) == NULL
+    assert f(X, 2, 64, 64, 0, S, None) == NULL
+    assert f(X, 2, 64, 64, Q + 8, S, None) == ALIGN
+    assert f(X, 2, 64, 64, X + 64, S, None) == OVERLAP    # data over the input
+    assert f(X, 2 ** 19, 8192, 64, Q, S, None) == SHAPE    # E * N beyond the TMA coordinate range

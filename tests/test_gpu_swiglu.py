@@ -1,0 +1,272 @@
+"""GPU parity of the fused SwiGLU + MXFP8 forward and backward.
+
+Tolerance (stated for the SwiGLU paths): E8M0 scales bit-exact; at most 1e-4
+of the E4M3 codes may differ from the oracle, each by at most one code.  The
+activation is rounded to bf16 once from an fp32-accurate value in both, so
+the expected number of differing codes is zero; the tests report it.
+
+Workloads: the packed (128, 128) forward; the (4096, 7168) mix of per-row
+2^k scaling and zeroed 32-blocks (full comparison); the (16384, 7168)
+outlier mix and the (131072, 8192) normal data compared on sampled 32-row
+blocks; every bf16 gate value; amax at the E4M3 boundary.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from gpu_util import Guarded, bits, compare_codes, u8
+from mxfp8_quantization_moe_gb300 import capi, device_status, synthetic
+
+pytestmark = pytest.mark.gpu
+
+CODE_TOL = 1e-4
+
+
+def _stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+def fwd_gpu(gate, up, mode, blocks=None):
+    """Run the fused forward; return host outputs (only the 32-row blocks in
+    `blocks` when given, gathered on the device)."""
+    M, N = gate.shape
+    o = {}
+    if mode & 1:
+        o["q_row"], o["s_row"] = Guarded((M, N)), Guarded((M, N // 32))
+    if mode & 2:
+        o["q_col"], o["s_col"] = Guarded((N, M)), Guarded((M // 32, N))
+    p = lambda k: o[k].t.data_ptr() if k in o else None
+    ld = lambda k: o[k].t.stride(0) if k in o else 0
+    st = capi.mxfp8_swiglu_fwd(gate.data_ptr(), up.data_ptr(), gate.stride(0), M, N, mode,
+                               p("q_row"), ld("q_row"), p("s_row"), ld("s_row"),
+                               p("q_col"), ld("q_col"), p("s_col"), ld("s_col"), _stream())
+    assert st == 0, capi.STATUS_NAMES[st]
+    torch.cuda.synchronize()
+    for k, g in o.items():
+        assert g.intact(), k
+    return gather({k: g.t for k, g in o.items()}, blocks)
+
+
+def gather(d, blocks):
+    """Device outputs -> host numpy, restricted to 32-row blocks if given."""
+    if blocks is None:
+        return {k: u8(t) for k, t in d.items()}
+    sel = torch.tensor(rows_of(blocks), device="cuda")
+    bl = torch.tensor(blocks, device="cuda")
+    out = {}
+    for k, t in d.items():
+        if k in ("q_row", "s_row"):
+            out[k] = u8(t.index_select(0, sel))
+        elif k == "q_col":
+            out[k] = u8(t.index_select(1, sel))
+        else:
+            out[k] = u8(t.index_select(0, bl))
+    return out
+
+
+def rows_of(blocks):
+    return np.concatenate([np.arange(32 * b, 32 * b + 32) for b in blocks]).tolist()
+
+
+def bwd_gpu(dh, gate, up, mode, blocks=None):
+    """Packed [dGate | dUp] outputs; returns per-tensor dicts (dgate, dup)."""
+    M, N = gate.shape
+    o = {}
+    if mode & 1:
+        o["q_row"], o["s_row"] = Guarded((M, 2 * N)), Guarded((M, 2 * N // 32))
+    if mode & 2:
+        o["q_col"], o["s_col"] = Guarded((2 * N, M)), Guarded((M // 32, 2 * N))
+    qr = o["q_row"].t.data_ptr() if mode & 1 else None
+    sr = o["s_row"].t.data_ptr() if mode & 1 else None
+    qc = o["q_col"].t.data_ptr() if mode & 2 else None
+    sc = o["s_col"].t.data_ptr() if mode & 2 else None
+    st = capi.mxfp8_swiglu_bwd(
+        dh.data_ptr(), dh.stride(0), gate.data_ptr(), up.data_ptr(), gate.stride(0), M, N, mode,
+        qr, qr + N if qr else None, 2 * N if qr else 0,
+        sr, sr + N // 32 if sr else None, N // 16 if sr else 0,
+        qc, qc + N * M if qc else None, M if qc else 0,
+        sc, sc + N if sc else None, 2 * N if sc else 0, _stream())
+    assert st == 0, capi.STATUS_NAMES[st]
+    torch.cuda.synchronize()
+    for k, g in o.items():
+        assert g.intact(), k
+    t = {k: g.t for k, g in o.items()}
+    dg, du = {}, {}
+    if mode & 1:
+        dg["q_row"], du["q_row"] = t["q_row"][:, :N], t["q_row"][:, N:]
+        dg["s_row"], du["s_row"] = t["s_row"][:, :N // 32], t["s_row"][:, N // 32:]
+    if mode & 2:
+        dg["q_col"], du["q_col"] = t["q_col"][:N], t["q_col"][N:]
+        dg["s_col"], du["s_col"] = t["s_col"][:, :N], t["s_col"][:, N:]
+    return gather(dg, blocks), gather(du, blocks)
+
+
+def compare(got, want, what=""):
+    """Scales bit-exact; codes within tolerance.  Returns differing codes."""
+    n = 0
+    for k in want:
+        g, w = np.ascontiguousarray(got[k]), np.ascontiguousarray(want[k])
+        if k.startswith("s_"):
+            assert np.array_equal(g, w), "%s %s: scales differ at %d places" % (what, k, int((g != w).sum()))
+        else:
+            n += compare_codes(g, w, CODE_TOL, what + " " + k)
+    return n
+
+
+def _host_rows(t, blocks):
+    if blocks is None:
+        return bits(t)
+    sel = torch.tensor(rows_of(blocks), device=t.device)
+    return bits(t.index_select(0, sel))
+
+
+def oracle_fwd(gate, up, mode, blocks=None):
+    """Oracle on the whole tensors, or on the stacked 32-row blocks."""
+    return O.swiglu_fwd(_host_rows(gate, blocks), _host_rows(up, blocks), mode)[0]
+
+
+def oracle_bwd(dh, gate, up, mode, blocks=None):
+    r = O.swiglu_bwd(_host_rows(dh, blocks), _host_rows(gate, blocks), _host_rows(up, blocks), mode)
+    return r[0], r[1]
+
+
+# ------------------------------------------------------------ small shapes
+
+def rand_inputs(M, N, seed, std=(2.0, 1.0, 0.05)):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    return [(torch.randn((M, N), generator=g, device="cuda") * s).to(torch.bfloat16) for s in std]
+
+
+@pytest.mark.parametrize("shape", [(32, 64), (160, 96), (256, 320), (1024, 576)], ids=lambda s: "%dx%d" % s)
+@pytest.mark.parametrize("mode", [1, 2, 3])
+def test_fwd_small(shape, mode):
+    gate, up, _ = rand_inputs(*shape, seed=shape[0] + mode)
+    got = fwd_gpu(gate, up, mode)
+    assert compare(got, oracle_fwd(gate, up, mode), what="fwd") == 0
+
+
+@pytest.mark.parametrize("shape", [(32, 64), (160, 96), (256, 320), (1024, 576)], ids=lambda s: "%dx%d" % s)
+@pytest.mark.parametrize("mode", [1, 2, 3])
+def test_bwd_small(shape, mode):
+    gate, up, dh = rand_inputs(*shape, seed=shape[1] + mode)
+    dg, du = bwd_gpu(dh, gate, up, mode)
+    wg, wu = oracle_bwd(dh, gate, up, mode)
+    assert compare(dg, wg, what="dgate") == 0
+    assert compare(du, wu, what="dup") == 0
+
+
+def test_fwd_packed_128x128_rowwise():
+    """The (128, 128) forward of the pages' sweep, [gate | up] in one buffer."""
+    buf, gate, up = synthetic.fwd_128x128(device="cuda")
+    for mode in (1, 2, 3):
+        got = fwd_gpu(gate, up, mode)
+        assert compare(got, oracle_fwd(gate, up, mode), what="fwd128") == 0
+
+
+# ----------------------------------------------------------- every gate
+
+def every_gate(rows=512):
+    v = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(rows, 65536 // rows)
+    return torch.from_numpy(v.view(np.int16)).cuda().view(torch.bfloat16)
+
+
+@pytest.mark.parametrize("useed", [0, 1, 2])
+def test_fwd_every_bf16_gate(useed):
+    gate = every_gate()
+    g = torch.Generator(device="cuda").manual_seed(100 + useed)
+    up = (torch.randn(gate.shape, generator=g, device="cuda") *
+          (1.0 if useed < 2 else 1e3)).to(torch.bfloat16)
+    if useed == 1:
+        up.fill_(1.0)
+    for mode in (1, 2):
+        got = fwd_gpu(gate, up, mode)
+        assert compare(got, oracle_fwd(gate, up, mode), what="fwd-all-g") == 0
+
+
+@pytest.mark.parametrize("useed", [0, 1])
+def test_bwd_every_bf16_gate(useed):
+    gate = every_gate()
+    g = torch.Generator(device="cuda").manual_seed(200 + useed)
+    up = torch.randn(gate.shape, generator=g, device="cuda").to(torch.bfloat16)
+    dh = (torch.randn(gate.shape, generator=g, device="cuda") * 0.01).to(torch.bfloat16)
+    if useed == 1:
+        up.fill_(1.0)
+        dh.fill_(1.0)
+    for mode in (1, 2):
+        dg, du = bwd_gpu(dh, gate, up, mode)
+        wg, wu = oracle_bwd(dh, gate, up, mode)
+        assert compare(dg, wg, what="dgate-all-g") == 0
+        assert compare(du, wu, what="dup-all-g") == 0
+
+
+def test_fwd_amax_at_e4m3_boundary():
+    """Blocks whose largest h sits next to 448 * 2^k: the scale byte flips
+    there, so the bf16 rounding of h must match exactly."""
+    M, N = 512, 256
+    g = torch.Generator(device="cuda").manual_seed(7)
+    gate = (torch.rand((M, N), generator=g, device="cuda") * 6 - 1).to(torch.bfloat16)
+    up = (torch.randn((M, N), generator=g, device="cuda") * 0.1).to(torch.bfloat16)
+    gf = gate.float()
+    silu = gf * torch.sigmoid(gf)
+    k = torch.randint(-10, 10, (M, N // 32), generator=g, device="cuda").float()
+    target = 448.0 * torch.pow(2.0, k) * (1 + (torch.rand((M, N // 32), generator=g, device="cuda") - 0.5) * 0.02)
+    pos = torch.randint(0, 32, (M, N // 32), generator=g, device="cuda")
+    cols = torch.arange(N // 32, device="cuda") * 32 + pos
+    rows = torch.arange(M, device="cuda")[:, None].expand_as(cols)
+    s = silu[rows, cols]
+    ok = s.abs() > 0.05
+    u_new = torch.where(ok, target / s, up[rows, cols].float())
+    up[rows, cols] = u_new.to(torch.bfloat16)
+    for mode in (1, 2, 3):
+        got = fwd_gpu(gate, up, mode)
+        assert compare(got, oracle_fwd(gate, up, mode), what="fwd-boundary") == 0
+
+
+# ------------------------------------------------------- pages' workloads
+
+def test_mixed_4096x7168_both_full():
+    gate, up, dh = synthetic.mixed(device="cuda")
+    got = fwd_gpu(gate, up, 3)
+    n = compare(got, oracle_fwd(gate, up, 3), what="mixed fwd")
+    dg, du = bwd_gpu(dh, gate, up, 3)
+    wg, wu = oracle_bwd(dh, gate, up, 3)
+    n += compare(dg, wg, what="mixed dgate") + compare(du, wu, what="mixed dup")
+    assert n == 0
+
+
+def sample_blocks(M, count, seed):
+    rng = np.random.default_rng(seed)
+    nb = M // 32
+    pick = set(rng.choice(nb, size=min(count, nb), replace=False).tolist()) | {0, nb - 1}
+    return sorted(pick)
+
+
+@pytest.mark.parametrize("mode", [1, 2, 3])
+def test_outlier_16384x7168_sampled(mode):
+    gate, up, dh = synthetic.outlier(device="cuda")
+    rows = sample_blocks(gate.shape[0], 24, mode)
+    got = fwd_gpu(gate, up, mode, rows)
+    n = compare(got, oracle_fwd(gate, up, mode, rows), what="outlier fwd")
+    dg, du = bwd_gpu(dh, gate, up, mode, rows)
+    wg, wu = oracle_bwd(dh, gate, up, mode, rows)
+    n += compare(dg, wg, what="outlier dgate") + compare(du, wu, what="outlier dup")
+    assert n == 0
+
+
+@pytest.mark.parametrize("mode", [1, 2, 3])
+def test_large_131072x8192_sampled(mode):
+    gate, up, dh = synthetic.large(device="cuda")
+    rows = sample_blocks(gate.shape[0], 8, 10 + mode)
+    got = fwd_gpu(gate, up, mode, rows)
+    n = compare(got, oracle_fwd(gate, up, mode, rows), what="large fwd")
+    dg, du = bwd_gpu(dh, gate, up, mode, rows)
+    wg, wu = oracle_bwd(dh, gate, up, mode, rows)
+    n += compare(dg, wg, what="large dgate") + compare(du, wu, what="large dup")
+    assert n == 0
+
+
+def test_status_clean_and_fallback_path_used():
+    flags, fallbacks = device_status()
+    assert flags == 0
+    assert fallbacks > 0      # the every-gate tests exercise the double path
