@@ -1,6 +1,7 @@
 """Build libmxfp8.so in-tree with nvcc for sm_103a.
 
-Usage: ``python -m mxfp8_quantization_moe_gb300.build [--verbose]``.
+Usage: ``python mxfp8_quantization_moe_gb300/build.py [--verbose]`` (run as a
+script: importing the package needs the library this builds).
 The translation units are compiled in parallel and linked with the static
 CUDA runtime; the result is ``mxfp8_quantization_moe_gb300/lib/libmxfp8.so``.
 """
