@@ -206,6 +206,11 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--ref-blocks", type=int, default=2)
+    ap.add_argument("--cell", default=None,
+                    help="time one cell only (fwd_row ... bwd_both, quant_row/col/both, quant3d) "
+                         "on --rows rows; prints per-launch microseconds (for profiling)")
+    ap.add_argument("--rows", type=int, default=M_LARGE)
+    ap.add_argument("--experts", type=int, default=64)
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -214,6 +219,8 @@ def main():
 
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.cell:
+        return run_cell(args)
 
     import torch
     import torch.distributed as dist
@@ -332,6 +339,58 @@ def main():
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def run_cell(args):
+    """Time one kernel alone (used for ncu captures and tuning sweeps)."""
+    import torch
+    import mxfp8_quantization_moe_gb300 as mx
+    from mxfp8_quantization_moe_gb300 import synthetic
+    mx.init()
+    kind, _, mname = args.cell.partition("_")
+    mode = {"row": 1, "col": 2, "both": 3}.get(mname, 2)
+    if kind == "quant3d":
+        x = synthetic.experts(args.experts, device="cuda")
+        E, N, K = x.shape
+        q = torch.empty((E, K, N), dtype=torch.uint8, device="cuda")
+        s = torch.empty((E, N // 32, K), dtype=torch.uint8, device="cuda")
+        nbytes = E * N * K * 2 + E * N * K + E * N * K // 32
+        fn = lambda: mx.quant_3d_colwise(x, q, s)
+    else:
+        gate, up, dh = synthetic.large(M=args.rows, N=N_LARGE, device="cuda")
+        M, N = gate.shape
+        if kind == "quant":
+            out = mx._alloc(M, N, mode, gate.device)
+            k = 2 if mode == 3 else 1
+            nbytes = 2 * M * N + k * (M * N + M * N // 32)
+            fn = lambda: mx.quant_2d(gate, mode, out=out)
+        elif kind == "fwd":
+            out = mx._alloc(M, N, mode, gate.device)
+            nbytes = cell_bytes("fwd", mode, M, N)
+            fn = lambda: mx.swiglu_fwd(gate, up, mode, out=out)
+        else:
+            out = mx.swiglu_bwd(dh, gate, up, mode)
+            nbytes = cell_bytes("bwd", mode, M, N)
+            fn = lambda: mx.swiglu_bwd(dh, gate, up, mode, out=out)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for a, b in evs:
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    us = [a.elapsed_time(b) * 1e3 for a, b in evs]
+    flags, fb = mx.device_status()
+    peak, _ = peaks()
+    med = statistics.median(us)
+    print(json.dumps({"cell": args.cell, "rows": args.rows, "us_median": round(med, 2),
+                      "us_min": round(min(us), 2), "GBps": round(nbytes / med / 1e3, 1),
+                      "frac_of_peak": round(nbytes / med / 1e3 / peak, 4), "bytes": nbytes,
+                      "flags": flags, "fallbacks": fb}), flush=True)
+    return 0 if flags == 0 else 1
 
 
 def run_e2e(args, mx, gate, up, dh, fwd_out, bwd_out, launch, barrier, world):

@@ -157,6 +157,17 @@ mxfp8_status mxfp8_quant_3d_colwise(const uint16_t *x, int64_t E, int64_t N, int
 mxfp8_status mxfp8_device_status(uint32_t *flags, uint64_t *fallbacks, int reset, void *stream);
 
 /*
+ * Self-test of the SwiGLU fast path: writes, for every bf16 bit pattern g
+ * (index g), the fp32 values the kernels use -- out[k*65536 + g] for
+ * k = 0 sigmoid(g), 1 silu(g), 2 1 - sigmoid(g), 3 1 + g(1 - sigmoid(g)),
+ * 4 silu'(g) -- and the rounding-guard thresholds in fp32 ulps for h (k = 5),
+ * dup (6) and dgate (7).  `out` is a device buffer of 8 * 65536 floats,
+ * 16-byte aligned.  The tests compare these with the exact factors to show
+ * that every guard bounds the fast path's error.
+ */
+mxfp8_status mxfp8_selftest_activation(float *out, void *stream);
+
+/*
  * Failure-detection self-test: launches one thread that waits on a shared
  * memory barrier nobody arrives on, giving up after `limit_cycles` SM clock
  * cycles; it then sets status bit 3 and returns.  Used by the tests to show

@@ -40,6 +40,7 @@ SIGNATURES = {
     "mxfp8_device_status": (_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint64),
                                    _int, _vp]),
     "mxfp8_selftest_wait_timeout": (_int, [_u64, _vp]),
+    "mxfp8_selftest_activation": (_int, [_vp, _vp]),
 }
 
 
@@ -119,3 +120,7 @@ def mxfp8_device_status(reset: bool, stream):
 
 def mxfp8_selftest_wait_timeout(limit_cycles: int, stream) -> int:
     return _lib.mxfp8_selftest_wait_timeout(limit_cycles, stream)
+
+
+def mxfp8_selftest_activation(out, stream) -> int:
+    return _lib.mxfp8_selftest_activation(out, stream)

@@ -50,6 +50,29 @@ __global__ void selftest_wait_kernel(unsigned *status, long long limit)
     if (!mx::mbar_wait_bounded(b, 0u, limit)) atomicOr(status, mx::kStatusSelftestWait);
 }
 
+// The fast-path activation factors for every bf16 gate value, computed by the
+// same device functions the tile kernels inline: out[k * 65536 + g] for
+// k = 0 sigmoid, 1 silu, 2 1-sigmoid, 3 w = 1 + g(1-sigmoid), 4 silu',
+// 5..7 the rounding-guard thresholds (ulps) used for h, dup and dgate.
+__global__ void selftest_activation_kernel(float *out)
+{
+    const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= 65536u) return;
+    const float g = __uint_as_float(i << 16);
+    float t;
+    const float s = mx::sigmoid_fast(g, t);
+    const float sn = __fmul_rn(t, s);
+    const float w = __fmaf_rn(g, sn, 1.0f);
+    out[0 * 65536 + i] = s;
+    out[1 * 65536 + i] = __fmul_rn(g, s);
+    out[2 * 65536 + i] = sn;
+    out[3 * 65536 + i] = w;
+    out[4 * 65536 + i] = __fmul_rn(s, w);
+    out[5 * 65536 + i] = mx::kFwdUlps;
+    out[6 * 65536 + i] = mx::kDupUlps;
+    out[7 * 65536 + i] = mx::dgate_guard_ulps(g, sn, w);
+}
+
 constexpr int kMaxDevices = 64;
 
 struct DeviceState {
@@ -465,6 +488,19 @@ mxfp8_status mxfp8_device_status(uint32_t *flags, uint64_t *fallbacks, int reset
     if (flags) *flags = f;
     if (fallbacks) *fallbacks = n;
     return MXFP8_OK;
+}
+
+mxfp8_status mxfp8_selftest_activation(float *out, void *stream)
+{
+    if (!out) return MXFP8_ERR_NULL;
+    if (!aligned16(out)) return MXFP8_ERR_ALIGN;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int dev;
+    DeviceState *d;
+    mxfp8_status r = ensure_device(st, &dev, &d);
+    if (r != MXFP8_OK) return r;
+    selftest_activation_kernel<<<256, 256, 0, st>>>(out);
+    return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
 }
 
 mxfp8_status mxfp8_selftest_wait_timeout(uint64_t limit_cycles, void *stream)
