@@ -51,26 +51,32 @@ __global__ void selftest_wait_kernel(unsigned *status, long long limit)
 }
 
 // The fast-path activation factors for every bf16 gate value, computed by the
-// same device functions the tile kernels inline: out[k * 65536 + g] for
-// k = 0 sigmoid, 1 silu, 2 1-sigmoid, 3 w = 1 + g(1-sigmoid), 4 silu',
-// 5..7 the rounding-guard thresholds (ulps) used for h, dup and dgate.
+// same device functions the tile kernels inline (on pairs of adjacent
+// patterns): out[k * 65536 + g] for k = 0 sigmoid, 1 silu, 2 1-sigmoid,
+// 3 w = 1 + g(1-sigmoid), 4 silu', 5..7 the rounding guards (ulps) used for
+// h, dup and dgate.
 __global__ void selftest_activation_kernel(float *out)
 {
-    const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+    const uint32_t i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
     if (i >= 65536u) return;
-    const float g = __uint_as_float(i << 16);
-    float t;
-    const float s = mx::sigmoid_fast(g, t);
-    const float sn = __fmul_rn(t, s);
-    const float w = __fmaf_rn(g, sn, 1.0f);
-    out[0 * 65536 + i] = s;
-    out[1 * 65536 + i] = __fmul_rn(g, s);
-    out[2 * 65536 + i] = sn;
-    out[3 * 65536 + i] = w;
-    out[4 * 65536 + i] = __fmul_rn(s, w);
-    out[5 * 65536 + i] = mx::kFwdUlps;
-    out[6 * 65536 + i] = mx::kDupUlps;
-    out[7 * 65536 + i] = mx::dgate_guard_ulps(g, sn, w);
+    const uint64_t G = mx::f2(__uint_as_float(i << 16), __uint_as_float((i + 1) << 16));
+    uint64_t T;
+    const uint64_t S = mx::sigmoid2(G, T);
+    const uint64_t SN = mx::mul2(T, S);
+    const uint64_t W = mx::fma2(G, SN, mx::f2(1.0f, 1.0f));
+    const uint64_t V[5] = {S, mx::mul2(G, S), SN, W, mx::mul2(S, W)};
+    for (int k = 0; k < 5; ++k) {
+        out[k * 65536 + i] = mx::f2lo(V[k]);
+        out[k * 65536 + i + 1] = mx::f2hi(V[k]);
+    }
+    const uint64_t KG = mx::dgate_guard2(W);
+    for (int j = 0; j < 2; ++j) {
+        out[5 * 65536 + i + j] = static_cast<float>(mx::kFwdUlps);
+        out[6 * 65536 + i + j] = static_cast<float>(mx::kDupUlps);
+    }
+    // the integer guard the kernels derive from the float threshold
+    out[7 * 65536 + i] = static_cast<float>(__float_as_uint(__fadd_rn(mx::f2lo(KG), 8388609.0f)) - 0x4B000000u);
+    out[7 * 65536 + i + 1] = static_cast<float>(__float_as_uint(__fadd_rn(mx::f2hi(KG), 8388609.0f)) - 0x4B000000u);
 }
 
 constexpr int kMaxDevices = 64;
@@ -499,7 +505,7 @@ mxfp8_status mxfp8_selftest_activation(float *out, void *stream)
     DeviceState *d;
     mxfp8_status r = ensure_device(st, &dev, &d);
     if (r != MXFP8_OK) return r;
-    selftest_activation_kernel<<<256, 256, 0, st>>>(out);
+    selftest_activation_kernel<<<128, 256, 0, st>>>(out);
     return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
 }
 

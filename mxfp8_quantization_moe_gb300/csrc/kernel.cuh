@@ -1,17 +1,17 @@
 // kernel.cuh -- the persistent tile kernel shared by every entry point.
 //
-// One CTA per SM.  Warp 8 is the producer: its lane 0 streams the input tiles
-// (128 rows x 64 bf16 columns per tensor, 128-byte swizzle) into a ring of
-// shared-memory stages with TMA, each stage guarded by a "full" mbarrier
-// (transaction bytes) and an "empty" mbarrier (one arrive per consumer warp).
-// Warps 0..7 are consumers; per tile they
-//   row pass  : each thread owns one 1x32 block (row 16w + lane/2, block
-//               lane%2), evaluates the element op from four 16-byte shared
-//               loads per input and encodes the rowwise MXFP8 block;
-//   col pass  : warp w owns the 8-column chunk w; ldmatrix.trans hands each
-//               group of four lanes one column of a 32-row block, which is
-//               encoded colwise and written as 8-byte pieces of the
-//               column-major output.
+// One CTA per SM, NW consumer warps plus one producer warp.  The producer's
+// lane 0 streams the input tiles (128 rows x 64 bf16 columns per tensor,
+// 128-byte swizzle) into a ring of shared-memory stages with TMA; each stage
+// has a "full" mbarrier (transaction bytes) and an "empty" mbarrier (one
+// arrive per consumer warp).  Per tile the consumers run
+//   row pass: a lane owns one 16-byte chunk (8 elements) of a row, four
+//             consecutive lanes one 1x32 block; the element op runs on the
+//             chunk, the block amax takes two shuffles, each lane stores 8
+//             E4M3 codes (the four lanes: 32 contiguous bytes);
+//   col pass: a warp owns one 32-row x 8-column unit; ldmatrix.trans gives
+//             four lanes one column of the unit, which is encoded colwise
+//             and stored as 8-byte pieces of the column-major output.
 // In "both" mode the row pass writes the bf16 element values back into the
 // stage (over an input it no longer needs) and a named barrier separates the
 // passes, so both scale sets come from one read of the inputs.  In "col" mode
@@ -42,10 +42,10 @@ struct OpTraits<kBwd> {
 };
 
 template <int OP>
-constexpr int default_stages()
-{
-    return OP == kQuant ? 8 : (OP == kFwd ? 4 : 3);
-}
+struct Tuning {
+    static constexpr int kWarps = 16;                         // consumer warps
+    static constexpr int kStages = OP == kQuant ? 8 : 4;
+};
 
 template <int OP, int STAGES>
 constexpr size_t smem_bytes()
@@ -53,167 +53,65 @@ constexpr size_t smem_bytes()
     return 1024 + static_cast<size_t>(STAGES) * OpTraits<OP>::kIn * kTileBytes + 2 * STAGES * 8;
 }
 
-// ------------------------------------------------------------- row pass op
-// Evaluate the element op for one thread's 32 elements (16 packed words per
-// input) into out[o][16].
+// ------------------------------------------------------- element operation
+// Evaluate the element op on 8 elements (4 packed bf16x2 words per input)
+// into out[o][4] (packed bf16x2 words).
 template <int OP>
-__device__ __forceinline__ void row_elements(const KernelArgs &a, const uint32_t (&in)[3][16],
-                                             uint32_t (&out)[2][16])
-{
-    if constexpr (OP == kQuant) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) out[0][i] = in[0][i];
-    } else if constexpr (OP == kFwd) {
-        uint32_t bad = 0;
-        float hv[32];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float g0 = bf16lo(in[0][i]), g1 = bf16hi(in[0][i]);
-            const float u0 = bf16lo(in[1][i]), u1 = bf16hi(in[1][i]);
-            const bool ok0 = swiglu_h_fast(g0, u0, hv[2 * i]);
-            const bool ok1 = swiglu_h_fast(g1, u1, hv[2 * i + 1]);
-            bad |= (ok0 ? 0u : 1u) << (2 * i);
-            bad |= (ok1 ? 0u : 1u) << (2 * i + 1);
-        }
-        if (bad) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                if (bad & (1u << e)) {
-                    const uint32_t gw = in[0][e >> 1], uw = in[1][e >> 1];
-                    const float g = (e & 1) ? bf16hi(gw) : bf16lo(gw);
-                    const float u = (e & 1) ? bf16hi(uw) : bf16lo(uw);
-                    hv[e] = swiglu_h_exact(a.sig_table, g, u);
-                }
-            }
-        }
-        count_fallbacks(a.fallbacks, bad);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) out[0][i] = pack_bf16x2(hv[2 * i], hv[2 * i + 1]);
-    } else {
-        uint32_t bad_g = 0, bad_u = 0;
-        float dg[32], du[32];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int e = 2 * i + k;
-                const float d = k ? bf16hi(in[0][i]) : bf16lo(in[0][i]);
-                const float g = k ? bf16hi(in[1][i]) : bf16lo(in[1][i]);
-                const float u = k ? bf16hi(in[2][i]) : bf16lo(in[2][i]);
-                const uint32_t m = swiglu_grads_fast(d, g, u, dg[e], du[e]);
-                bad_g |= (m & 1u) << e;
-                bad_u |= ((m >> 1) & 1u) << e;
-            }
-        }
-        const uint32_t bad = bad_g | bad_u;
-        if (bad) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                if (bad & (1u << e)) {
-                    const int i = e >> 1, k = e & 1;
-                    const float d = k ? bf16hi(in[0][i]) : bf16lo(in[0][i]);
-                    const float g = k ? bf16hi(in[1][i]) : bf16lo(in[1][i]);
-                    const float u = k ? bf16hi(in[2][i]) : bf16lo(in[2][i]);
-                    float xg, xu;
-                    swiglu_grads_exact(a.sig_table, d, g, u, xg, xu);
-                    if (bad_g & (1u << e)) dg[e] = xg;
-                    if (bad_u & (1u << e)) du[e] = xu;
-                }
-            }
-        }
-        count_fallbacks(a.fallbacks, bad_g);
-        count_fallbacks(a.fallbacks, bad_u);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            out[0][i] = pack_bf16x2(dg[2 * i], dg[2 * i + 1]);
-            out[1][i] = pack_bf16x2(du[2 * i], du[2 * i + 1]);
-        }
-    }
-}
-
-// Same op on a transposed fragment: 4 packed words (8 elements) per input.
-template <int OP>
-__device__ __forceinline__ void col_elements(const KernelArgs &a, const uint32_t (&in)[3][4],
-                                             uint32_t (&out)[2][4])
+__device__ __forceinline__ void elements8(const KernelArgs &a, const uint32_t (&in)[3][4],
+                                          uint32_t (&out)[2][4])
 {
     if constexpr (OP == kQuant) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) out[0][i] = in[0][i];
     } else if constexpr (OP == kFwd) {
+        uint64_t H[4];
         uint32_t bad = 0;
-        float hv[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const bool ok0 = swiglu_h_fast(bf16lo(in[0][i]), bf16lo(in[1][i]), hv[2 * i]);
-            const bool ok1 = swiglu_h_fast(bf16hi(in[0][i]), bf16hi(in[1][i]), hv[2 * i + 1]);
-            bad |= (ok0 ? 0u : 1u) << (2 * i);
-            bad |= (ok1 ? 0u : 1u) << (2 * i + 1);
-        }
+        for (int p = 0; p < 4; ++p) bad |= swiglu_h2(in[0][p], in[1][p], H[p]) << (2 * p);
         if (bad) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                if (bad & (1u << e)) {
-                    const uint32_t gw = in[0][e >> 1], uw = in[1][e >> 1];
-                    const float g = (e & 1) ? bf16hi(gw) : bf16lo(gw);
-                    const float u = (e & 1) ? bf16hi(uw) : bf16lo(uw);
-                    hv[e] = swiglu_h_exact(a.sig_table, g, u);
+            for (int p = 0; p < 4; ++p) {
+                if (bad & (1u << (2 * p)))
+                    H[p] = f2(swiglu_h_exact(a.sig_table, bf16lo(in[0][p]), bf16lo(in[1][p])), f2hi(H[p]));
+                if (bad & (2u << (2 * p)))
+                    H[p] = f2(f2lo(H[p]), swiglu_h_exact(a.sig_table, bf16hi(in[0][p]), bf16hi(in[1][p])));
+            }
+        }
+        count_fallbacks(a.fallbacks, bad);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) out[0][p] = pack_bf16x2(f2lo(H[p]), f2hi(H[p]));
+    } else {
+        uint64_t DG[4], DU[4];
+        uint32_t bad = 0;  // 4 bits per pair: dgate lo/hi, dup lo/hi
+#pragma unroll
+        for (int p = 0; p < 4; ++p) bad |= swiglu_grads2(in[0][p], in[1][p], in[2][p], DG[p], DU[p]) << (4 * p);
+        if (bad) {
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                if (bad & (5u << (4 * p))) {
+                    const float2 x = swiglu_grads_exact(a.sig_table, bf16lo(in[0][p]), bf16lo(in[1][p]),
+                                                        bf16lo(in[2][p]));
+                    if (bad & (1u << (4 * p))) DG[p] = f2(x.x, f2hi(DG[p]));
+                    if (bad & (4u << (4 * p))) DU[p] = f2(x.y, f2hi(DU[p]));
+                }
+                if (bad & (10u << (4 * p))) {
+                    const float2 x = swiglu_grads_exact(a.sig_table, bf16hi(in[0][p]), bf16hi(in[1][p]),
+                                                        bf16hi(in[2][p]));
+                    if (bad & (2u << (4 * p))) DG[p] = f2(f2lo(DG[p]), x.x);
+                    if (bad & (8u << (4 * p))) DU[p] = f2(f2lo(DU[p]), x.y);
                 }
             }
         }
         count_fallbacks(a.fallbacks, bad);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) out[0][i] = pack_bf16x2(hv[2 * i], hv[2 * i + 1]);
-    } else {
-        uint32_t bad_g = 0, bad_u = 0;
-        float dg[8], du[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int i = e >> 1, k = e & 1;
-            const float d = k ? bf16hi(in[0][i]) : bf16lo(in[0][i]);
-            const float g = k ? bf16hi(in[1][i]) : bf16lo(in[1][i]);
-            const float u = k ? bf16hi(in[2][i]) : bf16lo(in[2][i]);
-            const uint32_t m = swiglu_grads_fast(d, g, u, dg[e], du[e]);
-            bad_g |= (m & 1u) << e;
-            bad_u |= ((m >> 1) & 1u) << e;
-        }
-        const uint32_t bad = bad_g | bad_u;
-        if (bad) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                if (bad & (1u << e)) {
-                    const int i = e >> 1, k = e & 1;
-                    const float d = k ? bf16hi(in[0][i]) : bf16lo(in[0][i]);
-                    const float g = k ? bf16hi(in[1][i]) : bf16lo(in[1][i]);
-                    const float u = k ? bf16hi(in[2][i]) : bf16lo(in[2][i]);
-                    float xg, xu;
-                    swiglu_grads_exact(a.sig_table, d, g, u, xg, xu);
-                    if (bad_g & (1u << e)) dg[e] = xg;
-                    if (bad_u & (1u << e)) du[e] = xu;
-                }
-            }
-        }
-        count_fallbacks(a.fallbacks, bad_g);
-        count_fallbacks(a.fallbacks, bad_u);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            out[0][i] = pack_bf16x2(dg[2 * i], dg[2 * i + 1]);
-            out[1][i] = pack_bf16x2(du[2 * i], du[2 * i + 1]);
+        for (int p = 0; p < 4; ++p) {
+            out[0][p] = pack_bf16x2(f2lo(DG[p]), f2hi(DG[p]));
+            out[1][p] = pack_bf16x2(f2lo(DU[p]), f2hi(DU[p]));
         }
     }
 }
 
 // ------------------------------------------------------------------ stores
-__device__ __forceinline__ void store_row_block(const KernelArgs &a, int o, int64_t row,
-                                                int64_t col, const uint32_t (&codes)[8],
-                                                uint32_t scale)
-{
-    uint8_t *q = a.q_row[o] + row * a.ld_qrow + col;
-    uint4 *q4 = reinterpret_cast<uint4 *>(q);
-    __stcs(q4, make_uint4(codes[0], codes[1], codes[2], codes[3]));
-    __stcs(q4 + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
-    a.s_row[o][row * a.ld_srow + (col >> 5)] = static_cast<uint8_t>(scale);
-}
-
 // colwise piece: rows row0 + 8q .. +7 of column col (row0 a multiple of 32)
 __device__ __forceinline__ void store_col_piece(const KernelArgs &a, int o, int64_t row0,
                                                 int64_t col, uint32_t q, uint32_t w0, uint32_t w1,
@@ -227,14 +125,16 @@ __device__ __forceinline__ void store_col_piece(const KernelArgs &a, int o, int6
 }
 
 // ------------------------------------------------------------------ kernel
-template <int OP, int MODE, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int OP, int MODE, int NW, int STAGES>
+__global__ void __launch_bounds__((NW + 1) * 32, 1)
     mxfp8_tile_kernel(const __grid_constant__ CUtensorMap tm0,
                       const __grid_constant__ CUtensorMap tm1,
                       const __grid_constant__ CUtensorMap tm2, const KernelArgs a)
 {
     constexpr int NIN = OpTraits<OP>::kIn;
     constexpr int NOUT = OpTraits<OP>::kOut;
+    constexpr int kConsumers = NW * 32;
+    static_assert(kTileM % (4 * NW) == 0 && 32 % NW == 0, "tile / warp mismatch");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -249,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, kConsumerWarps);
+            mbar_init(empty0 + 8 * s, NW);
         }
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -260,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t tiles_n = a.tiles_n;
 
     // ------------------------------------------------------- producer warp
-    if (warp == kConsumerWarps) {
+    if (warp == NW) {
         if (lane == 0) {
             prefetch_tensormap(&tm0);
             if (NIN > 1) prefetch_tensormap(&tm1);
@@ -297,10 +197,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------------------------- consumer warps
-    const uint32_t rrow = static_cast<uint32_t>(16 * warp + (lane >> 1));  // row-pass row
-    const uint32_t rblk = static_cast<uint32_t>(lane & 1);                  // row-pass block
+    // row pass: lane -> (row offset lane/8 within a 4-row group, chunk lane%8)
+    const uint32_t rsub = static_cast<uint32_t>(lane >> 3);
+    const uint32_t rchunk = static_cast<uint32_t>(lane & 7);
     const uint32_t q = static_cast<uint32_t>(lane & 3);
-    const uint32_t ccol = static_cast<uint32_t>(8 * warp + (lane >> 2));    // col-pass column
 
     // the fused "both" mode hands values from the row pass to the col pass
     // through shared memory, separated by a named barrier
@@ -322,41 +222,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         if constexpr (MODE & kRow) {
             if (!fail) {
-                uint32_t in[3][16];
-                uint32_t out[2][16];
+#pragma unroll 1
+                for (int i = 0; i < kTileM / (4 * NW); ++i) {
+                    const uint32_t row = 4u * static_cast<uint32_t>(warp + NW * i) + rsub;
+                    const uint32_t off = swz(row, rchunk);
+                    uint32_t in[3][4];
+                    uint32_t out[2][4];
 #pragma unroll
-                for (int i = 0; i < NIN; ++i) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint4 v = *reinterpret_cast<const uint4 *>(
-                            stage_ptr + i * kTileBytes + swz(rrow, 4 * rblk + k));
-                        in[i][4 * k + 0] = v.x;
-                        in[i][4 * k + 1] = v.y;
-                        in[i][4 * k + 2] = v.z;
-                        in[i][4 * k + 3] = v.w;
+                    for (int k = 0; k < NIN; ++k) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(stage_ptr + k * kTileBytes + off);
+                        in[k][0] = v.x;
+                        in[k][1] = v.y;
+                        in[k][2] = v.z;
+                        in[k][3] = v.w;
                     }
-                }
-                row_elements<OP>(a, in, out);
-                const int64_t grow = r0 + rrow;
-                const int64_t gcol = c0 + 32 * rblk;
-                const bool live = (grow < a.M) && (gcol < a.N);
-#pragma unroll
-                for (int o = 0; o < NOUT; ++o) {
-                    uint32_t codes[8];
-                    const uint32_t sc = encode_block32(out[o], codes);
-                    if (live) store_row_block(a, o, grow, gcol, codes, sc);
-                }
-                if constexpr (kSync) {
-                    // element values back into the stage for the col pass:
-                    // output o overwrites input (NIN - NOUT + o)
+                    elements8<OP>(a, in, out);
+                    const int64_t grow = r0 + row;
+                    const int64_t gcol = c0 + 8 * rchunk;
+                    const bool live = (grow < a.M) && (gcol < a.N);
 #pragma unroll
                     for (int o = 0; o < NOUT; ++o) {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            *reinterpret_cast<uint4 *>(stage_ptr + (NIN - NOUT + o) * kTileBytes +
-                                                       swz(rrow, 4 * rblk + k)) =
-                                make_uint4(out[o][4 * k], out[o][4 * k + 1], out[o][4 * k + 2],
-                                           out[o][4 * k + 3]);
+                        uint32_t w0, w1;
+                        const uint32_t sc = encode_row8(out[o], w0, w1);
+                        if (live) {
+                            __stcs(reinterpret_cast<uint2 *>(a.q_row[o] + grow * a.ld_qrow + gcol),
+                                   make_uint2(w0, w1));
+                            if (q == 0) a.s_row[o][grow * a.ld_srow + (gcol >> 5)] = static_cast<uint8_t>(sc);
+                        }
+                        if constexpr (kSync) {
+                            *reinterpret_cast<uint4 *>(stage_ptr + (NIN - NOUT + o) * kTileBytes + off) =
+                                make_uint4(out[o][0], out[o][1], out[o][2], out[o][3]);
                         }
                     }
                 }
@@ -364,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         if constexpr (kSync) {
-            fail = consumers_sync_or(fail);
+            fail = bar_sync_or<kConsumers>(fail);
             if (fail) {
                 if (tid == 0) atomicOr(a.status, kStatusConsumerWait);
                 return;
@@ -376,23 +271,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the values the row pass stored; fused "col" evaluates the op here
             constexpr bool kEval = (MODE == kCol) && (OP != kQuant);
             constexpr int kSrc = (MODE == kBoth) ? (NIN - NOUT) : 0;
-            const int64_t gcol = c0 + ccol;
-#pragma unroll
-            for (int rb = 0; rb < kTileM / 32; ++rb) {
-                const uint32_t lrow = static_cast<uint32_t>(32 * rb + lane);
-                const uint32_t off = swz(lrow, static_cast<uint32_t>(warp));
+#pragma unroll 1
+            for (int k = 0; k < 32 / NW; ++k) {
+                const int u = warp + NW * k;
+                const uint32_t cc = static_cast<uint32_t>(u & 7);
+                const uint32_t rb = static_cast<uint32_t>(u >> 3);
+                const uint32_t off = swz(32u * rb + static_cast<uint32_t>(lane), cc);
                 uint32_t out[2][4];
                 if constexpr (kEval) {
                     uint32_t in[3][4];
 #pragma unroll
                     for (int i = 0; i < NIN; ++i) ldsm_x4_trans(stage + i * kTileBytes + off, in[i]);
-                    col_elements<OP>(a, in, out);
+                    elements8<OP>(a, in, out);
                 } else {
 #pragma unroll
                     for (int o = 0; o < NOUT; ++o)
                         ldsm_x4_trans(stage + (kSrc + o) * kTileBytes + off, out[o]);
                 }
                 const int64_t row0 = r0 + 32 * rb;
+                const int64_t gcol = c0 + 8 * cc + (lane >> 2);
                 const bool live = (row0 < a.M) && (gcol < a.N);
 #pragma unroll
                 for (int o = 0; o < NOUT; ++o) {

@@ -13,9 +13,10 @@ template <int OP, int MODE>
 cudaError_t launch_tiles(const CUtensorMap (&maps)[3], const KernelArgs &a, int grid,
                          cudaStream_t stream, int device)
 {
-    constexpr int kStages = default_stages<OP>();
+    constexpr int kWarps = Tuning<OP>::kWarps;
+    constexpr int kStages = Tuning<OP>::kStages;
     constexpr size_t kSmem = smem_bytes<OP, kStages>();
-    auto kern = mxfp8_tile_kernel<OP, MODE, kStages>;
+    auto kern = mxfp8_tile_kernel<OP, MODE, kWarps, kStages>;
     static std::atomic<unsigned long long> attr_done{0};
     const unsigned long long bit = 1ull << (device & 63);
     if (!(attr_done.load(std::memory_order_acquire) & bit)) {
@@ -26,8 +27,8 @@ cudaError_t launch_tiles(const CUtensorMap (&maps)[3], const KernelArgs &a, int 
     }
     void *args[] = {const_cast<CUtensorMap *>(&maps[0]), const_cast<CUtensorMap *>(&maps[1]),
                     const_cast<CUtensorMap *>(&maps[2]), const_cast<KernelArgs *>(&a)};
-    return cudaLaunchKernel(reinterpret_cast<const void *>(kern), dim3(grid), dim3(kThreads), args,
-                            kSmem, stream);
+    return cudaLaunchKernel(reinterpret_cast<const void *>(kern), dim3(grid),
+                            dim3((kWarps + 1) * 32), args, kSmem, stream);
 }
 
 // per-op dispatch over the scale mode (one translation unit per op)

@@ -25,7 +25,7 @@ def test_guard_bounds_fast_path_error_for_every_gate():
     torch.cuda.synchronize()
     v = out.view(8, 65536).cpu().numpy().astype(np.float64)
     g = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
-    fast = np.isfinite(g) & (g >= -80.0)
+    fast = np.isfinite(g) & (g >= -64.0)
     sig = np.array([O.sigmoid(float(x)) for x in g[fast]])
     gf = g[fast]
     silu = gf * sig
@@ -48,8 +48,8 @@ def test_guard_bounds_fast_path_error_for_every_gate():
     e_d = rel(v[4][fast], dsilu) / u
     # h = silu * u rounds once more; dup = (dh g) * sigma likewise
     need_h = e_silu + 1 + 1.5
-    need_du = e_s + 1 + 1.5
-    need_dg = e_d + 1 + 1.5
+    need_du = e_s + 1 + 1 + 1.5
+    need_dg = e_d + 1 + 1 + 1.5
     print("max fast-path error (units of 2^-24): sigma %.3f silu %.3f silu' %.3f"
           % (e_s.max(), e_silu.max(), np.nanmax(e_d[np.isfinite(e_d)])))
     print("guard margins (ulps): h %.3f dup %.3f dgate %.3f"
