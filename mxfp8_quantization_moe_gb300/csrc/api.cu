@@ -26,15 +26,19 @@ using mx::KernelArgs;
 // status bits and the count of elements settled by the double path.  Each
 // device that loads the library holds its own copy.
 __device__ double g_sig_table[65536];
+__device__ float2 g_sig2_table[65536];
 __device__ unsigned g_status;
 __device__ unsigned long long g_fallbacks;
 
-__global__ void init_sigmoid_table_kernel(double *table)
+__global__ void init_sigmoid_table_kernel(double *table, float2 *table2)
 {
     const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= 65536u) return;
     const double g = static_cast<double>(__uint_as_float(i << 16));
-    table[i] = __drcp_rn(__dadd_rn(1.0, exp(-g)));  // 1 / (1 + e^-g)
+    const double s = __drcp_rn(__dadd_rn(1.0, exp(-g)));  // 1 / (1 + e^-g)
+    table[i] = s;
+    const float hi = __double2float_rn(s);
+    table2[i] = make_float2(hi, __double2float_rn(__dadd_rn(s, -static_cast<double>(hi))));
 }
 
 __global__ void selftest_wait_kernel(unsigned *status, long long limit)
@@ -84,6 +88,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
     std::atomic<bool> ready{false};
     double *table = nullptr;
+    float2 *table2 = nullptr;
     unsigned *status = nullptr;
     unsigned long long *fallbacks = nullptr;
     int sms = 0;
@@ -117,11 +122,13 @@ mxfp8_status ensure_device(cudaStream_t stream, int *dev_out, DeviceState **stat
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_sig_table) != cudaSuccess) return MXFP8_ERR_DEVICE;
     d.table = static_cast<double *>(p);
+    if (cudaGetSymbolAddress(&p, g_sig2_table) != cudaSuccess) return MXFP8_ERR_DEVICE;
+    d.table2 = static_cast<float2 *>(p);
     if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return MXFP8_ERR_DEVICE;
     d.status = static_cast<unsigned *>(p);
     if (cudaGetSymbolAddress(&p, g_fallbacks) != cudaSuccess) return MXFP8_ERR_DEVICE;
     d.fallbacks = static_cast<unsigned long long *>(p);
-    init_sigmoid_table_kernel<<<256, 256, 0, stream>>>(d.table);
+    init_sigmoid_table_kernel<<<256, 256, 0, stream>>>(d.table, d.table2);
     if (cudaGetLastError() != cudaSuccess) return MXFP8_ERR_DEVICE;
     if (cudaMemsetAsync(d.status, 0, sizeof(unsigned), stream) != cudaSuccess ||
         cudaMemsetAsync(d.fallbacks, 0, sizeof(unsigned long long), stream) != cudaSuccess)
@@ -329,6 +336,7 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     a.group_rows = s.group_rows > 0 ? s.group_rows : s.M;
     a.group_stride = s.group_stride;
     a.sig_table = d->table;
+    a.sig2_table = d->table2;
     a.status = d->status;
     a.fallbacks = d->fallbacks;
     a.wait_limit = d->wait_limit;

@@ -1,21 +1,28 @@
 // kernel.cuh -- the persistent tile kernel shared by every entry point.
 //
-// One CTA per SM, NW consumer warps plus one producer warp.  The producer's
-// lane 0 streams the input tiles (128 rows x 64 bf16 columns per tensor,
-// 128-byte swizzle) into a ring of shared-memory stages with TMA; each stage
-// has a "full" mbarrier (transaction bytes) and an "empty" mbarrier (one
-// arrive per consumer warp).  Per tile the consumers run
-//   row pass: a lane owns one 16-byte chunk (8 elements) of a row, four
-//             consecutive lanes one 1x32 block; the element op runs on the
-//             chunk, the block amax takes two shuffles, each lane stores 8
-//             E4M3 codes (the four lanes: 32 contiguous bytes);
-//   col pass: a warp owns one 32-row x 8-column unit; ldmatrix.trans gives
-//             four lanes one column of the unit, which is encoded colwise
-//             and stored as 8-byte pieces of the column-major output.
+// One CTA per SM: 16 consumer warps and one producer warp.  The producer's
+// lane 0 streams the input tiles (128 rows x 128 bf16 columns per tensor, as
+// two 64-column boxes with the 128-byte swizzle) into a ring of shared-memory
+// stages with TMA; each stage has a "full" mbarrier (transaction bytes) and
+// an "empty" mbarrier (one arrive per consumer warp).
+//
+// Consumer warp w owns the 32 x 32 sub-tile (row block w/4, column block w%4)
+// of every tile, so no two warps ever share data and the only
+// synchronisation inside a tile is __syncwarp:
+//   row pass: four iterations of 8 rows; a lane holds one 16-byte chunk
+//             (8 elements) of a row, four consecutive lanes one 1x32 block.
+//             The element op runs on the chunk, the block amax takes two
+//             shuffles, each lane stores its 8 E4M3 codes (the four lanes: 32
+//             contiguous bytes).
+//   col pass: four 32-row x 8-column units; ldmatrix.trans gives four lanes
+//             one column of a unit, which is encoded colwise; the codes are
+//             transposed through a warp-private staging buffer and each lane
+//             stores one column's 32 codes (32 contiguous bytes of the
+//             column-major output).
 // In "both" mode the row pass writes the bf16 element values back into the
-// stage (over an input it no longer needs) and a named barrier separates the
-// passes, so both scale sets come from one read of the inputs.  In "col" mode
-// the element op runs directly on the transposed fragments.
+// stage (over an input it no longer needs), so both scale sets come from one
+// read of the inputs.  In "col" mode the element op runs directly on the
+// transposed fragments.
 //
 // Every wait is bounded (about a second); on time-out the kernel sets a bit in
 // the status word and returns, after the producer has waited (bounded) for
@@ -41,16 +48,20 @@ struct OpTraits<kBwd> {
     static constexpr int kIn = 3, kOut = 2;
 };
 
+constexpr int kWarps = (kTileM / kSub) * (kTileN / kSub);  // 16 consumer warps
+
 template <int OP>
 struct Tuning {
-    static constexpr int kWarps = 16;                         // consumer warps
-    static constexpr int kStages = OP == kQuant ? 8 : 4;
+    static constexpr int kStages = OP == kQuant ? 6 : (OP == kFwd ? 3 : 2);
 };
 
+// shared memory: 1 KB alignment slack, the stages, the per-warp colwise
+// staging buffers (1 KB per output), the mbarriers
 template <int OP, int STAGES>
 constexpr size_t smem_bytes()
 {
-    return 1024 + static_cast<size_t>(STAGES) * OpTraits<OP>::kIn * kTileBytes + 2 * STAGES * 8;
+    return 1024 + static_cast<size_t>(STAGES) * OpTraits<OP>::kIn * kTileBytes +
+           static_cast<size_t>(kWarps) * OpTraits<OP>::kOut * 1024 + 2 * STAGES * 8;
 }
 
 // ------------------------------------------------------- element operation
@@ -72,9 +83,9 @@ __device__ __forceinline__ void elements8(const KernelArgs &a, const uint32_t (&
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
                 if (bad & (1u << (2 * p)))
-                    H[p] = f2(swiglu_h_exact(a.sig_table, bf16lo(in[0][p]), bf16lo(in[1][p])), f2hi(H[p]));
+                    H[p] = f2(swiglu_h_exact(a.sig2_table, bf16lo(in[0][p]), bf16lo(in[1][p])), f2hi(H[p]));
                 if (bad & (2u << (2 * p)))
-                    H[p] = f2(f2lo(H[p]), swiglu_h_exact(a.sig_table, bf16hi(in[0][p]), bf16hi(in[1][p])));
+                    H[p] = f2(f2lo(H[p]), swiglu_h_exact(a.sig2_table, bf16hi(in[0][p]), bf16hi(in[1][p])));
             }
         }
         count_fallbacks(a.fallbacks, bad);
@@ -89,13 +100,13 @@ __device__ __forceinline__ void elements8(const KernelArgs &a, const uint32_t (&
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
                 if (bad & (5u << (4 * p))) {
-                    const float2 x = swiglu_grads_exact(a.sig_table, bf16lo(in[0][p]), bf16lo(in[1][p]),
+                    const float2 x = swiglu_grads_exact(a.sig2_table, bf16lo(in[0][p]), bf16lo(in[1][p]),
                                                         bf16lo(in[2][p]));
                     if (bad & (1u << (4 * p))) DG[p] = f2(x.x, f2hi(DG[p]));
                     if (bad & (4u << (4 * p))) DU[p] = f2(x.y, f2hi(DU[p]));
                 }
                 if (bad & (10u << (4 * p))) {
-                    const float2 x = swiglu_grads_exact(a.sig_table, bf16hi(in[0][p]), bf16hi(in[1][p]),
+                    const float2 x = swiglu_grads_exact(a.sig2_table, bf16hi(in[0][p]), bf16hi(in[1][p]),
                                                         bf16hi(in[2][p]));
                     if (bad & (2u << (4 * p))) DG[p] = f2(f2lo(DG[p]), x.x);
                     if (bad & (8u << (4 * p))) DU[p] = f2(f2lo(DU[p]), x.y);
@@ -111,34 +122,20 @@ __device__ __forceinline__ void elements8(const KernelArgs &a, const uint32_t (&
     }
 }
 
-// ------------------------------------------------------------------ stores
-// colwise piece: rows row0 + 8q .. +7 of column col (row0 a multiple of 32)
-__device__ __forceinline__ void store_col_piece(const KernelArgs &a, int o, int64_t row0,
-                                                int64_t col, uint32_t q, uint32_t w0, uint32_t w1,
-                                                uint32_t scale)
-{
-    const int64_t grp = row0 / a.group_rows;
-    const int64_t rin = row0 - grp * a.group_rows;
-    uint8_t *dst = a.q_col[o] + grp * a.group_stride + col * a.ld_qcol + rin + 8 * q;
-    __stcs(reinterpret_cast<uint2 *>(dst), make_uint2(w0, w1));
-    if (q == 0) a.s_col[o][(row0 >> 5) * a.ld_scol + col] = static_cast<uint8_t>(scale);
-}
-
 // ------------------------------------------------------------------ kernel
-template <int OP, int MODE, int NW, int STAGES>
-__global__ void __launch_bounds__((NW + 1) * 32, 1)
+template <int OP, int MODE, int STAGES>
+__global__ void __launch_bounds__((kWarps + 1) * 32, 1)
     mxfp8_tile_kernel(const __grid_constant__ CUtensorMap tm0,
                       const __grid_constant__ CUtensorMap tm1,
                       const __grid_constant__ CUtensorMap tm2, const KernelArgs a)
 {
     constexpr int NIN = OpTraits<OP>::kIn;
     constexpr int NOUT = OpTraits<OP>::kOut;
-    constexpr int kConsumers = NW * 32;
-    static_assert(kTileM % (4 * NW) == 0 && 32 % NW == 0, "tile / warp mismatch");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * NIN * kTileBytes);
+    uint8_t *staging = smem + STAGES * NIN * kTileBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(staging + kWarps * NOUT * 1024);
     const uint32_t smem_base = smem_u32(smem);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = smem_u32(bars + STAGES);
@@ -149,7 +146,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, NW);
+            mbar_init(empty0 + 8 * s, kWarps);
         }
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -160,7 +157,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     const int64_t tiles_n = a.tiles_n;
 
     // ------------------------------------------------------- producer warp
-    if (warp == NW) {
+    if (warp == kWarps) {
         if (lane == 0) {
             prefetch_tensormap(&tm0);
             if (NIN > 1) prefetch_tensormap(&tm1);
@@ -181,8 +178,15 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
                 const uint32_t dst = smem_base + static_cast<uint32_t>(s * NIN) * kTileBytes;
                 mbar_expect_tx(bar, NIN * kTileBytes);
                 tma_load_2d(dst, &tm0, c0, r0, bar);
-                if (NIN > 1) tma_load_2d(dst + kTileBytes, &tm1, c0, r0, bar);
-                if (NIN > 2) tma_load_2d(dst + 2 * kTileBytes, &tm2, c0, r0, bar);
+                tma_load_2d(dst + kBoxBytes, &tm0, c0 + kBoxN, r0, bar);
+                if (NIN > 1) {
+                    tma_load_2d(dst + kTileBytes, &tm1, c0, r0, bar);
+                    tma_load_2d(dst + kTileBytes + kBoxBytes, &tm1, c0 + kBoxN, r0, bar);
+                }
+                if (NIN > 2) {
+                    tma_load_2d(dst + 2 * kTileBytes, &tm2, c0, r0, bar);
+                    tma_load_2d(dst + 2 * kTileBytes + kBoxBytes, &tm2, c0 + kBoxN, r0, bar);
+                }
             }
             if (failed) {
                 // wait (bounded) for every load still in flight before leaving
@@ -197,73 +201,68 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     }
 
     // ------------------------------------------------------- consumer warps
-    // row pass: lane -> (row offset lane/8 within a 4-row group, chunk lane%8)
-    const uint32_t rsub = static_cast<uint32_t>(lane >> 3);
-    const uint32_t rchunk = static_cast<uint32_t>(lane & 7);
+    const uint32_t srb = static_cast<uint32_t>(warp >> 2);        // sub-tile row block
+    const uint32_t scb = static_cast<uint32_t>(warp & 3);         // sub-tile column block
+    const uint32_t box_off = (scb >> 1) * kBoxBytes;              // which 64-column box
+    const uint32_t chunk0 = (scb & 1) * 4;                        // first 16-byte chunk in it
     const uint32_t q = static_cast<uint32_t>(lane & 3);
+    // row pass: lane -> row 8i + perm(lane/4), chunk chunk0 + lane%4; the
+    // permutation puts rows r and r+4 in one 8-lane phase (conflict-free
+    // with the 128-byte swizzle)
+    const uint32_t rl = static_cast<uint32_t>(lane >> 2);
+    const uint32_t rperm = ((rl & 1u) << 2) | (rl >> 1);
+    uint8_t *stg = staging + warp * NOUT * 1024;   // this warp's colwise staging
 
-    // the fused "both" mode hands values from the row pass to the col pass
-    // through shared memory, separated by a named barrier
-    constexpr bool kSync = (MODE == kBoth) && (OP != kQuant);
+    constexpr bool kSplit = (MODE == kBoth) && (OP != kQuant);  // values handed row -> col pass
     int it = 0;
     for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = static_cast<uint32_t>(it / STAGES) & 1u;
-        bool fail = !mbar_wait_bounded(full0 + 8 * s, ph, a.wait_limit);
-        fail = __any_sync(0xFFFFFFFFu, fail);
-        if (fail && !kSync) {
+        const bool fail = __any_sync(0xFFFFFFFFu, !mbar_wait_bounded(full0 + 8 * s, ph, a.wait_limit));
+        if (fail) {
             if (lane == 0) atomicOr(a.status, kStatusConsumerWait);
             return;
         }
-        const int64_t r0 = (t / tiles_n) * kTileM;
-        const int64_t c0 = (t % tiles_n) * kTileN;
-        const uint32_t stage = smem_base + static_cast<uint32_t>(s * NIN) * kTileBytes;
-        uint8_t *stage_ptr = smem + static_cast<size_t>(s * NIN) * kTileBytes;
+        const int64_t r0 = (t / tiles_n) * kTileM + kSub * srb;   // sub-tile origin
+        const int64_t c0 = (t % tiles_n) * kTileN + kSub * scb;
+        const uint32_t stage = smem_base + static_cast<uint32_t>(s * NIN) * kTileBytes + box_off;
+        uint8_t *stage_ptr = smem + static_cast<size_t>(s * NIN) * kTileBytes + box_off;
 
         if constexpr (MODE & kRow) {
-            if (!fail) {
+            const int64_t gcol = c0 + 8 * q;
 #pragma unroll 1
-                for (int i = 0; i < kTileM / (4 * NW); ++i) {
-                    const uint32_t row = 4u * static_cast<uint32_t>(warp + NW * i) + rsub;
-                    const uint32_t off = swz(row, rchunk);
-                    uint32_t in[3][4];
-                    uint32_t out[2][4];
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t row = kSub * srb + 8u * i + rperm;
+                const uint32_t off = swz(row, chunk0 + q);
+                uint32_t in[3][4];
+                uint32_t out[2][4];
 #pragma unroll
-                    for (int k = 0; k < NIN; ++k) {
-                        const uint4 v = *reinterpret_cast<const uint4 *>(stage_ptr + k * kTileBytes + off);
-                        in[k][0] = v.x;
-                        in[k][1] = v.y;
-                        in[k][2] = v.z;
-                        in[k][3] = v.w;
+                for (int k = 0; k < NIN; ++k) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(stage_ptr + k * kTileBytes + off);
+                    in[k][0] = v.x;
+                    in[k][1] = v.y;
+                    in[k][2] = v.z;
+                    in[k][3] = v.w;
+                }
+                elements8<OP>(a, in, out);
+                const int64_t grow = r0 + 8 * i + rperm;
+                const bool live = (grow < a.M) && (gcol < a.N);
+#pragma unroll
+                for (int o = 0; o < NOUT; ++o) {
+                    uint32_t w0, w1;
+                    const uint32_t sc = encode_row8(out[o], w0, w1);
+                    if (live) {
+                        __stcs(reinterpret_cast<uint2 *>(a.q_row[o] + grow * a.ld_qrow + gcol),
+                               make_uint2(w0, w1));
+                        if (q == 0) a.s_row[o][grow * a.ld_srow + (gcol >> 5)] = static_cast<uint8_t>(sc);
                     }
-                    elements8<OP>(a, in, out);
-                    const int64_t grow = r0 + row;
-                    const int64_t gcol = c0 + 8 * rchunk;
-                    const bool live = (grow < a.M) && (gcol < a.N);
-#pragma unroll
-                    for (int o = 0; o < NOUT; ++o) {
-                        uint32_t w0, w1;
-                        const uint32_t sc = encode_row8(out[o], w0, w1);
-                        if (live) {
-                            __stcs(reinterpret_cast<uint2 *>(a.q_row[o] + grow * a.ld_qrow + gcol),
-                                   make_uint2(w0, w1));
-                            if (q == 0) a.s_row[o][grow * a.ld_srow + (gcol >> 5)] = static_cast<uint8_t>(sc);
-                        }
-                        if constexpr (kSync) {
-                            *reinterpret_cast<uint4 *>(stage_ptr + (NIN - NOUT + o) * kTileBytes + off) =
-                                make_uint4(out[o][0], out[o][1], out[o][2], out[o][3]);
-                        }
+                    if constexpr (kSplit) {
+                        *reinterpret_cast<uint4 *>(stage_ptr + (NIN - NOUT + o) * kTileBytes + off) =
+                            make_uint4(out[o][0], out[o][1], out[o][2], out[o][3]);
                     }
                 }
             }
-        }
-
-        if constexpr (kSync) {
-            fail = bar_sync_or<kConsumers>(fail);
-            if (fail) {
-                if (tid == 0) atomicOr(a.status, kStatusConsumerWait);
-                return;
-            }
+            if constexpr (kSplit) __syncwarp();
         }
 
         if constexpr (MODE & kCol) {
@@ -271,12 +270,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
             // the values the row pass stored; fused "col" evaluates the op here
             constexpr bool kEval = (MODE == kCol) && (OP != kQuant);
             constexpr int kSrc = (MODE == kBoth) ? (NIN - NOUT) : 0;
+            const uint32_t crow = kSub * srb + static_cast<uint32_t>(lane);
+            const uint32_t cc = static_cast<uint32_t>(lane >> 2);   // column within a unit
 #pragma unroll 1
-            for (int k = 0; k < 32 / NW; ++k) {
-                const int u = warp + NW * k;
-                const uint32_t cc = static_cast<uint32_t>(u & 7);
-                const uint32_t rb = static_cast<uint32_t>(u >> 3);
-                const uint32_t off = swz(32u * rb + static_cast<uint32_t>(lane), cc);
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t off = swz(crow, chunk0 + k);
                 uint32_t out[2][4];
                 if constexpr (kEval) {
                     uint32_t in[3][4];
@@ -288,19 +286,46 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
                     for (int o = 0; o < NOUT; ++o)
                         ldsm_x4_trans(stage + (kSrc + o) * kTileBytes + off, out[o]);
                 }
-                const int64_t row0 = r0 + 32 * rb;
-                const int64_t gcol = c0 + 8 * cc + (lane >> 2);
-                const bool live = (row0 < a.M) && (gcol < a.N);
+                const int64_t gcol = c0 + 8 * k + cc;
+                const bool live = (r0 < a.M) && (gcol < a.N);
 #pragma unroll
                 for (int o = 0; o < NOUT; ++o) {
-                    uint32_t w0, w1;
-                    const uint32_t sc = encode_col32(out[o], q, w0, w1);
-                    if (live) store_col_piece(a, o, row0, gcol, q, w0, w1, sc);
+                    uint32_t pc[4];
+                    const uint32_t sc = encode_col8(out[o], pc);
+                    // column 8k + cc, rows 8m + 2q, 8m + 2q + 1 of the sub-tile
+                    const uint32_t col = 8u * k + cc;
+                    uint8_t *base = stg + o * 1024 + col * 32;
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const uint32_t byte = 8u * m + 2u * q;
+                        *reinterpret_cast<uint16_t *>(base + ((byte ^ ((col >> 2) & 1u) * 16u))) =
+                            static_cast<uint16_t>(pc[m]);
+                    }
+                    if (live && q == 0) a.s_col[o][(r0 >> 5) * a.ld_scol + gcol] = static_cast<uint8_t>(sc);
                 }
             }
+            __syncwarp();
+            // each lane stores one column's 32 codes
+            const int64_t gcol = c0 + lane;
+            if (r0 < a.M && gcol < a.N) {
+                const int64_t grp = r0 / a.group_rows;
+                const int64_t rin = r0 - grp * a.group_rows;
+#pragma unroll
+                for (int o = 0; o < NOUT; ++o) {
+                    const uint8_t *src = stg + o * 1024 + lane * 32;
+                    const uint32_t sw = ((static_cast<uint32_t>(lane) >> 2) & 1u) * 16u;
+                    const uint4 lo = *reinterpret_cast<const uint4 *>(src + (0u ^ sw));
+                    const uint4 hi = *reinterpret_cast<const uint4 *>(src + (16u ^ sw));
+                    uint4 *dst = reinterpret_cast<uint4 *>(a.q_col[o] + grp * a.group_stride +
+                                                           gcol * a.ld_qcol + rin);
+                    __stcs(dst, lo);
+                    __stcs(dst + 1, hi);
+                }
+            }
+            __syncwarp();
         }
 
-        if constexpr (kSync) fence_proxy_async_smem();
+        if constexpr (kSplit) fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * s);
     }

@@ -13,10 +13,10 @@ template <int OP, int MODE>
 cudaError_t launch_tiles(const CUtensorMap (&maps)[3], const KernelArgs &a, int grid,
                          cudaStream_t stream, int device)
 {
-    constexpr int kWarps = Tuning<OP>::kWarps;
     constexpr int kStages = Tuning<OP>::kStages;
     constexpr size_t kSmem = smem_bytes<OP, kStages>();
-    auto kern = mxfp8_tile_kernel<OP, MODE, kWarps, kStages>;
+    static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
+    auto kern = mxfp8_tile_kernel<OP, MODE, kStages>;
     static std::atomic<unsigned long long> attr_done{0};
     const unsigned long long bit = 1ull << (device & 63);
     if (!(attr_done.load(std::memory_order_acquire) & bit)) {
