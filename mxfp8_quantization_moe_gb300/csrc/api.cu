@@ -163,7 +163,7 @@ bool make_bf16_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols,
 {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(mx::kTileN), static_cast<cuuint32_t>(mx::kTileM)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(mx::kBoxN), static_cast<cuuint32_t>(mx::kTileM)};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
