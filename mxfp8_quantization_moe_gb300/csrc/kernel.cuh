@@ -76,10 +76,23 @@ __device__ __forceinline__ void elements8(const KernelArgs &a, const uint32_t (&
         for (int i = 0; i < 4; ++i) out[0][i] = in[0][i];
     } else if constexpr (OP == kFwd) {
         uint64_t H[4];
-        uint32_t bad = 0;
+        bool all_ok = true;
 #pragma unroll
-        for (int p = 0; p < 4; ++p) bad |= swiglu_h2(in[0][p], in[1][p], H[p]) << (2 * p);
-        if (bad) {
+        for (int p = 0; p < 4; ++p) {
+            bool ok0, ok1;
+            swiglu_h2(in[0][p], in[1][p], H[p], ok0, ok1);
+            all_ok = all_ok && ok0 && ok1;
+        }
+        if (!all_ok) {  // rare: find the elements to replace and settle them exactly
+            uint32_t bad = 0;
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                uint64_t tmp;
+                bool ok0, ok1;
+                swiglu_h2(in[0][p], in[1][p], tmp, ok0, ok1);
+                bad |= ((ok0 ? 0u : 1u) | (ok1 ? 0u : 2u)) << (2 * p);
+            }
+            count_fallbacks(a.fallbacks, bad);
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
                 if (bad & (1u << (2 * p)))
@@ -88,15 +101,27 @@ __device__ __forceinline__ void elements8(const KernelArgs &a, const uint32_t (&
                     H[p] = f2(f2lo(H[p]), swiglu_h_exact(a.sig2_table, bf16hi(in[0][p]), bf16hi(in[1][p])));
             }
         }
-        count_fallbacks(a.fallbacks, bad);
 #pragma unroll
         for (int p = 0; p < 4; ++p) out[0][p] = pack_bf16x2(f2lo(H[p]), f2hi(H[p]));
     } else {
         uint64_t DG[4], DU[4];
-        uint32_t bad = 0;  // 4 bits per pair: dgate lo/hi, dup lo/hi
+        bool all_ok = true;
 #pragma unroll
-        for (int p = 0; p < 4; ++p) bad |= swiglu_grads2(in[0][p], in[1][p], in[2][p], DG[p], DU[p]) << (4 * p);
-        if (bad) {
+        for (int p = 0; p < 4; ++p) {
+            bool g0, g1, u0, u1;
+            swiglu_grads2(in[0][p], in[1][p], in[2][p], DG[p], DU[p], g0, g1, u0, u1);
+            all_ok = all_ok && g0 && g1 && u0 && u1;
+        }
+        if (!all_ok) {  // rare: find the elements to replace and settle them exactly
+            uint32_t bad = 0;  // 4 bits per pair: dgate lo/hi, dup lo/hi
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                uint64_t t0, t1;
+                bool g0, g1, u0, u1;
+                swiglu_grads2(in[0][p], in[1][p], in[2][p], t0, t1, g0, g1, u0, u1);
+                bad |= ((g0 ? 0u : 1u) | (g1 ? 0u : 2u) | (u0 ? 0u : 4u) | (u1 ? 0u : 8u)) << (4 * p);
+            }
+            count_fallbacks(a.fallbacks, bad);
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
                 if (bad & (5u << (4 * p))) {
@@ -113,7 +138,6 @@ __device__ __forceinline__ void elements8(const KernelArgs &a, const uint32_t (&
                 }
             }
         }
-        count_fallbacks(a.fallbacks, bad);
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
             out[0][p] = pack_bf16x2(f2lo(DG[p]), f2hi(DG[p]));
@@ -214,6 +238,7 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, 1)
     uint8_t *stg = staging + warp * NOUT * 1024;   // this warp's colwise staging
 
     constexpr bool kSplit = (MODE == kBoth) && (OP != kQuant);  // values handed row -> col pass
+    constexpr int kUnroll = (OP == kQuant) ? 4 : 1;  // the cast alone: unroll for ILP
     int it = 0;
     for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
         const int s = it % STAGES;
@@ -230,7 +255,7 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, 1)
 
         if constexpr (MODE & kRow) {
             const int64_t gcol = c0 + 8 * q;
-#pragma unroll 1
+#pragma unroll kUnroll
             for (int i = 0; i < 4; ++i) {
                 const uint32_t row = kSub * srb + 8u * i + rperm;
                 const uint32_t off = swz(row, chunk0 + q);
@@ -272,7 +297,8 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, 1)
             constexpr int kSrc = (MODE == kBoth) ? (NIN - NOUT) : 0;
             const uint32_t crow = kSub * srb + static_cast<uint32_t>(lane);
             const uint32_t cc = static_cast<uint32_t>(lane >> 2);   // column within a unit
-#pragma unroll 1
+            const uint32_t stg_off = (2u * q) ^ (((cc >> 2) & 1u) * 16u);
+#pragma unroll kUnroll
             for (int k = 0; k < 4; ++k) {
                 const uint32_t off = swz(crow, chunk0 + k);
                 uint32_t out[2][4];
@@ -290,17 +316,16 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, 1)
                 const bool live = (r0 < a.M) && (gcol < a.N);
 #pragma unroll
                 for (int o = 0; o < NOUT; ++o) {
-                    uint32_t pc[4];
-                    const uint32_t sc = encode_col8(out[o], pc);
-                    // column 8k + cc, rows 8m + 2q, 8m + 2q + 1 of the sub-tile
-                    const uint32_t col = 8u * k + cc;
-                    uint8_t *base = stg + o * 1024 + col * 32;
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const uint32_t byte = 8u * m + 2u * q;
-                        *reinterpret_cast<uint16_t *>(base + ((byte ^ ((col >> 2) & 1u) * 16u))) =
-                            static_cast<uint16_t>(pc[m]);
-                    }
+                    uint32_t w0, w1;
+                    const uint32_t sc = encode_col8(out[o], w0, w1);
+                    // column 8k + cc of the sub-tile: rows 8m + 2q, 8m + 2q + 1 at
+                    // bytes 8m + 2q of its 32-byte column (16-byte halves swapped
+                    // for columns with bit 2 set: conflict-free reads below)
+                    uint8_t *base = stg + o * 1024 + (8u * k + cc) * 32;
+                    *reinterpret_cast<uint16_t *>(base + (stg_off ^ 0u)) = static_cast<uint16_t>(w0);
+                    *reinterpret_cast<uint16_t *>(base + (stg_off ^ 8u)) = static_cast<uint16_t>(w0 >> 16);
+                    *reinterpret_cast<uint16_t *>(base + (stg_off ^ 16u)) = static_cast<uint16_t>(w1);
+                    *reinterpret_cast<uint16_t *>(base + (stg_off ^ 24u)) = static_cast<uint16_t>(w1 >> 16);
                     if (live && q == 0) a.s_col[o][(r0 >> 5) * a.ld_scol + gcol] = static_cast<uint8_t>(sc);
                 }
             }
@@ -308,8 +333,11 @@ __global__ void __launch_bounds__((kWarps + 1) * 32, 1)
             // each lane stores one column's 32 codes
             const int64_t gcol = c0 + lane;
             if (r0 < a.M && gcol < a.N) {
-                const int64_t grp = r0 / a.group_rows;
-                const int64_t rin = r0 - grp * a.group_rows;
+                int64_t grp = 0, rin = r0;
+                if (a.group_stride != 0) {  // 3D: per-expert column-major output
+                    grp = r0 / a.group_rows;
+                    rin = r0 - grp * a.group_rows;
+                }
 #pragma unroll
                 for (int o = 0; o < NOUT; ++o) {
                     const uint8_t *src = stg + o * 1024 + lane * 32;
