@@ -105,22 +105,14 @@ __device__ __forceinline__ void elements8(const KernelArgs &a, const uint32_t (&
         for (int p = 0; p < 4; ++p) out[0][p] = pack_bf16x2(f2lo(H[p]), f2hi(H[p]));
     } else {
         uint64_t DG[4], DU[4];
-        bool all_ok = true;
+        uint32_t bad = 0;  // 4 bits per pair: dgate lo/hi, dup lo/hi
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
             bool g0, g1, u0, u1;
             swiglu_grads2(in[0][p], in[1][p], in[2][p], DG[p], DU[p], g0, g1, u0, u1);
-            all_ok = all_ok && g0 && g1 && u0 && u1;
+            bad |= ((g0 ? 0u : 1u) | (g1 ? 0u : 2u) | (u0 ? 0u : 4u) | (u1 ? 0u : 8u)) << (4 * p);
         }
-        if (!all_ok) {  // rare: find the elements to replace and settle them exactly
-            uint32_t bad = 0;  // 4 bits per pair: dgate lo/hi, dup lo/hi
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                uint64_t t0, t1;
-                bool g0, g1, u0, u1;
-                swiglu_grads2(in[0][p], in[1][p], in[2][p], t0, t1, g0, g1, u0, u1);
-                bad |= ((g0 ? 0u : 1u) | (g1 ? 0u : 2u) | (u0 ? 0u : 4u) | (u1 ? 0u : 8u)) << (4 * p);
-            }
+        if (bad) {  // rare: settle the flagged elements exactly
             count_fallbacks(a.fallbacks, bad);
 #pragma unroll
             for (int p = 0; p < 4; ++p) {

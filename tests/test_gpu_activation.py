@@ -55,6 +55,14 @@ def test_guard_bounds_fast_path_error_for_every_gate():
     print("guard margins (ulps): h %.3f dup %.3f dgate %.3f"
           % ((v[5][fast] - need_h).min(), (v[6][fast] - need_du).min(),
              (v[7][fast] - need_dg).min()))
+    # the dgate guard's shape: need_dg <= base + c * |w-1|/|w| -- report the
+    # smallest c that works with the kernel's base
+    wf = v[3][fast]
+    fac = np.abs(wf - 1) / np.abs(wf)
+    base = v[7][fast].min()
+    big = fac > 0.05
+    print("dgate: kernel base %.2f, needed cancel coefficient %.3f"
+          % (base, np.max((need_dg[big] - base) / fac[big])))
     assert np.all(need_h <= v[5][fast]), gf[np.argmax(need_h - v[5][fast])]
     assert np.all(need_du <= v[6][fast]), gf[np.argmax(need_du - v[6][fast])]
     ok = need_dg <= v[7][fast]
