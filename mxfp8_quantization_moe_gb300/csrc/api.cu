@@ -157,13 +157,14 @@ bool get_encoder()
     return g_encode != nullptr;
 }
 
-// bf16 (rows, cols) with row pitch ld elements, boxes of 128 rows x 64 cols,
+// bf16 (rows, cols) with row pitch ld elements, boxes of box_rows x 64 cols,
 // 128-byte swizzle, zero fill outside the tensor.
-bool make_bf16_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64_t ld)
+bool make_bf16_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64_t ld,
+                   int box_rows)
 {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(mx::kBoxN), static_cast<cuuint32_t>(mx::kTileM)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(mx::kBoxN), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -311,18 +312,19 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     if (st != MXFP8_OK) return st;
     if (!get_encoder()) return MXFP8_ERR_DEVICE;
     const int nin = s.op == mx::kQuant ? 1 : (s.op == mx::kFwd ? 2 : 3);
+    const int tm = mx::tile_rows(s.op, s.mode);
     CUtensorMap maps[3];
     std::memset(maps, 0, sizeof(maps));
     for (int i = 0; i < 3; ++i) {
         const int src = i < nin ? i : 0;
-        if (!make_bf16_map(&maps[i], s.in[src], s.M, s.N, s.ld_in[src])) return MXFP8_ERR_ALIGN;
+        if (!make_bf16_map(&maps[i], s.in[src], s.M, s.N, s.ld_in[src], tm)) return MXFP8_ERR_ALIGN;
     }
     KernelArgs a;
     std::memset(&a, 0, sizeof(a));
     a.M = s.M;
     a.N = s.N;
     a.tiles_n = (s.N + mx::kTileN - 1) / mx::kTileN;
-    a.num_tiles = ((s.M + mx::kTileM - 1) / mx::kTileM) * a.tiles_n;
+    a.num_tiles = ((s.M + tm - 1) / tm) * a.tiles_n;
     for (int o = 0; o < 2; ++o) {
         a.q_row[o] = s.q_row[o];
         a.s_row[o] = s.s_row[o];

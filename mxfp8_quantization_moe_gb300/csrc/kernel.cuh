@@ -48,20 +48,27 @@ struct OpTraits<kBwd> {
     static constexpr int kIn = 3, kOut = 2;
 };
 
-constexpr int kWarps = (kTileM / kSub) * (kTileN / kSub);  // 16 consumer warps
-
-template <int OP>
+// Tile height and pipeline depth per instantiation: more warps hide more
+// latency where the registers allow it (the cast alone needs few).
+template <int OP, int MODE>
 struct Tuning {
-    static constexpr int kStages = OP == kQuant ? 6 : (OP == kFwd ? 3 : 2);
+    static constexpr int kTM = OP == kQuant ? 256 : ((OP == kFwd && MODE != kBoth) ? 192 : 128);
+    static constexpr int kStages = OP == kQuant ? 3 : 2 + (OP == kFwd && MODE == kBoth);
 };
+
+template <int TM>
+__host__ __device__ constexpr int warps_of() { return (TM / kSub) * (kTileN / kSub); }
+
+template <int TM>
+__host__ __device__ constexpr int tile_bytes() { return TM * kTileN * 2; }
 
 // shared memory: 1 KB alignment slack, the stages, the per-warp colwise
 // staging buffers (1 KB per output), the mbarriers
-template <int OP, int STAGES>
+template <int OP, int TM, int STAGES>
 constexpr size_t smem_bytes()
 {
-    return 1024 + static_cast<size_t>(STAGES) * OpTraits<OP>::kIn * kTileBytes +
-           static_cast<size_t>(kWarps) * OpTraits<OP>::kOut * 1024 + 2 * STAGES * 8;
+    return 1024 + static_cast<size_t>(STAGES) * OpTraits<OP>::kIn * tile_bytes<TM>() +
+           static_cast<size_t>(warps_of<TM>()) * OpTraits<OP>::kOut * 1024 + 2 * STAGES * 8;
 }
 
 // ------------------------------------------------------- element operation
@@ -139,14 +146,18 @@ __device__ __forceinline__ void elements8(const KernelArgs &a, const uint32_t (&
 }
 
 // ------------------------------------------------------------------ kernel
-template <int OP, int MODE, int STAGES>
-__global__ void __launch_bounds__((kWarps + 1) * 32, 1)
+template <int OP, int MODE, int TM, int STAGES>
+__global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, 1)
     mxfp8_tile_kernel(const __grid_constant__ CUtensorMap tm0,
                       const __grid_constant__ CUtensorMap tm1,
                       const __grid_constant__ CUtensorMap tm2, const KernelArgs a)
 {
     constexpr int NIN = OpTraits<OP>::kIn;
     constexpr int NOUT = OpTraits<OP>::kOut;
+    constexpr int kWarps = warps_of<TM>();
+    constexpr int kTileM = TM;
+    constexpr int kBoxBytes = TM * kBoxN * 2;
+    constexpr int kTileBytes = tile_bytes<TM>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
