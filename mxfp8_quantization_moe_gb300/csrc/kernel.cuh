@@ -52,7 +52,8 @@ struct OpTraits<kBwd> {
 // latency where the registers allow it (the cast alone needs few).
 template <int OP, int MODE>
 struct Tuning {
-    static constexpr int kTM = OP == kQuant ? 256 : ((OP == kFwd && MODE != kBoth) ? 192 : 128);
+    static constexpr int kTM = OP == kQuant ? 224 : ((OP == kFwd && MODE != kBoth) ? 192 : 128);
+    static_assert((kTM / 32) * 4 + 1 <= 32, "at most 1024 threads per CTA");
     static constexpr int kStages = OP == kQuant ? 3 : 2 + (OP == kFwd && MODE == kBoth);
 };
 
