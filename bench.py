@@ -42,6 +42,33 @@ PAGES_US = {("fwd", 1): 904.19, ("fwd", 2): 1022.98, ("fwd", 3): 1216.08,
             ("bwd", 1): 1321.98, ("bwd", 2): 1710.08, ("bwd", 3): 1859.09}
 
 
+# DRAM traffic (read + write bytes) of one full-size launch, from the ncu
+# captures summarised under profiles/ (small case scaled by the units
+# processed); valid only for the kernel sources they were taken on.
+TRAFFIC = {
+    "bwd_both": (10.52346368e9, "35ce231032847831", "profiles/bwd_both_ncu.md"),
+    "fwd_both": (6.214535168e9, "35ce231032847831", "profiles/fwd_both_ncu.md"),
+    "fwd_col": (5.2343808e9, "35ce231032847831", "profiles/fwd_col_ncu.md"),
+}
+
+
+def kernel_source_hash() -> str:
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "mxfp8_quantization_moe_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(cell: str):
+    t = TRAFFIC.get(cell)
+    if t is None or t[1] != kernel_source_hash():
+        return None
+    return t[0]
+
+
 def cell_bytes(kind: str, mode: int, M: int, N: int) -> int:
     k = 2 if mode == 3 else 1
     mn = M * N
@@ -325,7 +352,8 @@ def main():
         "per_cell": per_cell,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": dom_achieved, "peak": peak,
                      "peak_kind": "%s hbm_gbs (copy)" % peak_kind, "unit": "GB/s",
-                     "frac": round(dom_achieved / peak, 4), "traffic": None},
+                     "frac": round(dom_achieved / peak, 4), "traffic": traffic_for(dom),
+                     "algorithmic_bytes": per_cell[dom]["bytes"]},
         "gpu_launches": K * len(CELLS),
         "fallback_elements": fallbacks,
         "clocks": clk,
