@@ -146,6 +146,33 @@ mxfp8_status mxfp8_quant_3d_colwise(const uint16_t *x, int64_t E, int64_t N, int
                                     uint8_t *q, uint8_t *s, void *stream);
 
 /*
+ * Allocation-free forward, for callers that cannot call cudaMalloc at all:
+ * code that must live inside a host framework's fixed device-memory arena,
+ * or that runs where allocation is forbidden.  (The pages have no
+ * counterpart: this is the unfused order -- activation, then the standalone
+ * cast -- with the activation kept in library-owned scratch.)
+ * Same arguments, rules and results as mxfp8_swiglu_fwd: pass 1 writes the
+ * bf16 activation h (computed exactly as the fused kernel computes it) into a
+ * static scratch array, pass 2 casts h with the standalone quantizer.
+ *  - Scratch: 8,388,608 bf16 elements (16 MiB) reserved in every device that
+ *    loads the library, held until the process exits.  Rows are padded to a
+ *    multiple of 8 elements, so the limit is M * roundup(N, 8) <= 8,388,608;
+ *    larger problems return MXFP8_ERR_SHAPE before anything is enqueued.
+ *  - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *  - The first call on a device looks up the scratch's device address (and
+ *    does the library's one-time set-up, see mxfp8_init); make that first
+ *    call before any stream capture.
+ *  - Every call shares the one scratch array and overwrites the part it uses
+ *    before reading it; calls that overlap on the GPU (on different streams)
+ *    race on it and must be ordered by the caller.
+ */
+mxfp8_status mxfp8_swiglu_fwd_noalloc(const uint16_t *gate, const uint16_t *up, int64_t ld_in,
+                                      int64_t M, int64_t N, int mode,
+                                      uint8_t *q_row, int64_t ld_qrow, uint8_t *s_row, int64_t ld_srow,
+                                      uint8_t *q_col, int64_t ld_qcol, uint8_t *s_col, int64_t ld_scol,
+                                      void *stream);
+
+/*
  * Sticky device-side status of the current device.  Kernels never trap: a
  * pipeline wait that exceeds its limit (about a second) makes the kernel set
  * a flag bit and return.  flags: bit 0 consumer wait, bit 1 producer wait,

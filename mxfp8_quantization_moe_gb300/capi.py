@@ -41,6 +41,8 @@ SIGNATURES = {
                                    _int, _vp]),
     "mxfp8_selftest_wait_timeout": (_int, [_u64, _vp]),
     "mxfp8_selftest_activation": (_int, [_vp, _vp]),
+    "mxfp8_swiglu_fwd_noalloc": (_int, [_vp, _vp, _i64, _i64, _i64, _int,
+                                        _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]),
 }
 
 
@@ -124,3 +126,9 @@ def mxfp8_selftest_wait_timeout(limit_cycles: int, stream) -> int:
 
 def mxfp8_selftest_activation(out, stream) -> int:
     return _lib.mxfp8_selftest_activation(out, stream)
+
+
+def mxfp8_swiglu_fwd_noalloc(gate, up, ld_in, M, N, mode, q_row, ld_qrow, s_row, ld_srow,
+                             q_col, ld_qcol, s_col, ld_scol, stream) -> int:
+    return _lib.mxfp8_swiglu_fwd_noalloc(gate, up, ld_in, M, N, mode, q_row, ld_qrow, s_row, ld_srow,
+                                         q_col, ld_qcol, s_col, ld_scol, stream)

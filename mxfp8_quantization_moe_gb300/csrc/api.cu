@@ -9,6 +9,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -532,3 +533,140 @@ mxfp8_status mxfp8_selftest_wait_timeout(uint64_t limit_cycles, void *stream)
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------
+// Allocation-free forward: for callers that cannot call cudaMalloc at all
+// (code running inside a host framework's fixed device-memory arena, or in
+// a context where allocating is forbidden, such as between the start and end
+// of a stream capture that must not record allocation nodes).  It takes the
+// same arguments as mxfp8_swiglu_fwd but materialises the activation in a
+// scratch buffer that the library itself reserves statically.
+namespace {
+
+// Scratch for the bf16 activation of one call: 8,388,608 elements (16 MiB),
+// reserved in every device's global memory when the library is loaded and
+// held until the process exits.  Every call of the entry point reuses it.
+constexpr int64_t kNoAllocScratchElems = 8ll * 1024 * 1024;
+static __device__ __align__(256) uint16_t g_noalloc_scratch[kNoAllocScratchElems];
+
+// device address of the scratch, looked up once per device (host code must
+// not pass the symbol itself: on the host it is only a stand-in)
+uint16_t *g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mutex;
+
+mxfp8_status noalloc_scratch_ptr(uint16_t **out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MXFP8_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MXFP8_ERR_DEVICE;
+        g_noalloc_ptr[dev] = static_cast<uint16_t *>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return MXFP8_OK;
+}
+
+// h = bf16(silu(gate) * up) for one 8-column chunk per thread, written to the
+// scratch with row pitch ld_h; the same fast path and exact fallback as the
+// fused kernels, so the values are the ones the fused forward casts.
+__global__ void swiglu_activation_kernel(const uint16_t *__restrict__ gate,
+                                         const uint16_t *__restrict__ up, int64_t ld_in,
+                                         int64_t M, int64_t N, uint16_t *__restrict__ h,
+                                         int64_t ld_h, KernelArgs a)
+{
+    const int64_t chunks_n = (N + 7) / 8;
+    const int64_t total = M * chunks_n;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = i / chunks_n;
+        const int64_t c = (i - r * chunks_n) * 8;
+        const uint16_t *g = gate + r * ld_in + c;
+        const uint16_t *u = up + r * ld_in + c;
+        uint16_t *o = h + r * ld_h + c;
+        if (c + 8 <= N) {
+            const uint4 gv = *reinterpret_cast<const uint4 *>(g);
+            const uint4 uv = *reinterpret_cast<const uint4 *>(u);
+            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+            const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+            uint32_t ow[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                uint64_t H;
+                bool ok0, ok1;
+                mx::swiglu_h2(gw[p], uw[p], H, ok0, ok1);
+                float h0 = mx::f2lo(H), h1 = mx::f2hi(H);
+                if (!ok0) h0 = mx::swiglu_h_exact(a.sig2_table, mx::bf16lo(gw[p]), mx::bf16lo(uw[p]));
+                if (!ok1) h1 = mx::swiglu_h_exact(a.sig2_table, mx::bf16hi(gw[p]), mx::bf16hi(uw[p]));
+                ow[p] = mx::pack_bf16x2(h0, h1);
+            }
+            *reinterpret_cast<uint4 *>(o) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+        } else {
+            for (int64_t k = 0; c + k < N; ++k) {
+                const float gf = __uint_as_float(static_cast<uint32_t>(g[k]) << 16);
+                const float uf = __uint_as_float(static_cast<uint32_t>(u[k]) << 16);
+                const float hv = mx::swiglu_h_exact(a.sig2_table, gf, uf);
+                o[k] = static_cast<uint16_t>(mx::pack_bf16x2(hv, 0.0f) & 0xFFFFu);
+            }
+        }
+    }
+}
+
+}  // namespace
+
+extern "C" mxfp8_status mxfp8_swiglu_fwd_noalloc(const uint16_t *gate, const uint16_t *up,
+                                                 int64_t ld_in, int64_t M, int64_t N, int mode,
+                                                 uint8_t *q_row, int64_t ld_qrow, uint8_t *s_row,
+                                                 int64_t ld_srow, uint8_t *q_col, int64_t ld_qcol,
+                                                 uint8_t *s_col, int64_t ld_scol, void *stream)
+{
+    // the fused forward's argument rules apply unchanged
+    Spec fs = blank(mx::kFwd, mode, M, N);
+    fs.in[0] = gate;
+    fs.in[1] = up;
+    fs.ld_in[0] = fs.ld_in[1] = ld_in;
+    fs.q_row[0] = q_row;
+    fs.s_row[0] = s_row;
+    fs.q_col[0] = q_col;
+    fs.s_col[0] = s_col;
+    fs.ld_qrow = ld_qrow;
+    fs.ld_srow = ld_srow;
+    fs.ld_qcol = ld_qcol;
+    fs.ld_scol = ld_scol;
+    mxfp8_status st = validate(fs);
+    if (st != MXFP8_OK || M == 0 || N == 0) return st;
+    const int64_t ld_h = (N + 7) / 8 * 8;  // 16-byte rows for the cast's TMA tiles
+    if (M > kNoAllocScratchElems / ld_h) return MXFP8_ERR_SHAPE;  // beyond the static scratch
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int dev = -1;
+    DeviceState *d = nullptr;
+    st = ensure_device(s, &dev, &d);
+    if (st != MXFP8_OK) return st;
+    uint16_t *h = nullptr;
+    st = noalloc_scratch_ptr(&h);
+    if (st != MXFP8_OK) return st;
+    KernelArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.sig_table = d->table;
+    a.sig2_table = d->table2;
+    a.fallbacks = d->fallbacks;
+    a.status = d->status;
+    const int64_t chunks = M * ((N + 7) / 8);
+    const int blocks = static_cast<int>(std::min<int64_t>((chunks + 255) / 256, int64_t(d->sms) * 8));
+    swiglu_activation_kernel<<<blocks, 256, 0, s>>>(gate, up, ld_in, M, N, h, ld_h, a);
+    if (cudaGetLastError() != cudaSuccess) return MXFP8_ERR_LAUNCH;
+    // second pass: the standalone cast of the activation just written
+    Spec qs = blank(mx::kQuant, mode, M, N);
+    qs.in[0] = h;
+    qs.ld_in[0] = ld_h;
+    qs.q_row[0] = q_row;
+    qs.s_row[0] = s_row;
+    qs.q_col[0] = q_col;
+    qs.s_col[0] = s_col;
+    qs.ld_qrow = ld_qrow;
+    qs.ld_srow = ld_srow;
+    qs.ld_qcol = ld_qcol;
+    qs.ld_scol = ld_scol;
+    return run(qs, stream);
+}
