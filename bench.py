@@ -46,9 +46,9 @@ PAGES_US = {("fwd", 1): 904.19, ("fwd", 2): 1022.98, ("fwd", 3): 1216.08,
 # captures summarised under profiles/ (small case scaled by the units
 # processed); valid only for the kernel sources they were taken on.
 TRAFFIC = {
-    "bwd_both": (10.52346368e9, "35ce231032847831", "profiles/bwd_both_ncu.md"),
-    "fwd_both": (6.214535168e9, "35ce231032847831", "profiles/fwd_both_ncu.md"),
-    "fwd_col": (5.2343808e9, "35ce231032847831", "profiles/fwd_col_ncu.md"),
+    "bwd_both": (10.52346368e9, "736dc6a9a92a4711", "profiles/bwd_both_ncu.md"),
+    "fwd_both": (6.214535168e9, "736dc6a9a92a4711", "profiles/fwd_both_ncu.md"),
+    "fwd_col": (5.2343808e9, "736dc6a9a92a4711", "profiles/fwd_col_ncu.md"),
 }
 
 
@@ -56,7 +56,10 @@ def kernel_source_hash() -> str:
     import glob
     import hashlib
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "mxfp8_quantization_moe_gb300", "csrc", "*"))):
+    csrc = os.path.join(ROOT, "mxfp8_quantization_moe_gb300", "csrc")
+    files = [os.path.join(csrc, n) for n in ("device.cuh", "kernel.cuh", "launch.cuh")]
+    files += sorted(glob.glob(os.path.join(csrc, "ops_*.cu")))
+    for f in files:
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
