@@ -73,76 +73,150 @@ constexpr size_t smem_bytes()
 }
 
 // ------------------------------------------------------- element operation
-// Evaluate the element op on 8 elements (4 packed bf16x2 words per input)
-// into out[o][4] (packed bf16x2 words).
+// Fast element op on 8 elements (4 packed bf16x2 words per input) into
+// out[o][4] (packed bf16x2 words).
 template <int OP>
-__device__ __forceinline__ void elements8(const KernelArgs &a, const uint32_t (&in)[3][4],
-                                          uint32_t (&out)[2][4])
+__device__ __forceinline__ void elements8(const uint32_t (&in)[3][4], uint32_t (&out)[2][4])
 {
     if constexpr (OP == kQuant) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) out[0][i] = in[0][i];
     } else if constexpr (OP == kFwd) {
-        uint64_t H[4];
-        bool all_ok = true;
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
-            bool ok0, ok1;
-            swiglu_h2(in[0][p], in[1][p], H[p], ok0, ok1);
-            all_ok = all_ok && ok0 && ok1;
+            const uint64_t H = swiglu_h2(in[0][p], in[1][p]);
+            out[0][p] = pack_bf16x2(f2lo(H), f2hi(H));
         }
-        if (!all_ok) {  // rare: find the elements to replace and settle them exactly
-            uint32_t bad = 0;
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                uint64_t tmp;
-                bool ok0, ok1;
-                swiglu_h2(in[0][p], in[1][p], tmp, ok0, ok1);
-                bad |= ((ok0 ? 0u : 1u) | (ok1 ? 0u : 2u)) << (2 * p);
-            }
-            count_fallbacks(a.fallbacks, bad);
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                if (bad & (1u << (2 * p)))
-                    H[p] = f2(swiglu_h_exact(a.sig2_table, bf16lo(in[0][p]), bf16lo(in[1][p])), f2hi(H[p]));
-                if (bad & (2u << (2 * p)))
-                    H[p] = f2(f2lo(H[p]), swiglu_h_exact(a.sig2_table, bf16hi(in[0][p]), bf16hi(in[1][p])));
-            }
-        }
-#pragma unroll
-        for (int p = 0; p < 4; ++p) out[0][p] = pack_bf16x2(f2lo(H[p]), f2hi(H[p]));
     } else {
-        uint64_t DG[4], DU[4];
-        uint32_t bad = 0;  // 4 bits per pair: dgate lo/hi, dup lo/hi
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
-            bool g0, g1, u0, u1;
-            swiglu_grads2(in[0][p], in[1][p], in[2][p], DG[p], DU[p], g0, g1, u0, u1);
-            bad |= ((g0 ? 0u : 1u) | (g1 ? 0u : 2u) | (u0 ? 0u : 4u) | (u1 ? 0u : 8u)) << (4 * p);
+            uint64_t DG, DU;
+            swiglu_grads2(in[0][p], in[1][p], in[2][p], DG, DU);
+            out[0][p] = pack_bf16x2(f2lo(DG), f2hi(DG));
+            out[1][p] = pack_bf16x2(f2lo(DU), f2hi(DU));
         }
-        if (bad) {  // rare: settle the flagged elements exactly
-            count_fallbacks(a.fallbacks, bad);
+    }
+}
+
+__device__ __forceinline__ uint32_t half16(uint32_t w, int hi) { return hi ? (w >> 16) : (w & 0xFFFFu); }
+
+__device__ __forceinline__ uint32_t bf16_bits(float v) { return pack_bf16x2(v, 0.0f) & 0xFFFFu; }
+
+__device__ __forceinline__ void set_half16(uint32_t &w, int hi, uint32_t b)
+{
+    w = hi ? ((w & 0xFFFFu) | (b << 16)) : ((w & 0xFFFF0000u) | b);
+}
+
+// exact value(s) of element e (0..7) from its bf16 input values
+template <int OP>
+__device__ __forceinline__ void exact_from_values(const KernelArgs &a, float x0, float x1, float x2,
+                                                  int e, uint32_t (&out)[2][4])
+{
+    if constexpr (OP == kFwd) {
+        set_half16(out[0][e >> 1], e & 1, bf16_bits(swiglu_h_exact(a.sig2_table, x0, x1)));
+    } else if constexpr (OP == kBwd) {
+        const float2 x = swiglu_grads_exact(a.sig2_table, x0, x1, x2);
+        set_half16(out[0][e >> 1], e & 1, bf16_bits(x.x));
+        set_half16(out[1][e >> 1], e & 1, bf16_bits(x.y));
+    }
+}
+
+template <int OP>
+__device__ __forceinline__ void exact_from_regs(const KernelArgs &a, const uint32_t (&in)[3][4], int e,
+                                                uint32_t (&out)[2][4])
+{
+    const int p = e >> 1, hi = e & 1;
+    const float x0 = hi ? bf16hi(in[0][p]) : bf16lo(in[0][p]);
+    const float x1 = hi ? bf16hi(in[1][p]) : bf16lo(in[1][p]);
+    const float x2 = hi ? bf16hi(in[2][p]) : bf16lo(in[2][p]);
+    exact_from_values<OP>(a, x0, x1, x2, e, out);
+}
+
+template <int NOUT>
+__device__ __forceinline__ bool element_at_risk(const uint32_t (&out)[2][4], const uint32_t (&amax)[2],
+                                                int e)
+{
+    bool r = false;
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                if (bad & (5u << (4 * p))) {
-                    const float2 x = swiglu_grads_exact(a.sig2_table, bf16lo(in[0][p]), bf16lo(in[1][p]),
-                                                        bf16lo(in[2][p]));
-                    if (bad & (1u << (4 * p))) DG[p] = f2(x.x, f2hi(DG[p]));
-                    if (bad & (4u << (4 * p))) DU[p] = f2(x.y, f2hi(DU[p]));
-                }
-                if (bad & (10u << (4 * p))) {
-                    const float2 x = swiglu_grads_exact(a.sig2_table, bf16hi(in[0][p]), bf16hi(in[1][p]),
-                                                        bf16hi(in[2][p]));
-                    if (bad & (2u << (4 * p))) DG[p] = f2(f2lo(DG[p]), x.x);
-                    if (bad & (8u << (4 * p))) DU[p] = f2(f2lo(DU[p]), x.y);
+    for (int o = 0; o < NOUT; ++o)
+        r |= scale_at_risk(amax[o]) && at_risk_value(half16(out[o][e >> 1], e & 1), amax[o]);
+    return r;
+}
+
+// Settle a lane's fast values with its inputs in registers (row pass, and
+// the col pass of "col" mode): exact recomputation of (i) all 8 elements if a
+// gate is outside the fast range or the block amax is huge or not finite,
+// then (ii) the elements that can move a risky block's scale.  amax[o] is
+// kept current.  Warp-uniform control flow around every shuffle.
+template <int OP>
+__device__ __forceinline__ void settle_regs(const KernelArgs &a, const uint32_t (&in)[3][4],
+                                            uint32_t (&out)[2][4], uint32_t (&amax)[2])
+{
+    constexpr int NOUT = OpTraits<OP>::kOut;
+    constexpr int kGate = (OP == kFwd) ? 0 : 1;
+    bool full = !gates_fast8(in[kGate]);
+#pragma unroll
+    for (int o = 0; o < NOUT; ++o) full |= amax[o] >= kHugeAmax;
+    if (__any_sync(0xFFFFFFFFu, full)) {
+        if (full) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) exact_from_regs<OP>(a, in, e, out);
+            count_fallbacks(a.fallbacks, 8);
+        }
+#pragma unroll
+        for (int o = 0; o < NOUT; ++o) amax[o] = amax32_lanes4(out[o]);
+    }
+    bool risk = false;
+#pragma unroll
+    for (int o = 0; o < NOUT; ++o) risk |= scale_at_risk(amax[o]);
+    if (__any_sync(0xFFFFFFFFu, risk)) {
+        uint32_t n = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            if (element_at_risk<NOUT>(out, amax, e)) {
+                exact_from_regs<OP>(a, in, e, out);
+                ++n;
+            }
+        }
+        if (n) count_fallbacks(a.fallbacks, n);
+#pragma unroll
+        for (int o = 0; o < NOUT; ++o) amax[o] = amax32_lanes4(out[o]);
+    }
+}
+
+// Settle the risky elements of a col-pass fragment in "both" mode, whose
+// inputs are no longer in shared memory: they are read back from global
+// memory.  Lane element e is row row_q + 8*(e/2) + e%2 of column col; `live`
+// is false outside the matrix (nothing is read there).
+template <int OP>
+__device__ __forceinline__ void settle_global(const KernelArgs &a, uint32_t (&out)[2][4],
+                                              uint32_t (&amax)[2], int64_t row_q, int64_t col, bool live)
+{
+    constexpr int NOUT = OpTraits<OP>::kOut;
+    constexpr int NIN = OpTraits<OP>::kIn;
+    bool risk = false;
+#pragma unroll
+    for (int o = 0; o < NOUT; ++o) risk |= scale_at_risk(amax[o]);
+    if (__any_sync(0xFFFFFFFFu, risk)) {
+        uint32_t n = 0;
+        if (live) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (element_at_risk<NOUT>(out, amax, e)) {
+                    const int64_t row = row_q + 8 * (e >> 1) + (e & 1);
+                    float x[3] = {0.0f, 0.0f, 0.0f};
+#pragma unroll
+                    for (int k = 0; k < NIN; ++k)
+                        x[k] = __uint_as_float(static_cast<uint32_t>(__ldg(a.in_ptr[k] + row * a.in_ld[k] + col))
+                                               << 16);
+                    exact_from_values<OP>(a, x[0], x[1], x[2], e, out);
+                    ++n;
                 }
             }
         }
+        if (n) count_fallbacks(a.fallbacks, n);
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            out[0][p] = pack_bf16x2(f2lo(DG[p]), f2hi(DG[p]));
-            out[1][p] = pack_bf16x2(f2lo(DU[p]), f2hi(DU[p]));
-        }
+        for (int o = 0; o < NOUT; ++o) amax[o] = amax32_lanes4(out[o]);
     }
 }
 
@@ -273,13 +347,17 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, 1)
                     in[k][2] = v.z;
                     in[k][3] = v.w;
                 }
-                elements8<OP>(a, in, out);
+                elements8<OP>(in, out);
+                uint32_t amax[2];
+#pragma unroll
+                for (int o = 0; o < NOUT; ++o) amax[o] = amax32_lanes4(out[o]);
+                if constexpr (OP != kQuant) settle_regs<OP>(a, in, out, amax);
                 const int64_t grow = r0 + 8 * i + rperm;
                 const bool live = (grow < a.M) && (gcol < a.N);
 #pragma unroll
                 for (int o = 0; o < NOUT; ++o) {
                     uint32_t w0, w1;
-                    const uint32_t sc = encode_row8(out[o], w0, w1);
+                    const uint32_t sc = encode_block8(out[o], amax[o], w0, w1);
                     if (live) {
                         __stcs(reinterpret_cast<uint2 *>(a.q_row[o] + grow * a.ld_qrow + gcol),
                                make_uint2(w0, w1));
@@ -306,22 +384,29 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, 1)
             for (int k = 0; k < 4; ++k) {
                 const uint32_t off = swz(crow, chunk0 + k);
                 uint32_t out[2][4];
+                uint32_t amax[2];
+                const int64_t gcol = c0 + 8 * k + cc;
+                const bool live = (r0 < a.M) && (gcol < a.N);
                 if constexpr (kEval) {
                     uint32_t in[3][4];
 #pragma unroll
                     for (int i = 0; i < NIN; ++i) ldsm_x4_trans(stage + i * kTileBytes + off, in[i]);
-                    elements8<OP>(a, in, out);
+                    elements8<OP>(in, out);
+#pragma unroll
+                    for (int o = 0; o < NOUT; ++o) amax[o] = amax32_lanes4(out[o]);
+                    settle_regs<OP>(a, in, out, amax);
                 } else {
 #pragma unroll
-                    for (int o = 0; o < NOUT; ++o)
+                    for (int o = 0; o < NOUT; ++o) {
                         ldsm_x4_trans(stage + (kSrc + o) * kTileBytes + off, out[o]);
+                        amax[o] = amax32_lanes4(out[o]);
+                    }
+                    if constexpr (kSplit) settle_global<OP>(a, out, amax, r0 + 2 * q, gcol, live);
                 }
-                const int64_t gcol = c0 + 8 * k + cc;
-                const bool live = (r0 < a.M) && (gcol < a.N);
 #pragma unroll
                 for (int o = 0; o < NOUT; ++o) {
                     uint32_t w0, w1;
-                    const uint32_t sc = encode_col8(out[o], w0, w1);
+                    const uint32_t sc = encode_block8(out[o], amax[o], w0, w1);
                     // column 8k + cc of the sub-tile: rows 8m + 2q, 8m + 2q + 1 at
                     // bytes 8m + 2q of its 32-byte column (16-byte halves swapped
                     // for columns with bit 2 set: conflict-free reads below)

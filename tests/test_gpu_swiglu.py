@@ -2,8 +2,9 @@
 
 Tolerance (stated for the SwiGLU paths): E8M0 scales bit-exact; at most 1e-4
 of the E4M3 codes may differ from the oracle, each by at most one code.  The
-activation is rounded to bf16 once from an fp32-accurate value in both, so
-the expected number of differing codes is zero; the tests report it.
+kernels keep a fast activation value (within one bf16 step of the correctly
+rounded one) except where it could move a scale, so a few codes per million
+may differ; every comparison checks the bound and the totals are printed.
 
 Workloads: the packed (128, 128) forward; the (4096, 7168) mix of per-row
 2^k scaling and zeroed 32-blocks (full comparison); the (16384, 7168)
@@ -110,7 +111,10 @@ def compare(got, want, what=""):
         if k.startswith("s_"):
             assert np.array_equal(g, w), "%s %s: scales differ at %d places" % (what, k, int((g != w).sum()))
         else:
-            n += compare_codes(g, w, CODE_TOL, what + " " + k)
+            d = compare_codes(g, w, CODE_TOL, what + " " + k)
+            if d:
+                print("%s %s: %d of %d codes differ by one" % (what, k, d, g.size))
+            n += d
     return n
 
 
@@ -143,7 +147,7 @@ def rand_inputs(M, N, seed, std=(2.0, 1.0, 0.05)):
 def test_fwd_small(shape, mode):
     gate, up, _ = rand_inputs(*shape, seed=shape[0] + mode)
     got = fwd_gpu(gate, up, mode)
-    assert compare(got, oracle_fwd(gate, up, mode), what="fwd") == 0
+    compare(got, oracle_fwd(gate, up, mode), what="fwd")
 
 
 @pytest.mark.parametrize("shape", [(32, 64), (160, 96), (256, 320), (1024, 576)], ids=lambda s: "%dx%d" % s)
@@ -152,8 +156,8 @@ def test_bwd_small(shape, mode):
     gate, up, dh = rand_inputs(*shape, seed=shape[1] + mode)
     dg, du = bwd_gpu(dh, gate, up, mode)
     wg, wu = oracle_bwd(dh, gate, up, mode)
-    assert compare(dg, wg, what="dgate") == 0
-    assert compare(du, wu, what="dup") == 0
+    compare(dg, wg, what="dgate")
+    compare(du, wu, what="dup")
 
 
 def test_fwd_packed_128x128_rowwise():
@@ -161,7 +165,7 @@ def test_fwd_packed_128x128_rowwise():
     buf, gate, up = synthetic.fwd_128x128(device="cuda")
     for mode in (1, 2, 3):
         got = fwd_gpu(gate, up, mode)
-        assert compare(got, oracle_fwd(gate, up, mode), what="fwd128") == 0
+        compare(got, oracle_fwd(gate, up, mode), what="fwd128")
 
 
 # ----------------------------------------------------------- every gate
@@ -181,7 +185,7 @@ def test_fwd_every_bf16_gate(useed):
         up.fill_(1.0)
     for mode in (1, 2):
         got = fwd_gpu(gate, up, mode)
-        assert compare(got, oracle_fwd(gate, up, mode), what="fwd-all-g") == 0
+        compare(got, oracle_fwd(gate, up, mode), what="fwd-all-g")
 
 
 @pytest.mark.parametrize("useed", [0, 1])
@@ -196,8 +200,8 @@ def test_bwd_every_bf16_gate(useed):
     for mode in (1, 2):
         dg, du = bwd_gpu(dh, gate, up, mode)
         wg, wu = oracle_bwd(dh, gate, up, mode)
-        assert compare(dg, wg, what="dgate-all-g") == 0
-        assert compare(du, wu, what="dup-all-g") == 0
+        compare(dg, wg, what="dgate-all-g")
+        compare(du, wu, what="dup-all-g")
 
 
 def test_fwd_amax_at_e4m3_boundary():
@@ -220,7 +224,7 @@ def test_fwd_amax_at_e4m3_boundary():
     up[rows, cols] = u_new.to(torch.bfloat16)
     for mode in (1, 2, 3):
         got = fwd_gpu(gate, up, mode)
-        assert compare(got, oracle_fwd(gate, up, mode), what="fwd-boundary") == 0
+        compare(got, oracle_fwd(gate, up, mode), what="fwd-boundary")
 
 
 # ------------------------------------------------------- pages' workloads
@@ -232,7 +236,7 @@ def test_mixed_4096x7168_both_full():
     dg, du = bwd_gpu(dh, gate, up, 3)
     wg, wu = oracle_bwd(dh, gate, up, 3)
     n += compare(dg, wg, what="mixed dgate") + compare(du, wu, what="mixed dup")
-    assert n == 0
+    print("differing codes:", n)
 
 
 def sample_blocks(M, count, seed):
@@ -251,7 +255,7 @@ def test_outlier_16384x7168_sampled(mode):
     dg, du = bwd_gpu(dh, gate, up, mode, rows)
     wg, wu = oracle_bwd(dh, gate, up, mode, rows)
     n += compare(dg, wg, what="outlier dgate") + compare(du, wu, what="outlier dup")
-    assert n == 0
+    print("differing codes:", n)
 
 
 @pytest.mark.parametrize("mode", [1, 2, 3])
@@ -263,7 +267,7 @@ def test_large_131072x8192_sampled(mode):
     dg, du = bwd_gpu(dh, gate, up, mode, rows)
     wg, wu = oracle_bwd(dh, gate, up, mode, rows)
     n += compare(dg, wg, what="large dgate") + compare(du, wu, what="large dup")
-    assert n == 0
+    print("differing codes:", n)
 
 
 def test_status_clean_and_fallback_path_used():
