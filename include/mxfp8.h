@@ -177,7 +177,8 @@ mxfp8_status mxfp8_swiglu_fwd_noalloc(const uint16_t *gate, const uint16_t *up, 
  * pipeline wait that exceeds its limit (about a second) makes the kernel set
  * a flag bit and return.  flags: bit 0 consumer wait, bit 1 producer wait,
  * bit 2 drain wait, bit 3 self-test wait.  fallbacks: number of SwiGLU
- * elements whose bf16 rounding was settled by the double-precision path.
+ * elements the fused kernels recomputed exactly (values near a scale
+ * boundary, gates outside the fast range, huge or non-finite blocks).
  * Synchronizes `stream`; with reset != 0 clears both afterwards.
  * Either output pointer (host memory) may be NULL.
  */
@@ -186,10 +187,11 @@ mxfp8_status mxfp8_device_status(uint32_t *flags, uint64_t *fallbacks, int reset
 /*
  * Self-test of the SwiGLU fast path: writes, for every bf16 bit pattern g
  * (index g), the fp32 factors the kernels compute -- out[k*65536 + g] for
- * k = 0 sigmoid(g), 1 silu(g), 2 1 - sigmoid(g), 3 1 + g(1 - sigmoid(g)),
- * 4 silu'(g).  `out` is a device buffer of 5 * 65536 floats, 16-byte
- * aligned.  The tests compare these with the exact factors to show that the
- * fast path stays far within one bf16 step everywhere.
+ * k = 0 sigmoid(g), 1 2^60 silu(g) (the forward's scaled form), 2 1 -
+ * sigmoid(g), 3 1 + g(1 - sigmoid(g)), 4 silu'(g).  `out` is a device buffer
+ * of 5 * 65536 floats, 16-byte aligned.  The tests compare these with the
+ * exact factors: the error bounds they establish are the ones the fused
+ * kernels' recomputation windows are sized for.
  */
 mxfp8_status mxfp8_selftest_activation(float *out, void *stream);
 

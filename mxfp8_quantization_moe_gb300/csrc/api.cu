@@ -65,10 +65,10 @@ __global__ void selftest_activation_kernel(float *out)
     if (i >= 65536u) return;
     const uint64_t G = mx::f2(__uint_as_float(i << 16), __uint_as_float((i + 1) << 16));
     uint64_t T;
-    const uint64_t S = mx::sigmoid2(G, T);
+    const uint64_t S = mx::sigmoid2(G, T, 1.0f);
     const uint64_t SN = mx::mul2(T, S);
     const uint64_t W = mx::fma2(G, SN, mx::f2(1.0f, 1.0f));
-    const uint64_t V[5] = {S, mx::mul2(G, S), SN, W, mx::mul2(S, W)};
+    const uint64_t V[5] = {S, mx::silu2_up(G), SN, W, mx::mul2(S, W)};
     for (int k = 0; k < 5; ++k) {
         out[k * 65536 + i] = mx::f2lo(V[k]);
         out[k * 65536 + i + 1] = mx::f2hi(V[k]);
@@ -329,10 +329,6 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     a.ld_scol = s.ld_scol;
     a.group_rows = s.group_rows > 0 ? s.group_rows : s.M;
     a.group_stride = s.group_stride;
-    for (int i = 0; i < 3; ++i) {
-        a.in_ptr[i] = static_cast<const uint16_t *>(s.in[i]);
-        a.in_ld[i] = s.ld_in[i];
-    }
     a.sig_table = d->table;
     a.sig2_table = d->table2;
     a.status = d->status;

@@ -74,10 +74,15 @@ constexpr size_t smem_bytes()
 
 // ------------------------------------------------------- element operation
 // Fast element op on 8 elements (4 packed bf16x2 words per input) into
-// out[o][4] (packed bf16x2 words).
-template <int OP>
-__device__ __forceinline__ void elements8(const uint32_t (&in)[3][4], uint32_t (&out)[2][4])
+// out[o][4] (packed bf16x2 words).  With kKeep the fp32 pairs are kept in
+// hv[o][4] for a later look (returns 0); without it the pairs (bit p:
+// elements 2p and 2p+1) holding a value near a 0x60/0x61 rounding midpoint
+// are returned.
+template <int OP, bool kKeep>
+__device__ __forceinline__ uint32_t elements8(const uint32_t (&in)[3][4], uint32_t (&out)[2][4],
+                                              uint64_t (&hv)[2][4])
 {
+    uint32_t near = 0;
     if constexpr (OP == kQuant) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) out[0][i] = in[0][i];
@@ -86,6 +91,8 @@ __device__ __forceinline__ void elements8(const uint32_t (&in)[3][4], uint32_t (
         for (int p = 0; p < 4; ++p) {
             const uint64_t H = swiglu_h2(in[0][p], in[1][p]);
             out[0][p] = pack_bf16x2(f2lo(H), f2hi(H));
+            if constexpr (kKeep) hv[0][p] = H;
+            else near |= static_cast<uint32_t>(near_mid2(H, kNearH)) << p;
         }
     } else {
 #pragma unroll
@@ -94,11 +101,16 @@ __device__ __forceinline__ void elements8(const uint32_t (&in)[3][4], uint32_t (
             swiglu_grads2(in[0][p], in[1][p], in[2][p], DG, DU);
             out[0][p] = pack_bf16x2(f2lo(DG), f2hi(DG));
             out[1][p] = pack_bf16x2(f2lo(DU), f2hi(DU));
+            if constexpr (kKeep) {
+                hv[0][p] = DG;
+                hv[1][p] = DU;
+            } else {
+                near |= static_cast<uint32_t>(near_mid2(DG, kNearDgate) | near_mid2(DU, kNearDup)) << p;
+            }
         }
     }
+    return near;
 }
-
-__device__ __forceinline__ uint32_t half16(uint32_t w, int hi) { return hi ? (w >> 16) : (w & 0xFFFFu); }
 
 __device__ __forceinline__ uint32_t bf16_bits(float v) { return pack_bf16x2(v, 0.0f) & 0xFFFFu; }
 
@@ -107,114 +119,70 @@ __device__ __forceinline__ void set_half16(uint32_t &w, int hi, uint32_t b)
     w = hi ? ((w & 0xFFFFu) | (b << 16)) : ((w & 0xFFFF0000u) | b);
 }
 
-// exact value(s) of element e (0..7) from its bf16 input values
+// exact value(s) of element e (0..7) from the inputs in registers
 template <int OP>
-__device__ __forceinline__ void exact_from_values(const KernelArgs &a, float x0, float x1, float x2,
-                                                  int e, uint32_t (&out)[2][4])
-{
-    if constexpr (OP == kFwd) {
-        set_half16(out[0][e >> 1], e & 1, bf16_bits(swiglu_h_exact(a.sig2_table, x0, x1)));
-    } else if constexpr (OP == kBwd) {
-        const float2 x = swiglu_grads_exact(a.sig2_table, x0, x1, x2);
-        set_half16(out[0][e >> 1], e & 1, bf16_bits(x.x));
-        set_half16(out[1][e >> 1], e & 1, bf16_bits(x.y));
-    }
-}
-
-template <int OP>
-__device__ __forceinline__ void exact_from_regs(const KernelArgs &a, const uint32_t (&in)[3][4], int e,
-                                                uint32_t (&out)[2][4])
+__device__ __forceinline__ void exact_element(const KernelArgs &a, const uint32_t (&in)[3][4], int e,
+                                              uint32_t (&out)[2][4])
 {
     const int p = e >> 1, hi = e & 1;
     const float x0 = hi ? bf16hi(in[0][p]) : bf16lo(in[0][p]);
     const float x1 = hi ? bf16hi(in[1][p]) : bf16lo(in[1][p]);
-    const float x2 = hi ? bf16hi(in[2][p]) : bf16lo(in[2][p]);
-    exact_from_values<OP>(a, x0, x1, x2, e, out);
+    if constexpr (OP == kFwd) {
+        set_half16(out[0][p], hi, bf16_bits(swiglu_h_exact(a.sig2_table, x0, x1)));
+    } else if constexpr (OP == kBwd) {
+        const float x2 = hi ? bf16hi(in[2][p]) : bf16lo(in[2][p]);
+        const float2 x = swiglu_grads_exact(a.sig2_table, x0, x1, x2);
+        set_half16(out[0][p], hi, bf16_bits(x.x));
+        set_half16(out[1][p], hi, bf16_bits(x.y));
+    }
 }
 
-template <int NOUT>
-__device__ __forceinline__ bool element_at_risk(const uint32_t (&out)[2][4], const uint32_t (&amax)[2],
-                                                int e)
-{
-    bool r = false;
-#pragma unroll
-    for (int o = 0; o < NOUT; ++o)
-        r |= scale_at_risk(amax[o]) && at_risk_value(half16(out[o][e >> 1], e & 1), amax[o]);
-    return r;
-}
-
-// Settle a lane's fast values with its inputs in registers (row pass, and
-// the col pass of "col" mode): exact recomputation of (i) all 8 elements if a
-// gate is outside the fast range or the block amax is huge or not finite,
-// then (ii) the elements that can move a risky block's scale.  amax[o] is
-// kept current.  Warp-uniform control flow around every shuffle.
-template <int OP>
-__device__ __forceinline__ void settle_regs(const KernelArgs &a, const uint32_t (&in)[3][4],
-                                            uint32_t (&out)[2][4], uint32_t (&amax)[2])
+// Settle a lane's fast values (row pass; col pass of "col" mode): exact
+// recomputation of all 8 elements if a gate is outside the fast range or the
+// block amax is huge or not finite; otherwise of the pairs near a 0x60/0x61
+// rounding midpoint.  With kKeep the midpoint test runs only in blocks whose
+// fast amax has mantissa 0x60 or 0x61 -- a scale can move nowhere else --
+// on the kept fp32 values; without it `near` holds the test's result for
+// every pair (needed when the values also feed the other direction's
+// blocks).  amax[o] is kept current.  Warp-uniform control flow around every
+// shuffle.
+template <int OP, bool kKeep>
+__device__ __forceinline__ void settle(const KernelArgs &a, const uint32_t (&in)[3][4],
+                                       uint32_t (&out)[2][4], uint32_t (&amax)[2], uint32_t near,
+                                       const uint64_t (&hv)[2][4])
 {
     constexpr int NOUT = OpTraits<OP>::kOut;
     constexpr int kGate = (OP == kFwd) ? 0 : 1;
     bool full = !gates_fast8(in[kGate]);
 #pragma unroll
     for (int o = 0; o < NOUT; ++o) full |= amax[o] >= kHugeAmax;
-    if (__any_sync(0xFFFFFFFFu, full)) {
-        if (full) {
+    if constexpr (kKeep) {
+        bool risk = false;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) exact_from_regs<OP>(a, in, e, out);
-            count_fallbacks(a.fallbacks, 8);
-        }
+        for (int o = 0; o < NOUT; ++o) risk |= scale_at_risk(amax[o]);
+        if (!__any_sync(0xFFFFFFFFu, full || risk)) return;
+        if (risk) {
 #pragma unroll
-        for (int o = 0; o < NOUT; ++o) amax[o] = amax32_lanes4(out[o]);
-    }
-    bool risk = false;
+            for (int p = 0; p < 4; ++p) {
+                bool n = false;
 #pragma unroll
-    for (int o = 0; o < NOUT; ++o) risk |= scale_at_risk(amax[o]);
-    if (__any_sync(0xFFFFFFFFu, risk)) {
-        uint32_t n = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            if (element_at_risk<NOUT>(out, amax, e)) {
-                exact_from_regs<OP>(a, in, e, out);
-                ++n;
+                for (int o = 0; o < NOUT; ++o)
+                    n |= scale_at_risk(amax[o]) &&
+                         near_mid2(hv[o][p], (OP == kFwd) ? kNearH : (o == 0 ? kNearDgate : kNearDup));
+                near |= static_cast<uint32_t>(n) << p;
             }
         }
-        if (n) count_fallbacks(a.fallbacks, n);
-#pragma unroll
-        for (int o = 0; o < NOUT; ++o) amax[o] = amax32_lanes4(out[o]);
     }
-}
-
-// Settle the risky elements of a col-pass fragment in "both" mode, whose
-// inputs are no longer in shared memory: they are read back from global
-// memory.  Lane element e is row row_q + 8*(e/2) + e%2 of column col; `live`
-// is false outside the matrix (nothing is read there).
-template <int OP>
-__device__ __forceinline__ void settle_global(const KernelArgs &a, uint32_t (&out)[2][4],
-                                              uint32_t (&amax)[2], int64_t row_q, int64_t col, bool live)
-{
-    constexpr int NOUT = OpTraits<OP>::kOut;
-    constexpr int NIN = OpTraits<OP>::kIn;
-    bool risk = false;
+    if (full) near = 0xFu;
+    if (__any_sync(0xFFFFFFFFu, near != 0u)) {
 #pragma unroll
-    for (int o = 0; o < NOUT; ++o) risk |= scale_at_risk(amax[o]);
-    if (__any_sync(0xFFFFFFFFu, risk)) {
-        uint32_t n = 0;
-        if (live) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                if (element_at_risk<NOUT>(out, amax, e)) {
-                    const int64_t row = row_q + 8 * (e >> 1) + (e & 1);
-                    float x[3] = {0.0f, 0.0f, 0.0f};
-#pragma unroll
-                    for (int k = 0; k < NIN; ++k)
-                        x[k] = __uint_as_float(static_cast<uint32_t>(__ldg(a.in_ptr[k] + row * a.in_ld[k] + col))
-                                               << 16);
-                    exact_from_values<OP>(a, x[0], x[1], x[2], e, out);
-                    ++n;
-                }
+        for (int p = 0; p < 4; ++p) {
+            if ((near >> p) & 1u) {
+                exact_element<OP>(a, in, 2 * p, out);
+                exact_element<OP>(a, in, 2 * p + 1, out);
             }
         }
-        if (n) count_fallbacks(a.fallbacks, n);
+        count_fallbacks_warp(a.fallbacks, 2u * __popc(near));
 #pragma unroll
         for (int o = 0; o < NOUT; ++o) amax[o] = amax32_lanes4(out[o]);
     }
@@ -316,6 +284,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, 1)
     uint8_t *stg = staging + warp * NOUT * 1024;   // this warp's colwise staging
 
     constexpr bool kSplit = (MODE == kBoth) && (OP != kQuant);  // values handed row -> col pass
+    constexpr bool kKeep = !kSplit;   // midpoint test deferred to risky blocks
     constexpr int kUnroll = (OP == kQuant) ? 4 : 1;  // the cast alone: unroll for ILP
     int it = 0;
     for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
@@ -339,6 +308,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, 1)
                 const uint32_t off = swz(row, chunk0 + q);
                 uint32_t in[3][4];
                 uint32_t out[2][4];
+                uint64_t hv[2][4];
 #pragma unroll
                 for (int k = 0; k < NIN; ++k) {
                     const uint4 v = *reinterpret_cast<const uint4 *>(stage_ptr + k * kTileBytes + off);
@@ -347,11 +317,11 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, 1)
                     in[k][2] = v.z;
                     in[k][3] = v.w;
                 }
-                elements8<OP>(in, out);
+                const uint32_t near = elements8<OP, kKeep>(in, out, hv);
                 uint32_t amax[2];
 #pragma unroll
                 for (int o = 0; o < NOUT; ++o) amax[o] = amax32_lanes4(out[o]);
-                if constexpr (OP != kQuant) settle_regs<OP>(a, in, out, amax);
+                if constexpr (OP != kQuant) settle<OP, kKeep>(a, in, out, amax, near, hv);
                 const int64_t grow = r0 + 8 * i + rperm;
                 const bool live = (grow < a.M) && (gcol < a.N);
 #pragma unroll
@@ -389,19 +359,19 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, 1)
                 const bool live = (r0 < a.M) && (gcol < a.N);
                 if constexpr (kEval) {
                     uint32_t in[3][4];
+                    uint64_t hv[2][4];
 #pragma unroll
                     for (int i = 0; i < NIN; ++i) ldsm_x4_trans(stage + i * kTileBytes + off, in[i]);
-                    elements8<OP>(in, out);
+                    const uint32_t near = elements8<OP, true>(in, out, hv);
 #pragma unroll
                     for (int o = 0; o < NOUT; ++o) amax[o] = amax32_lanes4(out[o]);
-                    settle_regs<OP>(a, in, out, amax);
+                    settle<OP, true>(a, in, out, amax, near, hv);
                 } else {
 #pragma unroll
                     for (int o = 0; o < NOUT; ++o) {
                         ldsm_x4_trans(stage + (kSrc + o) * kTileBytes + off, out[o]);
                         amax[o] = amax32_lanes4(out[o]);
                     }
-                    if constexpr (kSplit) settle_global<OP>(a, out, amax, r0 + 2 * q, gcol, live);
                 }
 #pragma unroll
                 for (int o = 0; o < NOUT; ++o) {

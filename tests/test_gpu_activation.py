@@ -1,14 +1,13 @@
 """Exhaustive check of the SwiGLU fast path's accuracy.
 
 The fused kernels keep the fast fp32 activation (and gradient) values and
-round them to bf16.  Their correctness argument rests on one fact: for every
-bf16 gate value g in the fast range (g >= -64) the fast factors' relative
-error is far below one bf16 step (2^-8), so a fast bf16 value is the
-correctly rounded one or an adjacent bf16.  That caps every code difference
-at one code and confines scale changes to blocks whose amax mantissa is 0x60
-or 0x61, which the kernels recompute exactly.  The gate takes only 65536
-values, so the fact is checked for all of them against the oracle's
-double-precision sigmoid, with a wide margin (2^-12).
+round them to bf16, recomputing exactly only the elements whose fast value
+lies within a window around a 0x60/0x61 bf16 rounding midpoint (where a
+scale byte could move).  The windows (64 fp32 ulps for h and dup, 1024 for
+dgate) are sized, with a margin of at least 2, from error bounds on the
+gate-only factors: sigmoid and silu within 32 units of 2^-24, silu' within
+512.  The gate takes only 65536 values, so those bounds are checked here for
+all of them against the oracle's double-precision sigmoid.
 """
 import numpy as np
 import pytest
@@ -20,7 +19,7 @@ from mxfp8_quantization_moe_gb300 import capi, init
 pytestmark = pytest.mark.gpu
 
 
-def test_fast_path_error_is_far_below_one_bf16_step_for_every_gate():
+def test_fast_path_error_bounds_for_every_gate():
     init()
     out = torch.empty(5 * 65536, dtype=torch.float32, device="cuda")
     assert capi.mxfp8_selftest_activation(out.data_ptr(), torch.cuda.current_stream().cuda_stream) == 0
@@ -38,15 +37,27 @@ def test_fast_path_error_is_far_below_one_bf16_step_for_every_gate():
     dsilu = sig * w
 
     def rel(a, b):
-        with np.errstate(divide="ignore", invalid="ignore"):
+        with np.errstate(divide="ignore", invalid="ignore", over="ignore"):
             r = np.abs(a - b) / np.abs(b)
         r[(a == b)] = 0.0
         return r
 
     u = 2.0 ** -24
-    errs = {"sigma": rel(v[0][fast], sig) / u, "silu": rel(v[1][fast], silu) / u,
-            "1-sigma": rel(v[2][fast], sn) / u, "silu'": rel(v[4][fast], dsilu) / u}
+    # the forward's silu comes scaled by 2^60: finite for every gate up to
+    # 2^67 (beyond, it overflows to Inf, which the kernels recompute exactly)
+    silu_up = v[1][fast] / 2.0 ** 60
+    fin = np.abs(gf) < 2.0 ** 67
+    assert np.all(np.isfinite(silu_up[fin]))
+    assert np.all(np.isinf(silu_up[~fin]) | (rel(silu_up[~fin], silu[~fin]) <= 32 * 2.0 ** -24))
+    # 1 - sigma is checked while it is a normal fp32 number with room to
+    # spare; below 2^-100 the fast e^-g may flush to zero, harmlessly: there
+    # g (1 - sigma) < 2^-90 vanishes against the 1 it is added to in silu'
+    normal = sn >= 2.0 ** -100
+    errs = {"sigma": (rel(v[0][fast], sig) / u, 32),
+            "silu": (rel(silu_up[fin], silu[fin]) / u, 32),
+            "1-sigma": (rel(v[2][fast][normal], sn[normal]) / u, 64),
+            "silu'": (rel(v[4][fast], dsilu) / u, 512)}
     print("max fast-path relative error (units of 2^-24): " +
-          ", ".join("%s %.2f" % (k, e.max()) for k, e in errs.items()))
-    for k, e in errs.items():
-        assert np.all(np.isfinite(e)) and e.max() < 2.0 ** 12, (k, gf[np.argmax(e)])
+          ", ".join("%s %.2f" % (k, e.max()) for k, (e, _) in errs.items()))
+    for k, (e, bound) in errs.items():
+        assert np.all(np.isfinite(e)) and e.max() <= bound, (k, e.max(), bound)
