@@ -15,10 +15,10 @@
 //             shuffles, each lane stores its 8 E4M3 codes (the four lanes: 32
 //             contiguous bytes).
 //   col pass: four 32-row x 8-column units; ldmatrix.trans gives four lanes
-//             one column of a unit, which is encoded colwise; the codes are
-//             transposed through a warp-private staging buffer and each lane
-//             stores one column's 32 codes (32 contiguous bytes of the
-//             column-major output).
+//             one column of a unit, which is encoded colwise; stmatrix moves
+//             the codes into a warp-private staging buffer, column by column,
+//             and each lane stores one column's 32 codes (32 contiguous bytes
+//             of the column-major output).
 // In "both" mode the row pass writes the bf16 element values back into the
 // stage (over an input it no longer needs), so both scale sets come from one
 // read of the inputs.  In "col" mode the element op runs directly on the
@@ -301,7 +301,21 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, 1)
         uint8_t *stage_ptr = smem + static_cast<size_t>(s * NIN) * kTileBytes + box_off;
 
         if constexpr (MODE & kRow) {
+            // this lane's rows are r0 + 8i + rperm; all addressing is set up
+            // once per tile
             const int64_t gcol = c0 + 8 * q;
+            const int64_t grow0 = r0 + rperm;
+            const int64_t left64 = a.M - grow0;
+            const int rows_left = left64 > 32 ? 32 : static_cast<int>(left64 < 0 ? 0 : left64);
+            const bool col_ok = gcol < a.N;
+            uint8_t *qp[2];
+            uint8_t *sp[2];
+#pragma unroll
+            for (int o = 0; o < NOUT; ++o) {
+                qp[o] = a.q_row[o] + grow0 * a.ld_qrow + gcol;
+                sp[o] = a.s_row[o] + grow0 * a.ld_srow + (gcol >> 5);
+            }
+            const int64_t qstep = 8 * a.ld_qrow, sstep = 8 * a.ld_srow;
 #pragma unroll kUnroll
             for (int i = 0; i < 4; ++i) {
                 const uint32_t row = kSub * srb + 8u * i + rperm;
@@ -322,17 +336,17 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, 1)
 #pragma unroll
                 for (int o = 0; o < NOUT; ++o) amax[o] = amax32_lanes4(out[o]);
                 if constexpr (OP != kQuant) settle<OP, kKeep>(a, in, out, amax, near, hv);
-                const int64_t grow = r0 + 8 * i + rperm;
-                const bool live = (grow < a.M) && (gcol < a.N);
+                const bool live = col_ok && (8 * i < rows_left);
 #pragma unroll
                 for (int o = 0; o < NOUT; ++o) {
                     uint32_t w0, w1;
                     const uint32_t sc = encode_block8(out[o], amax[o], w0, w1);
                     if (live) {
-                        __stcs(reinterpret_cast<uint2 *>(a.q_row[o] + grow * a.ld_qrow + gcol),
-                               make_uint2(w0, w1));
-                        if (q == 0) a.s_row[o][grow * a.ld_srow + (gcol >> 5)] = static_cast<uint8_t>(sc);
+                        __stcs(reinterpret_cast<uint2 *>(qp[o]), make_uint2(w0, w1));
+                        if (q == 0) *sp[o] = static_cast<uint8_t>(sc);
                     }
+                    qp[o] += qstep;
+                    sp[o] += sstep;
                     if constexpr (kSplit) {
                         *reinterpret_cast<uint4 *>(stage_ptr + (NIN - NOUT + o) * kTileBytes + off) =
                             make_uint4(out[o][0], out[o][1], out[o][2], out[o][3]);
@@ -349,14 +363,24 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, 1)
             constexpr int kSrc = (MODE == kBoth) ? (NIN - NOUT) : 0;
             const uint32_t crow = kSub * srb + static_cast<uint32_t>(lane);
             const uint32_t cc = static_cast<uint32_t>(lane >> 2);   // column within a unit
-            const uint32_t stg_off = (2u * q) ^ (((cc >> 2) & 1u) * 16u);
+            // stmatrix row address of this lane (lanes 0-15): matrix t/8 = which
+            // 16-byte half of column (t%8)'s 32 staged bytes, halves swapped for
+            // columns with bit 2 set (conflict-free for both the stores and the
+            // reads below)
+            const uint32_t t16 = static_cast<uint32_t>(lane) & 15u;
+            const uint32_t stg_row = smem_u32(stg) + (t16 & 7u) * 32u + (((t16 >> 3) ^ ((t16 >> 2) & 1u)) * 16u);
+            const int64_t left64 = a.N - (c0 + cc);
+            const int cols_left = left64 > 32 ? 32 : static_cast<int>(left64 < 0 ? 0 : left64);
+            const bool row_ok = r0 < a.M;
+            uint8_t *sp[2];
+#pragma unroll
+            for (int o = 0; o < NOUT; ++o) sp[o] = a.s_col[o] + (r0 >> 5) * a.ld_scol + (c0 + cc);
 #pragma unroll kUnroll
             for (int k = 0; k < 4; ++k) {
                 const uint32_t off = swz(crow, chunk0 + k);
                 uint32_t out[2][4];
                 uint32_t amax[2];
-                const int64_t gcol = c0 + 8 * k + cc;
-                const bool live = (r0 < a.M) && (gcol < a.N);
+                const bool live = row_ok && (8 * k < cols_left);
                 if constexpr (kEval) {
                     uint32_t in[3][4];
                     uint64_t hv[2][4];
@@ -377,15 +401,12 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, 1)
                 for (int o = 0; o < NOUT; ++o) {
                     uint32_t w0, w1;
                     const uint32_t sc = encode_block8(out[o], amax[o], w0, w1);
-                    // column 8k + cc of the sub-tile: rows 8m + 2q, 8m + 2q + 1 at
-                    // bytes 8m + 2q of its 32-byte column (16-byte halves swapped
-                    // for columns with bit 2 set: conflict-free reads below)
-                    uint8_t *base = stg + o * 1024 + (8u * k + cc) * 32;
-                    *reinterpret_cast<uint16_t *>(base + (stg_off ^ 0u)) = static_cast<uint16_t>(w0);
-                    *reinterpret_cast<uint16_t *>(base + (stg_off ^ 8u)) = static_cast<uint16_t>(w0 >> 16);
-                    *reinterpret_cast<uint16_t *>(base + (stg_off ^ 16u)) = static_cast<uint16_t>(w1);
-                    *reinterpret_cast<uint16_t *>(base + (stg_off ^ 24u)) = static_cast<uint16_t>(w1 >> 16);
-                    if (live && q == 0) a.s_col[o][(r0 >> 5) * a.ld_scol + gcol] = static_cast<uint8_t>(sc);
+                    // w0 = codes of rows 2q, 2q+1, 8+2q, 9+2q of column 8k + cc,
+                    // w1 the same 16 rows further; they land at bytes 4q..4q+3
+                    // of the column's two 16-byte halves (row order restored
+                    // when the column is read back)
+                    stsm_x2(stg_row + static_cast<uint32_t>(o * 1024 + k * 256), w0, w1);
+                    if (live && q == 0) sp[o][8 * k] = static_cast<uint8_t>(sc);
                 }
             }
             __syncwarp();
@@ -403,10 +424,15 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, 1)
                     const uint32_t sw = ((static_cast<uint32_t>(lane) >> 2) & 1u) * 16u;
                     const uint4 lo = *reinterpret_cast<const uint4 *>(src + (0u ^ sw));
                     const uint4 hi = *reinterpret_cast<const uint4 *>(src + (16u ^ sw));
+                    // staged words hold rows (j, j+1, j+8, j+9), j = 0, 2, 4, 6
+                    const uint4 r_lo = make_uint4(__byte_perm(lo.x, lo.y, 0x5410), __byte_perm(lo.z, lo.w, 0x5410),
+                                                  __byte_perm(lo.x, lo.y, 0x7632), __byte_perm(lo.z, lo.w, 0x7632));
+                    const uint4 r_hi = make_uint4(__byte_perm(hi.x, hi.y, 0x5410), __byte_perm(hi.z, hi.w, 0x5410),
+                                                  __byte_perm(hi.x, hi.y, 0x7632), __byte_perm(hi.z, hi.w, 0x7632));
                     uint4 *dst = reinterpret_cast<uint4 *>(a.q_col[o] + grp * a.group_stride +
                                                            gcol * a.ld_qcol + rin);
-                    __stcs(dst, lo);
-                    __stcs(dst + 1, hi);
+                    __stcs(dst, r_lo);
+                    __stcs(dst + 1, r_hi);
                 }
             }
             __syncwarp();
