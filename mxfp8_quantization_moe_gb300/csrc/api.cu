@@ -304,7 +304,8 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     if (st != MXFP8_OK) return st;
     if (!get_encoder()) return MXFP8_ERR_DEVICE;
     const int nin = s.op == mx::kQuant ? 1 : (s.op == mx::kFwd ? 2 : 3);
-    const int tm = mx::tile_rows(s.op, s.mode);
+    const mx::LaunchShape shape = mx::launch_shape(s.op, s.mode);
+    const int tm = shape.tile_rows;
     CUtensorMap maps[3];
     std::memset(maps, 0, sizeof(maps));
     for (int i = 0; i < 3; ++i) {
@@ -329,12 +330,21 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     a.ld_scol = s.ld_scol;
     a.group_rows = s.group_rows > 0 ? s.group_rows : s.M;
     a.group_stride = s.group_stride;
+    // whole 32-byte output blocks can go out as single 256-bit stores when
+    // every block start is 32-byte aligned
+    a.wide_row = (s.ld_qrow % 32) == 0;
+    a.wide_col = (s.ld_qcol % 32) == 0 && (s.group_stride % 32) == 0;
+    for (int o = 0; o < 2; ++o) {
+        if (s.q_row[o] && (reinterpret_cast<uintptr_t>(s.q_row[o]) & 31u) != 0) a.wide_row = 0;
+        if (s.q_col[o] && (reinterpret_cast<uintptr_t>(s.q_col[o]) & 31u) != 0) a.wide_col = 0;
+    }
     a.sig_table = d->table;
     a.sig2_table = d->table2;
     a.status = d->status;
     a.fallbacks = d->fallbacks;
     a.wait_limit = d->wait_limit;
-    const int grid = static_cast<int>(a.num_tiles < d->sms ? a.num_tiles : d->sms);
+    const int64_t slots = static_cast<int64_t>(d->sms) * shape.ctas_per_sm;
+    const int grid = static_cast<int>(a.num_tiles < slots ? a.num_tiles : slots);
     cudaError_t e;
     switch (s.op) {
     case mx::kQuant: e = mx::launch_quant(s.mode, maps, a, grid, stream, dev); break;

@@ -15,9 +15,11 @@ cudaError_t launch_tiles(const CUtensorMap (&maps)[3], const KernelArgs &a, int 
 {
     constexpr int kTM = Tuning<OP, MODE>::kTM;
     constexpr int kStages = Tuning<OP, MODE>::kStages;
+    constexpr int kCtas = Tuning<OP, MODE>::kCtas;
     constexpr size_t kSmem = smem_bytes<OP, kTM, kStages>();
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
-    auto kern = mxfp8_tile_kernel<OP, MODE, kTM, kStages>;
+    static_assert(kCtas * (kSmem + 1024) <= 228 * 1024, "shared memory per SM");
+    auto kern = mxfp8_tile_kernel<OP, MODE, kTM, kStages, kCtas>;
     static std::atomic<unsigned long long> attr_done{0};
     const unsigned long long bit = 1ull << (device & 63);
     if (!(attr_done.load(std::memory_order_acquire) & bit)) {
@@ -32,19 +34,24 @@ cudaError_t launch_tiles(const CUtensorMap (&maps)[3], const KernelArgs &a, int 
                             dim3((warps_of<kTM>() + 1) * 32), args, kSmem, stream);
 }
 
-// tile rows of the instantiation the host will launch
-inline int tile_rows(int op, int mode)
+// tile rows and resident CTAs per SM of the instantiation the host will launch
+struct LaunchShape {
+    int tile_rows, ctas_per_sm;
+};
+template <int OP, int MODE>
+constexpr LaunchShape shape_of() { return {Tuning<OP, MODE>::kTM, Tuning<OP, MODE>::kCtas}; }
+inline LaunchShape launch_shape(int op, int mode)
 {
     switch (op * 4 + mode) {
-    case kQuant * 4 + kRow: return Tuning<kQuant, kRow>::kTM;
-    case kQuant * 4 + kCol: return Tuning<kQuant, kCol>::kTM;
-    case kQuant * 4 + kBoth: return Tuning<kQuant, kBoth>::kTM;
-    case kFwd * 4 + kRow: return Tuning<kFwd, kRow>::kTM;
-    case kFwd * 4 + kCol: return Tuning<kFwd, kCol>::kTM;
-    case kFwd * 4 + kBoth: return Tuning<kFwd, kBoth>::kTM;
-    case kBwd * 4 + kRow: return Tuning<kBwd, kRow>::kTM;
-    case kBwd * 4 + kCol: return Tuning<kBwd, kCol>::kTM;
-    default: return Tuning<kBwd, kBoth>::kTM;
+    case kQuant * 4 + kRow: return shape_of<kQuant, kRow>();
+    case kQuant * 4 + kCol: return shape_of<kQuant, kCol>();
+    case kQuant * 4 + kBoth: return shape_of<kQuant, kBoth>();
+    case kFwd * 4 + kRow: return shape_of<kFwd, kRow>();
+    case kFwd * 4 + kCol: return shape_of<kFwd, kCol>();
+    case kFwd * 4 + kBoth: return shape_of<kFwd, kBoth>();
+    case kBwd * 4 + kRow: return shape_of<kBwd, kRow>();
+    case kBwd * 4 + kCol: return shape_of<kBwd, kCol>();
+    default: return shape_of<kBwd, kBoth>();
     }
 }
 

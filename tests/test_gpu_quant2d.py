@@ -116,3 +116,38 @@ def test_quant_2d_every_bf16_pattern(shuffle):
 def test_no_device_errors_after_quant():
     flags, _ = device_status()
     assert flags == 0
+
+
+@pytest.mark.parametrize("mode", [1, 2, 3])
+def test_quant_2d_outputs_at_16_byte_strides(mode):
+    """E4M3 outputs whose leading dimensions are 16 (not 32) modulo 32, so
+    that every other 32-code block starts off a 32-byte boundary."""
+    M, N = 160, 224
+    x = mixed_bf16(M, N, seed=21)
+    o = {}
+    if mode & 1:
+        o["q_row"] = Guarded((M, N + 16))
+        o["s_row"] = Guarded((M, N // 32))
+    if mode & 2:
+        o["q_col"] = Guarded((N, M + 16))
+        o["s_col"] = Guarded((M // 32, N))
+    p = lambda k: o[k].t.data_ptr() if k in o else None
+    ld = lambda k: o[k].t.stride(0) if k in o else 0
+    st = capi.mxfp8_quant_2d(x.data_ptr(), x.stride(0), M, N, mode,
+                             p("q_row"), ld("q_row"), p("s_row"), ld("s_row"),
+                             p("q_col"), ld("q_col"), p("s_col"), ld("s_col"),
+                             torch.cuda.current_stream().cuda_stream)
+    assert st == 0, capi.STATUS_NAMES[st]
+    torch.cuda.synchronize()
+    want = O.quant_2d(bits(x), mode)
+    for k, g in o.items():
+        assert g.intact(), k
+        got = u8(g.t)
+        if k == "q_row":
+            assert np.array_equal(got[:, :N], want[k])
+            assert bool((got[:, N:] == 0xA5).all())
+        elif k == "q_col":
+            assert np.array_equal(got[:, :M], want[k])
+            assert bool((got[:, M:] == 0xA5).all())
+        else:
+            assert np.array_equal(got, want[k]), k
