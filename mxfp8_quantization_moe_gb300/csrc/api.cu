@@ -334,7 +334,9 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     // every block start is 32-byte aligned
     a.wide_row = (s.ld_qrow % 32) == 0;
     a.wide_col = (s.ld_qcol % 32) == 0 && (s.group_stride % 32) == 0;
+    a.wide_srow = (s.ld_srow % 4) == 0;
     for (int o = 0; o < 2; ++o) {
+        if (s.s_row[o] && (reinterpret_cast<uintptr_t>(s.s_row[o]) & 3u) != 0) a.wide_srow = 0;
         if (s.q_row[o] && (reinterpret_cast<uintptr_t>(s.q_row[o]) & 31u) != 0) a.wide_row = 0;
         if (s.q_col[o] && (reinterpret_cast<uintptr_t>(s.q_col[o]) & 31u) != 0) a.wide_col = 0;
     }

@@ -78,11 +78,17 @@ __host__ __device__ constexpr int warps_of() { return (TM / kSub) * (kTileN / kS
 template <int TM>
 __host__ __device__ constexpr int tile_bytes() { return TM * kTileN * 2; }
 
-// shared memory: 1 KB alignment slack, the stages, the mbarriers
+// row-scale bytes of one tile and output: 4 per row (one per 32-column block)
+template <int TM>
+__host__ __device__ constexpr int scale_tile_bytes() { return TM * 4; }
+
+// shared memory: 1 KB alignment slack, the stages, the row-scale buffers
+// (a ring of 2 * STAGES tiles, per output), the mbarriers
 template <int OP, int TM, int STAGES>
 constexpr size_t smem_bytes()
 {
-    return 1024 + static_cast<size_t>(STAGES) * OpTraits<OP>::kIn * tile_bytes<TM>() + 2 * STAGES * 8;
+    return 1024 + static_cast<size_t>(STAGES) * OpTraits<OP>::kIn * tile_bytes<TM>() +
+           static_cast<size_t>(2 * STAGES) * OpTraits<OP>::kOut * scale_tile_bytes<TM>() + 2 * STAGES * 8;
 }
 
 // ------------------------------------------------------------ block values
@@ -284,18 +290,17 @@ __device__ __forceinline__ void transpose_subtile(uint32_t slot, const uint32_t 
     __syncwarp();
 }
 
-// encode and store the lane's block(s): 32 codes at `q` (16-byte aligned;
-// one 256-bit store -- a whole sector -- when `wide` says 32-byte aligned),
-// the scale byte at `sc`
+// encode the lane's block(s) and store the 32 codes at `q` (16-byte aligned;
+// one 256-bit store -- a whole sector -- when `wide` says 32-byte aligned);
+// returns the scale bytes in b[o]
 template <int NOUT>
-__device__ __forceinline__ void store_blocks(const uint32_t (&out)[2][16], const uint32_t (&amax)[2],
-                                             uint8_t *const (&q)[2], uint8_t *const (&sc)[2], bool live,
-                                             bool wide)
+__device__ __forceinline__ void store_codes(const uint32_t (&out)[2][16], const uint32_t (&amax)[2],
+                                            uint8_t *const (&q)[2], bool live, bool wide, uint32_t (&b)[2])
 {
 #pragma unroll
     for (int o = 0; o < NOUT; ++o) {
         uint32_t c[8];
-        const uint32_t b = encode_block32(out[o], amax[o], c);
+        b[o] = encode_block32(out[o], amax[o], c);
         if (live) {
             if (wide) {
                 st_global_v8(q[o], c);
@@ -303,7 +308,35 @@ __device__ __forceinline__ void store_blocks(const uint32_t (&out)[2][16], const
                 __stcs(reinterpret_cast<uint4 *>(q[o]), make_uint4(c[0], c[1], c[2], c[3]));
                 __stcs(reinterpret_cast<uint4 *>(q[o]) + 1, make_uint4(c[4], c[5], c[6], c[7]));
             }
-            *sc[o] = static_cast<uint8_t>(b);
+        }
+    }
+}
+
+// Row scales of one finished tile, from its shared-memory buffer (4 bytes a
+// row: blocks 4tc..4tc+3) to s_row, by the whole producer warp: one 32-bit
+// store per row where rows are 4-byte aligned and all four blocks exist,
+// single bytes otherwise.
+template <int NOUT, int TM>
+__device__ __forceinline__ void flush_row_scales(const KernelArgs &a, const uint8_t *sbuf, int64_t tr, int64_t tc,
+                                                 int lane)
+{
+    const int64_t row0 = tr * TM;
+    const int64_t blk0 = tc * 4;
+    const int64_t nblk = a.N >> 5;
+    const bool whole = a.wide_srow != 0 && blk0 + 4 <= nblk;
+    for (int i = lane; i < TM; i += 32) {
+        const int64_t row = row0 + i;
+        if (row >= a.M) break;
+#pragma unroll
+        for (int o = 0; o < NOUT; ++o) {
+            const uint32_t v = *reinterpret_cast<const uint32_t *>(sbuf + o * scale_tile_bytes<TM>() + 4 * i);
+            uint8_t *dst = a.s_row[o] + row * a.ld_srow + blk0;
+            if (whole) {
+                *reinterpret_cast<uint32_t *>(dst) = v;
+            } else {
+                for (int j = 0; j < 4; ++j)
+                    if (blk0 + j < nblk) dst[j] = static_cast<uint8_t>(v >> (8 * j));
+            }
         }
     }
 }
@@ -355,7 +388,10 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * NIN * kTileBytes);
+    // row-scale buffers [slot][output]: tile j uses slot j % (2 STAGES), so the
+    // producer can write a finished tile's scales out after refilling its stage
+    uint8_t *sbuf0 = smem + STAGES * NIN * kTileBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sbuf0 + 2 * STAGES * NOUT * scale_tile_bytes<TM>());
     const uint32_t smem_base = smem_u32(smem);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = smem_u32(bars + STAGES);
@@ -377,20 +413,30 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
     const int64_t tiles_n = a.tiles_n;
 
     // ------------------------------------------------------- producer warp
+    // Lane 0 streams the tiles in; once a stage has been refilled, the whole
+    // warp writes the row scales of the tile that occupied it out of their
+    // buffer (and those of the last tiles at the end).
     if (warp == kWarps) {
         if (lane == 0) {
             prefetch_tensormap(&tm0);
             if (NIN > 1) prefetch_tensormap(&tm1);
             if (NIN > 2) prefetch_tensormap(&tm2);
-            int it = 0;
-            bool failed = false;
-            for (TileWalk<STAGES> w(tiles_n); w.t < num_tiles; w.next(), ++it) {
-                const int s = w.s;
-                if (it >= STAGES && !mbar_wait_bounded(empty0 + 8 * s, w.ph ^ 1u, a.wait_limit)) {
-                    atomicOr(a.status, kStatusProducerWait);
+        }
+        int it = 0;
+        bool failed = false;
+        TileWalk<STAGES> done(tiles_n);   // the oldest tile whose row scales are still buffered
+        for (TileWalk<STAGES> w(tiles_n); w.t < num_tiles; w.next(), ++it) {
+            const int s = w.s;
+            if (it >= STAGES) {
+                bool ok = lane == 0 ? mbar_wait_bounded(empty0 + 8 * s, w.ph ^ 1u, a.wait_limit) : true;
+                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                if (!ok) {
+                    if (lane == 0) atomicOr(a.status, kStatusProducerWait);
                     failed = true;
                     break;
                 }
+            }
+            if (lane == 0) {
                 const int32_t r0 = static_cast<int32_t>(w.tr * kTileM);
                 const int32_t c0 = static_cast<int32_t>(w.tc * kTileN);
                 const uint32_t bar = full0 + 8 * s;
@@ -407,14 +453,39 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
                     tma_load_2d(dst + 2 * kTileBytes + kBoxBytes, &tm2, c0 + kBoxN, r0, bar);
                 }
             }
-            if (failed) {
-                // wait (bounded) for every load still in flight before leaving
-                for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j) {
-                    const uint32_t ph = static_cast<uint32_t>(j / STAGES) & 1u;
-                    if (!mbar_wait_bounded(full0 + 8 * (j % STAGES), ph, a.wait_limit))
-                        atomicOr(a.status, kStatusDrainWait);
-                }
+            if (it >= STAGES) {
+                // tile it - STAGES is finished (its stage was free); its slot is
+                // written again only by tile it + STAGES, loaded after this
+                if constexpr (MODE & kRow)
+                    flush_row_scales<NOUT, TM>(
+                        a, sbuf0 + ((it - STAGES) % (2 * STAGES)) * NOUT * scale_tile_bytes<TM>(), done.tr, done.tc,
+                        lane);
+                done.next();
             }
+            __syncwarp();
+        }
+        // the last tiles: wait (bounded) until the consumers have finished
+        // each, then write its row scales; after a failure, only wait for the
+        // loads still in flight
+        for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j) {
+            const int s = j % STAGES;
+            const uint32_t ph = static_cast<uint32_t>(j / STAGES) & 1u;
+            bool ok;
+            if (failed) {
+                ok = lane == 0 ? mbar_wait_bounded(full0 + 8 * s, ph, a.wait_limit) : true;
+                if (!ok && lane == 0) atomicOr(a.status, kStatusDrainWait);
+                continue;
+            }
+            ok = lane == 0 ? mbar_wait_bounded(empty0 + 8 * s, ph, a.wait_limit) : true;
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) {
+                if (lane == 0) atomicOr(a.status, kStatusProducerWait);
+                break;
+            }
+            if constexpr (MODE & kRow)
+                flush_row_scales<NOUT, TM>(a, sbuf0 + (j % (2 * STAGES)) * NOUT * scale_tile_bytes<TM>(), done.tr,
+                                           done.tc, lane);
+            done.next();
         }
         return;
     }
@@ -439,7 +510,8 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
 
     constexpr bool kSplit = (MODE == kBoth) && (OP != kQuant);  // values handed row -> col pass
     constexpr bool kWrites = kSplit || (MODE & kCol);           // generic writes into the stage
-    for (TileWalk<STAGES> w(tiles_n); w.t < num_tiles; w.next()) {
+    int slot = 0;   // row-scale buffer slot of this tile: tile ordinal % (2 STAGES)
+    for (TileWalk<STAGES> w(tiles_n); w.t < num_tiles; w.next(), slot = (slot + 1 == 2 * STAGES) ? 0 : slot + 1) {
         const int s = w.s;
         const bool fail = __any_sync(0xFFFFFFFFu, !mbar_wait_bounded(full0 + 8 * s, w.ph, a.wait_limit));
         if (fail) {
@@ -456,13 +528,15 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             const bool live = grow < a.M && c0 < a.N;
             uint32_t out[2][16], amax[2];
             block_values<OP, kSplit>(a, stage_ptr, kTileBytes, roff, out, amax);
-            uint8_t *q[2], *sc[2];
+            uint8_t *q[2];
 #pragma unroll
-            for (int o = 0; o < NOUT; ++o) {
-                q[o] = a.q_row[o] + grow * a.ld_qrow + c0;
-                sc[o] = a.s_row[o] + grow * a.ld_srow + (c0 >> 5);
-            }
-            store_blocks<NOUT>(out, amax, q, sc, live, a.wide_row != 0);
+            for (int o = 0; o < NOUT; ++o) q[o] = a.q_row[o] + grow * a.ld_qrow + c0;
+            uint32_t b[2];
+            store_codes<NOUT>(out, amax, q, live, a.wide_row != 0, b);
+            // scale bytes to the tile's buffer: row (32 srb + lane), block scb
+            uint8_t *sb = sbuf0 + slot * NOUT * scale_tile_bytes<TM>() + 4 * myrow + scb;
+#pragma unroll
+            for (int o = 0; o < NOUT; ++o) sb[o * scale_tile_bytes<TM>()] = static_cast<uint8_t>(b[o]);
             if constexpr (kSplit) {
                 // the values the col pass encodes, over inputs no longer needed
 #pragma unroll
@@ -496,13 +570,16 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
                 grp = r0 / a.group_rows;
                 rin = r0 - grp * a.group_rows;
             }
-            uint8_t *q[2], *sc[2];
+            uint8_t *q[2];
 #pragma unroll
-            for (int o = 0; o < NOUT; ++o) {
-                q[o] = a.q_col[o] + grp * a.group_stride + gcol * a.ld_qcol + rin;
-                sc[o] = a.s_col[o] + (r0 >> 5) * a.ld_scol + gcol;
+            for (int o = 0; o < NOUT; ++o) q[o] = a.q_col[o] + grp * a.group_stride + gcol * a.ld_qcol + rin;
+            uint32_t b[2];
+            store_codes<NOUT>(out, amax, q, live, a.wide_col != 0, b);
+            if (live) {
+#pragma unroll
+                for (int o = 0; o < NOUT; ++o)
+                    a.s_col[o][(r0 >> 5) * a.ld_scol + gcol] = static_cast<uint8_t>(b[o]);
             }
-            store_blocks<NOUT>(out, amax, q, sc, live, a.wide_col != 0);
         }
 
         if constexpr (kWrites) fence_proxy_async_smem();
