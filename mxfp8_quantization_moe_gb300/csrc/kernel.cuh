@@ -107,46 +107,22 @@ __device__ __forceinline__ void set_half16(uint32_t &w, int hi, uint32_t b)
     w = hi ? ((w & 0xFFFFu) | (b << 16)) : ((w & 0xFFFF0000u) | b);
 }
 
-// A candidate element of a block whose fast amax has mantissa 0x60 or 0x61:
-// its fast fp32 value(s) are evaluated again (the same instruction sequence
-// as the packed path, the element in both halves) and compared with the
-// rounding-midpoint windows; if near, the exact values replace `cur`
-// (packed: output 0 in the low half, output 1 in the high half).  Returns
-// (bits, 1 if recomputed).
-template <int OP>
-static __device__ __noinline__ uint2 settle_candidate(const float2 *table, float x0, float x1, float x2,
-                                                      uint32_t cur)
-{
-    const uint32_t w0 = pack_bf16x2(x0, x0), w1 = pack_bf16x2(x1, x1);
-    if constexpr (OP == kFwd) {
-        if (!near_mid2(swiglu_h2(w0, w1), kNearH)) return make_uint2(cur, 0u);
-        return make_uint2(bf16_bits(swiglu_h_exact(table, x0, x1)), 1u);
-    } else {
-        uint64_t DG, DU;
-        swiglu_grads2(w0, w1, pack_bf16x2(x2, x2), DG, DU);
-        if (!(near_mid2(DG, kNearDgate) | near_mid2(DU, kNearDup))) return make_uint2(cur, 0u);
-        const float2 r = swiglu_grads_exact(table, x0, x1, x2);
-        return make_uint2(bf16_bits(r.x) | (bf16_bits(r.y) << 16), 1u);
-    }
-}
-
 // Element values of the lane's block.  For the cast, the input itself; for
 // SwiGLU, the fast element op on the NIN input slots, then the exact
 // recomputation of every element that needs it: all 32 if a gate is outside
-// the fast range or a block amax is huge or not finite; otherwise, with
-// kEager, every pair near a 0x60/0x61 rounding midpoint (the values feed
-// blocks of both directions), else only in blocks whose fast amax has
-// mantissa 0x60 or 0x61, their elements at that mantissa pair of the amax
-// exponent that turn out near a midpoint.  Returns the outputs' amax
-// patterns.
-template <int OP, bool kEager>
+// the fast range or a block amax is huge or not finite, otherwise every pair
+// holding a value near a 0x60/0x61 rounding midpoint.  (Testing every value,
+// rather than only the blocks whose amax sits at that mantissa pair, also
+// covers the other direction's blocks in "both" mode, and measured cheaper
+// than scanning the risky blocks.)  Returns the outputs' amax patterns.
+template <int OP>
 __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t *stage, int tile_bytes_,
                                              const uint32_t (&roff)[4], uint32_t (&out)[2][16],
                                              uint32_t (&amax)[2])
 {
     constexpr int NOUT = OpTraits<OP>::kOut;
     constexpr int NIN = OpTraits<OP>::kIn;
-    uint32_t near = 0;     // bit j: pair j (elements 2j, 2j+1), eager test
+    uint32_t near = 0;     // bit j: pair j (elements 2j, 2j+1)
     bool gates_ok = true;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -168,7 +144,7 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
             for (int p = 0; p < 4; ++p) {
                 const uint64_t H = swiglu_h2(in[0][p], in[1][p]);
                 out[0][4 * c + p] = pack_bf16x2(f2lo(H), f2hi(H));
-                if constexpr (kEager) near |= static_cast<uint32_t>(near_mid2(H, kNearH)) << (4 * c + p);
+                near |= static_cast<uint32_t>(near_mid2(H, kNearH)) << (4 * c + p);
             }
         } else {
             gates_ok &= gates_fast8(in[1]);
@@ -178,8 +154,7 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
                 swiglu_grads2(in[0][p], in[1][p], in[2][p], DG, DU);
                 out[0][4 * c + p] = pack_bf16x2(f2lo(DG), f2hi(DG));
                 out[1][4 * c + p] = pack_bf16x2(f2lo(DU), f2hi(DU));
-                if constexpr (kEager)
-                    near |= static_cast<uint32_t>(near_mid2(DG, kNearDgate) | near_mid2(DU, kNearDup)) << (4 * c + p);
+                near |= static_cast<uint32_t>(near_mid2(DG, kNearDgate) | near_mid2(DU, kNearDup)) << (4 * c + p);
             }
         }
     }
@@ -187,67 +162,30 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
     for (int o = 0; o < NOUT; ++o) amax[o] = amax32_lane(out[o]);
     if constexpr (OP != kQuant) {
         bool full = !gates_ok;
-        bool risky = false;
 #pragma unroll
-        for (int o = 0; o < NOUT; ++o) {
-            full |= amax[o] >= kHugeAmax;
-            if constexpr (!kEager) risky |= scale_at_risk(amax[o]);
-        }
+        for (int o = 0; o < NOUT; ++o) full |= amax[o] >= kHugeAmax;
         if (full) near = 0xFFFFu;
-        if (__any_sync(0xFFFFFFFFu, (near != 0u) || risky)) {
-            uint32_t n = 0;
-            if (near != 0u) {
+        if (__any_sync(0xFFFFFFFFu, near != 0u)) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    if ((near >> j) & 1u) {
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int e = 2 * j + h;
-                            const float x0 = elem_in(stage, roff, e);
-                            const float x1 = elem_in(stage + tile_bytes_, roff, e);
-                            if constexpr (OP == kFwd) {
-                                set_half16(out[0][j], h, bf16_bits(swiglu_h_exact(a.sig2_table, x0, x1)));
-                            } else {
-                                const float x2 = elem_in(stage + 2 * tile_bytes_, roff, e);
-                                const float2 r = swiglu_grads_exact(a.sig2_table, x0, x1, x2);
-                                set_half16(out[0][j], h, bf16_bits(r.x));
-                                set_half16(out[1][j], h, bf16_bits(r.y));
-                            }
-                        }
-                        n += 2;
-                    }
-                }
-            } else if (risky) {
-                // candidates: magnitude at mantissa 0x60 or 0x61 of a risky
-                // block's amax exponent
-                uint32_t t[2];
-#pragma unroll
-                for (int o = 0; o < NOUT; ++o)
-                    t[o] = scale_at_risk(amax[o]) ? (((amax[o] & 0x7F80u) | 0x60u) * 0x10001u) : 0xFFFFFFFFu;
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < 16; ++j) {
+                if ((near >> j) & 1u) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        bool cand = false;
-#pragma unroll
-                        for (int o = 0; o < NOUT; ++o)
-                            cand |= ((((out[o][j] ^ t[o]) & 0x7FFE7FFEu) >> (16 * h)) & 0xFFFFu) == 0u;
-                        if (cand) {
-                            const int e = 2 * j + h;
-                            const float x0 = elem_in(stage, roff, e);
-                            const float x1 = elem_in(stage + tile_bytes_, roff, e);
-                            const float x2 = NIN > 2 ? elem_in(stage + 2 * tile_bytes_, roff, e) : 0.0f;
-                            uint32_t cur = (out[0][j] >> (16 * h)) & 0xFFFFu;
-                            if (NOUT > 1) cur |= ((out[NOUT - 1][j] >> (16 * h)) & 0xFFFFu) << 16;
-                            const uint2 r = settle_candidate<OP>(a.sig2_table, x0, x1, x2, cur);
-                            n += r.y;
-                            set_half16(out[0][j], h, r.x & 0xFFFFu);
-                            if (NOUT > 1) set_half16(out[NOUT - 1][j], h, r.x >> 16);
+                        const int e = 2 * j + h;
+                        const float x0 = elem_in(stage, roff, e);
+                        const float x1 = elem_in(stage + tile_bytes_, roff, e);
+                        if constexpr (OP == kFwd) {
+                            set_half16(out[0][j], h, bf16_bits(swiglu_h_exact(a.sig2_table, x0, x1)));
+                        } else {
+                            const float x2 = elem_in(stage + 2 * tile_bytes_, roff, e);
+                            const float2 r = swiglu_grads_exact(a.sig2_table, x0, x1, x2);
+                            set_half16(out[0][j], h, bf16_bits(r.x));
+                            set_half16(out[1][j], h, bf16_bits(r.y));
                         }
                     }
                 }
             }
-            count_fallbacks_warp(a.fallbacks, n);
+            count_fallbacks_warp(a.fallbacks, 2u * __popc(near));
 #pragma unroll
             for (int o = 0; o < NOUT; ++o) amax[o] = amax32_lane(out[o]);
         }
@@ -527,7 +465,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             const int64_t grow = r0 + lane;
             const bool live = grow < a.M && c0 < a.N;
             uint32_t out[2][16], amax[2];
-            block_values<OP, kSplit>(a, stage_ptr, kTileBytes, roff, out, amax);
+            block_values<OP>(a, stage_ptr, kTileBytes, roff, out, amax);
             uint8_t *q[2];
 #pragma unroll
             for (int o = 0; o < NOUT; ++o) q[o] = a.q_row[o] + grow * a.ld_qrow + c0;
@@ -564,7 +502,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             if constexpr (kSplit || OP == kQuant)
                 block_settled<NOUT>(stage_ptr + kFirst * kTileBytes, kTileBytes, roff, out, amax);
             else
-                block_values<OP, false>(a, stage_ptr, kTileBytes, roff, out, amax);
+                block_values<OP>(a, stage_ptr, kTileBytes, roff, out, amax);
             int64_t grp = 0, rin = r0;
             if (a.group_stride != 0) {  // 3D: per-expert column-major output
                 grp = r0 / a.group_rows;
