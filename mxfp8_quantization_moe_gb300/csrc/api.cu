@@ -334,9 +334,13 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     // every block start is 32-byte aligned
     a.wide_row = (s.ld_qrow % 32) == 0;
     a.wide_col = (s.ld_qcol % 32) == 0 && (s.group_stride % 32) == 0;
-    a.wide_srow = (s.ld_srow % 4) == 0;
+    // a group of column tiles leaves its row scales as one 4*group-byte store
+    // per row when rows are aligned to that
+    const int64_t sgrp = 4 * static_cast<int64_t>(shape.group);
+    a.wide_srow = (s.ld_srow % sgrp) == 0;
     for (int o = 0; o < 2; ++o) {
-        if (s.s_row[o] && (reinterpret_cast<uintptr_t>(s.s_row[o]) & 3u) != 0) a.wide_srow = 0;
+        if (s.s_row[o] && (reinterpret_cast<uintptr_t>(s.s_row[o]) % static_cast<uintptr_t>(sgrp)) != 0)
+            a.wide_srow = 0;
         if (s.q_row[o] && (reinterpret_cast<uintptr_t>(s.q_row[o]) & 31u) != 0) a.wide_row = 0;
         if (s.q_col[o] && (reinterpret_cast<uintptr_t>(s.q_col[o]) & 31u) != 0) a.wide_col = 0;
     }
@@ -345,8 +349,10 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     a.status = d->status;
     a.fallbacks = d->fallbacks;
     a.wait_limit = d->wait_limit;
+    // CTAs walk groups of `group` consecutive column tiles
+    const int64_t supers = ((s.M + tm - 1) / tm) * ((a.tiles_n + shape.group - 1) / shape.group);
     const int64_t slots = static_cast<int64_t>(d->sms) * shape.ctas_per_sm;
-    const int grid = static_cast<int>(a.num_tiles < slots ? a.num_tiles : slots);
+    const int grid = static_cast<int>(supers < slots ? supers : slots);
     cudaError_t e;
     switch (s.op) {
     case mx::kQuant: e = mx::launch_quant(s.mode, maps, a, grid, stream, dev); break;

@@ -48,28 +48,30 @@ struct OpTraits<kBwd> {
     static constexpr int kIn = 3, kOut = 2;
 };
 
-// Tile height, pipeline depth and resident CTAs per SM for each
-// instantiation: more warps hide more latency where registers and shared
+// Tile height, pipeline depth, resident CTAs per SM and row-scale group
+// (consecutive column tiles a CTA takes in a row, so that their row scales
+// leave as one 4*GROUP-byte store per row; it pays in the "both" modes, the
+// plain tile-cyclic order is faster elsewhere) for each instantiation: more warps hide more latency where registers and shared
 // memory allow it (the cast alone needs few registers).  Registers are
 // granted per four warps, so the producer warp costs three warps' worth: 17
 // warps get at most 96 registers a thread, 13 warps 128.
 template <int OP, int MODE>
 struct Tuning;
-#define MX_TUNE(OP, MODE, TM, STAGES, CTAS)                                          \
+#define MX_TUNE(OP, MODE, TM, STAGES, CTAS, GROUP)                                   \
     template <>                                                                      \
     struct Tuning<OP, MODE> {                                                        \
-        static constexpr int kTM = TM, kStages = STAGES, kCtas = CTAS;               \
+        static constexpr int kTM = TM, kStages = STAGES, kCtas = CTAS, kGroup = GROUP; \
         static_assert((TM / 32) * 4 + 1 <= 32, "at most 1024 threads per CTA");     \
     };
-MX_TUNE(kQuant, kRow, 224, 3, 1)
-MX_TUNE(kQuant, kCol, 224, 3, 1)
-MX_TUNE(kQuant, kBoth, 224, 3, 1)
-MX_TUNE(kFwd, kRow, 128, 3, 1)
-MX_TUNE(kFwd, kCol, 128, 3, 1)
-MX_TUNE(kFwd, kBoth, 128, 3, 1)
-MX_TUNE(kBwd, kRow, 96, 3, 1)
-MX_TUNE(kBwd, kCol, 96, 3, 1)
-MX_TUNE(kBwd, kBoth, 96, 3, 1)
+MX_TUNE(kQuant, kRow, 224, 3, 1, 1)
+MX_TUNE(kQuant, kCol, 224, 3, 1, 1)
+MX_TUNE(kQuant, kBoth, 224, 3, 1, 4)
+MX_TUNE(kFwd, kRow, 128, 3, 1, 1)
+MX_TUNE(kFwd, kCol, 128, 3, 1, 1)
+MX_TUNE(kFwd, kBoth, 128, 3, 1, 4)
+MX_TUNE(kBwd, kRow, 96, 3, 1, 1)
+MX_TUNE(kBwd, kCol, 96, 3, 1, 1)
+MX_TUNE(kBwd, kBoth, 96, 3, 1, 2)
 #undef MX_TUNE
 
 template <int TM>
@@ -78,17 +80,18 @@ __host__ __device__ constexpr int warps_of() { return (TM / kSub) * (kTileN / kS
 template <int TM>
 __host__ __device__ constexpr int tile_bytes() { return TM * kTileN * 2; }
 
-// row-scale bytes of one tile and output: 4 per row (one per 32-column block)
-template <int TM>
-__host__ __device__ constexpr int scale_tile_bytes() { return TM * 4; }
+// row-scale bytes of one group of G column tiles and one output: 4 G per row
+// (one per 32-column block)
+template <int TM, int G>
+__host__ __device__ constexpr int scale_group_bytes() { return TM * 4 * G; }
 
 // shared memory: 1 KB alignment slack, the stages, the row-scale buffers
-// (a ring of 2 * STAGES tiles, per output), the mbarriers
-template <int OP, int TM, int STAGES>
+// (a ring of STAGES + 1 groups, per output), the mbarriers
+template <int OP, int TM, int STAGES, int G>
 constexpr size_t smem_bytes()
 {
     return 1024 + static_cast<size_t>(STAGES) * OpTraits<OP>::kIn * tile_bytes<TM>() +
-           static_cast<size_t>(2 * STAGES) * OpTraits<OP>::kOut * scale_tile_bytes<TM>() + 2 * STAGES * 8;
+           static_cast<size_t>(STAGES + 1) * OpTraits<OP>::kOut * scale_group_bytes<TM, G>() + 2 * STAGES * 8;
 }
 
 // ------------------------------------------------------------ block values
@@ -250,58 +253,76 @@ __device__ __forceinline__ void store_codes(const uint32_t (&out)[2][16], const 
     }
 }
 
-// Row scales of one finished tile, from its shared-memory buffer (4 bytes a
-// row: blocks 4tc..4tc+3) to s_row, by the whole producer warp: one 32-bit
-// store per row where rows are 4-byte aligned and all four blocks exist,
-// single bytes otherwise.
-template <int NOUT, int TM>
-__device__ __forceinline__ void flush_row_scales(const KernelArgs &a, const uint8_t *sbuf, int64_t tr, int64_t tc,
-                                                 int lane)
+// Row scales of one finished group of column tiles (tiles 0..gsize-1 of group
+// ug in row band tr), from its shared-memory buffer (4 G bytes a row) to s_row,
+// by the whole producer warp: one 4G-byte store per row where the group is
+// whole and rows are aligned (`wide`), 4-byte stores or single bytes
+// otherwise.
+template <int NOUT, int TM, int G>
+__device__ __forceinline__ void flush_row_scales(const KernelArgs &a, const uint8_t *gbuf, int64_t tr, int64_t ug,
+                                                 int gsize, int lane)
 {
     const int64_t row0 = tr * TM;
-    const int64_t blk0 = tc * 4;
+    const int64_t blk0 = ug * 4 * G;
     const int64_t nblk = a.N >> 5;
-    const bool whole = a.wide_srow != 0 && blk0 + 4 <= nblk;
+    const bool whole = a.wide_srow != 0 && gsize == G && blk0 + 4 * G <= nblk;
     for (int i = lane; i < TM; i += 32) {
         const int64_t row = row0 + i;
         if (row >= a.M) break;
 #pragma unroll
         for (int o = 0; o < NOUT; ++o) {
-            const uint32_t v = *reinterpret_cast<const uint32_t *>(sbuf + o * scale_tile_bytes<TM>() + 4 * i);
+            const uint8_t *src = gbuf + o * scale_group_bytes<TM, G>() + 4 * G * i;
             uint8_t *dst = a.s_row[o] + row * a.ld_srow + blk0;
             if (whole) {
-                *reinterpret_cast<uint32_t *>(dst) = v;
+                if constexpr (G == 4)
+                    *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
+                else if constexpr (G == 2)
+                    *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(src);
+                else
+                    *reinterpret_cast<uint32_t *>(dst) = *reinterpret_cast<const uint32_t *>(src);
             } else {
-                for (int j = 0; j < 4; ++j)
-                    if (blk0 + j < nblk) dst[j] = static_cast<uint8_t>(v >> (8 * j));
+                for (int j = 0; j < 4 * gsize; ++j)
+                    if (blk0 + j < nblk) dst[j] = src[j];
             }
         }
     }
 }
 
-// This CTA's tiles t = blockIdx.x, + gridDim.x, ... as (row tile, column
-// tile) and pipeline slot (stage, phase parity), advanced without divisions.
-template <int STAGES>
+// This CTA's tiles.  Column tiles are taken in groups of G consecutive ones
+// of a row band ("super-tiles" u = blockIdx.x, + gridDim.x, ...), tile by
+// tile; the walk keeps the row band tr, the group ug, the tile i within it,
+// the pipeline slot (stage, phase parity) and the group's row-scale buffer
+// slot (group ordinal % (STAGES + 1)), advanced without divisions.
+template <int STAGES, int G>
 struct TileWalk {
-    int64_t t, tr, tc, step_r, step_c, tiles_n;
-    int s;
+    int64_t u, tr, ug, step_r, step_c, tiles_g, tiles_n;
+    int i, gsize, s, gslot;
     uint32_t ph;
     __device__ __forceinline__ explicit TileWalk(int64_t n_tiles_n)
-        : t(blockIdx.x), tiles_n(n_tiles_n), s(0), ph(0)
+        : u(blockIdx.x), tiles_n(n_tiles_n), i(0), s(0), gslot(0), ph(0)
     {
-        tr = t / tiles_n;
-        tc = t - tr * tiles_n;
-        step_r = static_cast<int64_t>(gridDim.x) / tiles_n;
-        step_c = static_cast<int64_t>(gridDim.x) - step_r * tiles_n;
+        tiles_g = (tiles_n + G - 1) / G;
+        tr = u / tiles_g;
+        ug = u - tr * tiles_g;
+        step_r = static_cast<int64_t>(gridDim.x) / tiles_g;
+        step_c = static_cast<int64_t>(gridDim.x) - step_r * tiles_g;
+        gsize = static_cast<int>(min(static_cast<int64_t>(G), tiles_n - ug * G));
     }
+    __device__ __forceinline__ int64_t tc() const { return ug * G + i; }
+    __device__ __forceinline__ bool last_in_group() const { return i + 1 == gsize; }
     __device__ __forceinline__ void next()
     {
-        t += gridDim.x;
-        tr += step_r;
-        tc += step_c;
-        if (tc >= tiles_n) {
-            tc -= tiles_n;
-            ++tr;
+        if (++i == gsize) {
+            i = 0;
+            u += gridDim.x;
+            tr += step_r;
+            ug += step_c;
+            if (ug >= tiles_g) {
+                ug -= tiles_g;
+                ++tr;
+            }
+            gsize = static_cast<int>(min(static_cast<int64_t>(G), tiles_n - ug * G));
+            if (++gslot == STAGES + 1) gslot = 0;
         }
         if (++s == STAGES) {
             s = 0;
@@ -311,7 +332,7 @@ struct TileWalk {
 };
 
 // ------------------------------------------------------------------ kernel
-template <int OP, int MODE, int TM, int STAGES, int CTAS>
+template <int OP, int MODE, int TM, int STAGES, int CTAS, int G>
 __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
     mxfp8_tile_kernel(const __grid_constant__ CUtensorMap tm0,
                       const __grid_constant__ CUtensorMap tm1,
@@ -326,10 +347,11 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    // row-scale buffers [slot][output]: tile j uses slot j % (2 STAGES), so the
-    // producer can write a finished tile's scales out after refilling its stage
+    // row-scale buffers [slot][output]: a group of column tiles uses slot
+    // (group ordinal % (STAGES + 1)), so the producer can write a finished
+    // group's scales out after refilling the stage of its last tile
     uint8_t *sbuf0 = smem + STAGES * NIN * kTileBytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sbuf0 + 2 * STAGES * NOUT * scale_tile_bytes<TM>());
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sbuf0 + (STAGES + 1) * NOUT * scale_group_bytes<TM, G>());
     const uint32_t smem_base = smem_u32(smem);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = smem_u32(bars + STAGES);
@@ -347,8 +369,8 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
     }
     __syncthreads();
 
-    const int64_t num_tiles = a.num_tiles;
     const int64_t tiles_n = a.tiles_n;
+    const int64_t num_super = (a.num_tiles / tiles_n) * ((tiles_n + G - 1) / G);   // groups of column tiles
 
     // ------------------------------------------------------- producer warp
     // Lane 0 streams the tiles in; once a stage has been refilled, the whole
@@ -362,8 +384,8 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
         }
         int it = 0;
         bool failed = false;
-        TileWalk<STAGES> done(tiles_n);   // the oldest tile whose row scales are still buffered
-        for (TileWalk<STAGES> w(tiles_n); w.t < num_tiles; w.next(), ++it) {
+        TileWalk<STAGES, G> done(tiles_n);   // the oldest tile not yet recycled
+        for (TileWalk<STAGES, G> w(tiles_n); w.u < num_super; w.next(), ++it) {
             const int s = w.s;
             if (it >= STAGES) {
                 bool ok = lane == 0 ? mbar_wait_bounded(empty0 + 8 * s, w.ph ^ 1u, a.wait_limit) : true;
@@ -376,7 +398,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             }
             if (lane == 0) {
                 const int32_t r0 = static_cast<int32_t>(w.tr * kTileM);
-                const int32_t c0 = static_cast<int32_t>(w.tc * kTileN);
+                const int32_t c0 = static_cast<int32_t>(w.tc() * kTileN);
                 const uint32_t bar = full0 + 8 * s;
                 const uint32_t dst = smem_base + static_cast<uint32_t>(s * NIN) * kTileBytes;
                 mbar_expect_tx(bar, NIN * kTileBytes);
@@ -392,12 +414,14 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
                 }
             }
             if (it >= STAGES) {
-                // tile it - STAGES is finished (its stage was free); its slot is
-                // written again only by tile it + STAGES, loaded after this
-                if constexpr (MODE & kRow)
-                    flush_row_scales<NOUT, TM>(
-                        a, sbuf0 + ((it - STAGES) % (2 * STAGES)) * NOUT * scale_tile_bytes<TM>(), done.tr, done.tc,
-                        lane);
+                // tile it - STAGES is finished (its stage was free); if it ends
+                // its group, the group's slot is written again only by a
+                // group starting at tile it + 1 or later, loaded after this
+                if constexpr (MODE & kRow) {
+                    if (done.last_in_group())
+                        flush_row_scales<NOUT, TM, G>(a, sbuf0 + done.gslot * NOUT * scale_group_bytes<TM, G>(), done.tr,
+                                                      done.ug, done.gsize, lane);
+                }
                 done.next();
             }
             __syncwarp();
@@ -420,9 +444,11 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
                 if (lane == 0) atomicOr(a.status, kStatusProducerWait);
                 break;
             }
-            if constexpr (MODE & kRow)
-                flush_row_scales<NOUT, TM>(a, sbuf0 + (j % (2 * STAGES)) * NOUT * scale_tile_bytes<TM>(), done.tr,
-                                           done.tc, lane);
+            if constexpr (MODE & kRow) {
+                if (done.last_in_group() || j + 1 == it)
+                    flush_row_scales<NOUT, TM, G>(a, sbuf0 + done.gslot * NOUT * scale_group_bytes<TM, G>(), done.tr,
+                                                  done.ug, done.i + 1, lane);
+            }
             done.next();
         }
         return;
@@ -448,8 +474,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
 
     constexpr bool kSplit = (MODE == kBoth) && (OP != kQuant);  // values handed row -> col pass
     constexpr bool kWrites = kSplit || (MODE & kCol);           // generic writes into the stage
-    int slot = 0;   // row-scale buffer slot of this tile: tile ordinal % (2 STAGES)
-    for (TileWalk<STAGES> w(tiles_n); w.t < num_tiles; w.next(), slot = (slot + 1 == 2 * STAGES) ? 0 : slot + 1) {
+    for (TileWalk<STAGES, G> w(tiles_n); w.u < num_super; w.next()) {
         const int s = w.s;
         const bool fail = __any_sync(0xFFFFFFFFu, !mbar_wait_bounded(full0 + 8 * s, w.ph, a.wait_limit));
         if (fail) {
@@ -457,7 +482,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             return;
         }
         const int64_t r0 = w.tr * kTileM + kSub * srb;   // sub-tile origin
-        const int64_t c0 = w.tc * kTileN + kSub * scb;
+        const int64_t c0 = w.tc() * kTileN + kSub * scb;
         const uint32_t stage = smem_base + static_cast<uint32_t>(s * NIN) * kTileBytes;
         const uint8_t *stage_ptr = smem + static_cast<size_t>(s * NIN) * kTileBytes;
 
@@ -472,9 +497,9 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             uint32_t b[2];
             store_codes<NOUT>(out, amax, q, live, a.wide_row != 0, b);
             // scale bytes to the tile's buffer: row (32 srb + lane), block scb
-            uint8_t *sb = sbuf0 + slot * NOUT * scale_tile_bytes<TM>() + 4 * myrow + scb;
+            uint8_t *sb = sbuf0 + w.gslot * NOUT * scale_group_bytes<TM, G>() + 4 * G * myrow + 4 * w.i + scb;
 #pragma unroll
-            for (int o = 0; o < NOUT; ++o) sb[o * scale_tile_bytes<TM>()] = static_cast<uint8_t>(b[o]);
+            for (int o = 0; o < NOUT; ++o) sb[o * scale_group_bytes<TM, G>()] = static_cast<uint8_t>(b[o]);
             if constexpr (kSplit) {
                 // the values the col pass encodes, over inputs no longer needed
 #pragma unroll

@@ -16,10 +16,11 @@ cudaError_t launch_tiles(const CUtensorMap (&maps)[3], const KernelArgs &a, int 
     constexpr int kTM = Tuning<OP, MODE>::kTM;
     constexpr int kStages = Tuning<OP, MODE>::kStages;
     constexpr int kCtas = Tuning<OP, MODE>::kCtas;
-    constexpr size_t kSmem = smem_bytes<OP, kTM, kStages>();
+    constexpr int kGroup = Tuning<OP, MODE>::kGroup;
+    constexpr size_t kSmem = smem_bytes<OP, kTM, kStages, kGroup>();
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
     static_assert(kCtas * (kSmem + 1024) <= 228 * 1024, "shared memory per SM");
-    auto kern = mxfp8_tile_kernel<OP, MODE, kTM, kStages, kCtas>;
+    auto kern = mxfp8_tile_kernel<OP, MODE, kTM, kStages, kCtas, kGroup>;
     static std::atomic<unsigned long long> attr_done{0};
     const unsigned long long bit = 1ull << (device & 63);
     if (!(attr_done.load(std::memory_order_acquire) & bit)) {
@@ -34,12 +35,16 @@ cudaError_t launch_tiles(const CUtensorMap (&maps)[3], const KernelArgs &a, int 
                             dim3((warps_of<kTM>() + 1) * 32), args, kSmem, stream);
 }
 
-// tile rows and resident CTAs per SM of the instantiation the host will launch
+// tile rows, resident CTAs per SM and row-scale group of the instantiation
+// the host will launch
 struct LaunchShape {
-    int tile_rows, ctas_per_sm;
+    int tile_rows, ctas_per_sm, group;
 };
 template <int OP, int MODE>
-constexpr LaunchShape shape_of() { return {Tuning<OP, MODE>::kTM, Tuning<OP, MODE>::kCtas}; }
+constexpr LaunchShape shape_of()
+{
+    return {Tuning<OP, MODE>::kTM, Tuning<OP, MODE>::kCtas, Tuning<OP, MODE>::kGroup};
+}
 inline LaunchShape launch_shape(int op, int mode)
 {
     switch (op * 4 + mode) {
