@@ -71,7 +71,7 @@ MX_TUNE(kFwd, kCol, 128, 3, 1, 1)
 MX_TUNE(kFwd, kBoth, 128, 3, 1, 4)
 MX_TUNE(kBwd, kRow, 96, 3, 1, 1)
 MX_TUNE(kBwd, kCol, 96, 3, 1, 1)
-MX_TUNE(kBwd, kBoth, 96, 3, 1, 2)
+MX_TUNE(kBwd, kBoth, 128, 2, 1, 2)
 #undef MX_TUNE
 
 template <int TM>
@@ -195,9 +195,100 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
     }
 }
 
+// The same for the row pass of "both" mode, chunk by chunk: each chunk's
+// values are settled (exact recomputation of its pairs near a midpoint, or of
+// all 8 if a gate is outside the fast range or a value is huge or not
+// finite -- the per-element form of the block rules, which is all they need)
+// and written at once over the chunk's inputs in the value slots, so only
+// one chunk of outputs lives in registers.  Returns the outputs' amax.
+template <int OP>
+__device__ __forceinline__ void block_values_split(const KernelArgs &a, uint8_t *stage, int tile_bytes_,
+                                                   const uint32_t (&roff)[4], uint32_t (&amax)[2])
+{
+    constexpr int NOUT = OpTraits<OP>::kOut;
+    constexpr int NIN = OpTraits<OP>::kIn;
+    uint32_t acc[2] = {0u, 0u};   // running max of magnitudes (sign bits ignored)
+    uint32_t nfb = 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t in[3][4];
+#pragma unroll
+        for (int k = 0; k < NIN; ++k) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(stage + k * tile_bytes_ + roff[c]);
+            in[k][0] = v.x;
+            in[k][1] = v.y;
+            in[k][2] = v.z;
+            in[k][3] = v.w;
+        }
+        uint32_t o4[2][4];
+        uint32_t near = 0;   // bit p: pair p of the chunk
+        bool full;
+        if constexpr (OP == kFwd) {
+            full = !gates_fast8(in[0]);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const uint64_t H = swiglu_h2(in[0][p], in[1][p]);
+                o4[0][p] = pack_bf16x2(f2lo(H), f2hi(H));
+                near |= static_cast<uint32_t>(near_mid2(H, kNearH)) << p;
+            }
+        } else {
+            full = !gates_fast8(in[1]);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                uint64_t DG, DU;
+                swiglu_grads2(in[0][p], in[1][p], in[2][p], DG, DU);
+                o4[0][p] = pack_bf16x2(f2lo(DG), f2hi(DG));
+                o4[1][p] = pack_bf16x2(f2lo(DU), f2hi(DU));
+                near |= static_cast<uint32_t>(near_mid2(DG, kNearDgate) | near_mid2(DU, kNearDup)) << p;
+            }
+        }
+        uint32_t cm[2];
+#pragma unroll
+        for (int o = 0; o < NOUT; ++o) {
+            cm[o] = hmax_abs2(hmax_abs2(o4[o][0], o4[o][1]), hmax_abs2(o4[o][2], o4[o][3]));
+            full |= (hmax_abs2(cm[o], __byte_perm(cm[o], 0, 0x1032)) & 0x7FFFu) >= kHugeAmax;
+        }
+        if (full) near = 0xFu;
+        if (__any_sync(0xFFFFFFFFu, near != 0u)) {
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                if ((near >> p) & 1u) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int e = 8 * c + 2 * p + h;
+                        const float x0 = elem_in(stage, roff, e);
+                        const float x1 = elem_in(stage + tile_bytes_, roff, e);
+                        if constexpr (OP == kFwd) {
+                            set_half16(o4[0][p], h, bf16_bits(swiglu_h_exact(a.sig2_table, x0, x1)));
+                        } else {
+                            const float x2 = elem_in(stage + 2 * tile_bytes_, roff, e);
+                            const float2 r = swiglu_grads_exact(a.sig2_table, x0, x1, x2);
+                            set_half16(o4[0][p], h, bf16_bits(r.x));
+                            set_half16(o4[1][p], h, bf16_bits(r.y));
+                        }
+                    }
+                }
+            }
+            nfb += 2u * __popc(near);
+#pragma unroll
+            for (int o = 0; o < NOUT; ++o)
+                cm[o] = hmax_abs2(hmax_abs2(o4[o][0], o4[o][1]), hmax_abs2(o4[o][2], o4[o][3]));
+        }
+#pragma unroll
+        for (int o = 0; o < NOUT; ++o) {
+            acc[o] = hmax_abs2(acc[o], cm[o]);
+            *reinterpret_cast<uint4 *>(stage + (NIN - NOUT + o) * tile_bytes_ + roff[c]) =
+                make_uint4(o4[o][0], o4[o][1], o4[o][2], o4[o][3]);
+        }
+    }
+#pragma unroll
+    for (int o = 0; o < NOUT; ++o) amax[o] = hmax_abs2(acc[o], __byte_perm(acc[o], 0, 0x1032)) & 0x7FFFu;
+    if (__any_sync(0xFFFFFFFFu, nfb != 0u)) count_fallbacks_warp(a.fallbacks, nfb);
+}
+
 // Values already settled (the row pass's outputs in "both" mode, or the
 // cast's input), NV slots from `stage`: just load them and take the amax.
-template <int NV>
+template <int NV, bool kAmax = true>
 __device__ __forceinline__ void block_settled(const uint8_t *stage, int tile_bytes_, const uint32_t (&roff)[4],
                                               uint32_t (&out)[2][16], uint32_t (&amax)[2])
 {
@@ -211,7 +302,7 @@ __device__ __forceinline__ void block_settled(const uint8_t *stage, int tile_byt
             out[o][4 * c + 2] = v.z;
             out[o][4 * c + 3] = v.w;
         }
-        amax[o] = amax32_lane(out[o]);
+        if constexpr (kAmax) amax[o] = amax32_lane(out[o]);
     }
 }
 
@@ -489,28 +580,48 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
         if constexpr (MODE & kRow) {
             const int64_t grow = r0 + lane;
             const bool live = grow < a.M && c0 < a.N;
-            uint32_t out[2][16], amax[2];
-            block_values<OP>(a, stage_ptr, kTileBytes, roff, out, amax);
-            uint8_t *q[2];
-#pragma unroll
-            for (int o = 0; o < NOUT; ++o) q[o] = a.q_row[o] + grow * a.ld_qrow + c0;
             uint32_t b[2];
-            store_codes<NOUT>(out, amax, q, live, a.wide_row != 0, b);
-            // scale bytes to the tile's buffer: row (32 srb + lane), block scb
+            if constexpr (kSplit && OP == kBwd) {
+                // values settled chunk by chunk into the value slots (which
+                // the col pass then transposes), encoded from there: only one
+                // chunk of the two outputs lives in registers (measured: a
+                // gain for the backward, a loss for the forward)
+                uint32_t amax[2];
+                block_values_split<OP>(a, const_cast<uint8_t *>(stage_ptr), kTileBytes, roff, amax);
+#pragma unroll
+                for (int o = 0; o < NOUT; ++o) {
+                    uint32_t v[2][16], am[2];
+                    block_settled<1, false>(stage_ptr + (NIN - NOUT + o) * kTileBytes, kTileBytes, roff, v, am);
+                    uint8_t *q[2] = {a.q_row[o] + grow * a.ld_qrow + c0, nullptr};
+                    uint32_t bb[2];
+                    const uint32_t amx[2] = {amax[o], 0u};
+                    store_codes<1>(v, amx, q, live, a.wide_row != 0, bb);
+                    b[o] = bb[0];
+                }
+                __syncwarp();
+            } else {
+                uint32_t out[2][16], amax[2];
+                block_values<OP>(a, stage_ptr, kTileBytes, roff, out, amax);
+                uint8_t *q[2];
+#pragma unroll
+                for (int o = 0; o < NOUT; ++o) q[o] = a.q_row[o] + grow * a.ld_qrow + c0;
+                store_codes<NOUT>(out, amax, q, live, a.wide_row != 0, b);
+                if constexpr (kSplit) {
+                    // the values the col pass encodes, over inputs no longer needed
+#pragma unroll
+                    for (int o = 0; o < NOUT; ++o)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            *reinterpret_cast<uint4 *>(const_cast<uint8_t *>(stage_ptr) +
+                                                       (NIN - NOUT + o) * kTileBytes + roff[c]) =
+                                make_uint4(out[o][4 * c], out[o][4 * c + 1], out[o][4 * c + 2], out[o][4 * c + 3]);
+                    __syncwarp();
+                }
+            }
+            // scale bytes to the group's buffer: row (32 srb + lane), block 4 i + scb
             uint8_t *sb = sbuf0 + w.gslot * NOUT * scale_group_bytes<TM, G>() + 4 * G * myrow + 4 * w.i + scb;
 #pragma unroll
             for (int o = 0; o < NOUT; ++o) sb[o * scale_group_bytes<TM, G>()] = static_cast<uint8_t>(b[o]);
-            if constexpr (kSplit) {
-                // the values the col pass encodes, over inputs no longer needed
-#pragma unroll
-                for (int o = 0; o < NOUT; ++o)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        *reinterpret_cast<uint4 *>(const_cast<uint8_t *>(stage_ptr) + (NIN - NOUT + o) * kTileBytes +
-                                                   roff[c]) =
-                            make_uint4(out[o][4 * c], out[o][4 * c + 1], out[o][4 * c + 2], out[o][4 * c + 3]);
-                __syncwarp();
-            }
         }
 
         if constexpr (MODE & kCol) {
