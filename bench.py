@@ -46,12 +46,12 @@ PAGES_US = {("fwd", 1): 904.19, ("fwd", 2): 1022.98, ("fwd", 3): 1216.08,
 # captures summarised under profiles/ (small case scaled by the units
 # processed); valid only for the kernel sources they were taken on.
 TRAFFIC = {
-    "bwd_both": (10.5482e9, "468d6d0d668f7155", "profiles/bwd_both_ncu.md"),
-    "bwd_col": (8.45241e9, "468d6d0d668f7155", "profiles/bwd_col_ncu.md"),
-    "bwd_row": (8.45155e9, "468d6d0d668f7155", "profiles/bwd_row_ncu.md"),
-    "fwd_both": (6.24509e9, "468d6d0d668f7155", "profiles/fwd_both_ncu.md"),
-    "fwd_col": (5.25297e9, "468d6d0d668f7155", "profiles/fwd_col_ncu.md"),
-    "fwd_row": (5.24226e9, "468d6d0d668f7155", "profiles/fwd_row_ncu.md"),
+    "bwd_both": (10.5518e9, "61634f17427675b8", "profiles/bwd_both_ncu.md"),
+    "bwd_col": (8.45145e9, "61634f17427675b8", "profiles/bwd_col_ncu.md"),
+    "bwd_row": (8.45582e9, "61634f17427675b8", "profiles/bwd_row_ncu.md"),
+    "fwd_both": (6.24207e9, "61634f17427675b8", "profiles/fwd_both_ncu.md"),
+    "fwd_col": (5.247e9, "61634f17427675b8", "profiles/fwd_col_ncu.md"),
+    "fwd_row": (5.24108e9, "61634f17427675b8", "profiles/fwd_row_ncu.md"),
 }
 
 
