@@ -244,6 +244,8 @@ def main():
                          "on --rows rows; prints per-launch microseconds (for profiling)")
     ap.add_argument("--rows", type=int, default=M_LARGE)
     ap.add_argument("--experts", type=int, default=64)
+    ap.add_argument("--blocked", action="store_true",
+                    help="with --cell: scales in the blocked 128 x 4 tile layout")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -383,6 +385,8 @@ def run_cell(args):
     mx.init()
     kind, _, mname = args.cell.partition("_")
     mode = {"row": 1, "col": 2, "both": 3}.get(mname, 2)
+    if args.blocked:
+        mode |= mx.MXFP8_BLOCKED_SCALES
     if kind == "quant3d":
         x = synthetic.experts(args.experts, device="cuda")
         E, N, K = x.shape
@@ -395,16 +399,16 @@ def run_cell(args):
         M, N = gate.shape
         if kind == "quant":
             out = mx._alloc(M, N, mode, gate.device)
-            k = 2 if mode == 3 else 1
+            k = 2 if mode & 3 == 3 else 1
             nbytes = 2 * M * N + k * (M * N + M * N // 32)
             fn = lambda: mx.quant_2d(gate, mode, out=out)
         elif kind == "fwd":
             out = mx._alloc(M, N, mode, gate.device)
-            nbytes = cell_bytes("fwd", mode, M, N)
+            nbytes = cell_bytes("fwd", mode & 3, M, N)
             fn = lambda: mx.swiglu_fwd(gate, up, mode, out=out)
         else:
             out = mx.swiglu_bwd(dh, gate, up, mode)
-            nbytes = cell_bytes("bwd", mode, M, N)
+            nbytes = cell_bytes("bwd", mode & 3, M, N)
             fn = lambda: mx.swiglu_bwd(dh, gate, up, mode, out=out)
     for _ in range(args.warmup):
         fn()
@@ -420,7 +424,8 @@ def run_cell(args):
     flags, fb = mx.device_status()
     peak, _ = peaks()
     med = statistics.median(us)
-    print(json.dumps({"cell": args.cell, "rows": args.rows, "us_median": round(med, 2),
+    print(json.dumps({"cell": args.cell + ("+blocked" if args.blocked else ""), "rows": args.rows,
+                      "us_median": round(med, 2),
                       "us_min": round(min(us), 2), "GBps": round(nbytes / med / 1e3, 1),
                       "frac_of_peak": round(nbytes / med / 1e3 / peak, 4), "bytes": nbytes,
                       "flags": flags, "fallbacks": fb}), flush=True)

@@ -53,7 +53,24 @@ extern "C" {
 typedef enum {
     MXFP8_ROWWISE = 1, /* 1x32 blocks, row-major data + (M, N/32) scales     */
     MXFP8_COLWISE = 2, /* 32x1 blocks, column-major data + (M/32, N) scales  */
-    MXFP8_BOTH = 3     /* both sets from one read of the input               */
+    MXFP8_BOTH = 3,    /* both sets from one read of the input               */
+    /*
+     * Flag, OR-ed into any of the three (2D quantizer and the SwiGLU entry
+     * points): scales come out in the blocked layout that block-scaled
+     * tensor-core GEMMs read ("the same blocked tcgen05 layouts as the
+     * standalone quantizers", "Add swiglu + MXFP8 fused CuTe DSL kernel",
+     * commit message; 128 x 4 tiles, "[mxfp8 moe training] add compile
+     * support", review thread).  The row scales, as the (M, N/32) matrix, and
+     * the column scales, as the (N, M/32) matrix (column c's blocks along
+     * its rows), are padded to R' = 128 ceil(R/128) rows and C' = 4
+     * ceil(C/4) columns and cut into 128 x 4 tiles stored one after another
+     * row-major, 512 bytes each; entry (r, c) of a tile sits at byte
+     * (r % 32) * 16 + (r / 32) * 4 + c.  Each scale buffer then holds R' * C'
+     * bytes and its leading dimension is ignored; row-scale buffers must be
+     * 4-byte aligned.  Padding entries are left as they were or set to 0:
+     * pass zero-filled buffers.
+     */
+    MXFP8_BLOCKED_SCALES = 8
 } mxfp8_scale_mode;
 
 typedef enum {

@@ -18,10 +18,11 @@ from typing import Optional
 import torch
 
 from . import capi
-from .capi import MXFP8_BOTH, MXFP8_COLWISE, MXFP8_ROWWISE, MXFP8Error, check
+from .capi import MXFP8_BLOCKED_SCALES, MXFP8_BOTH, MXFP8_COLWISE, MXFP8_ROWWISE, MXFP8Error, check
 
 __all__ = ["capi", "MXFP8Cast", "quant_2d", "swiglu_fwd", "swiglu_bwd", "quant_3d_colwise",
-           "init", "device_status", "MXFP8_ROWWISE", "MXFP8_COLWISE", "MXFP8_BOTH", "MXFP8Error"]
+           "init", "device_status", "blocked_bytes", "MXFP8_ROWWISE", "MXFP8_COLWISE", "MXFP8_BOTH",
+           "MXFP8_BLOCKED_SCALES", "MXFP8Error"]
 
 
 @dataclass
@@ -48,22 +49,35 @@ def _check_bf16_2d(t: torch.Tensor, name: str):
         raise ValueError("%s must have unit column stride" % name)
 
 
+def blocked_bytes(rows: int, cols: int) -> int:
+    """Bytes of a (rows, cols) scale matrix in the blocked layout (padded to
+    multiples of 128 rows and 4 columns)."""
+    return -(-rows // 128) * 128 * (-(-cols // 4) * 4)
+
+
 def _alloc(M: int, N: int, mode: int, device, ld_row: Optional[int] = None) -> MXFP8Cast:
+    """Outputs for one cast; with MXFP8_BLOCKED_SCALES the scale buffers are
+    flat, zero-filled blocked matrices: (M, N/32) rowwise, (N, M/32) colwise."""
     out = MXFP8Cast()
+    blocked = bool(mode & MXFP8_BLOCKED_SCALES)
     if mode & MXFP8_ROWWISE:
         out.q_row = torch.empty((M, N), dtype=torch.uint8, device=device)
-        out.s_row = torch.empty((M, N // 32), dtype=torch.uint8, device=device)
+        out.s_row = (torch.zeros(blocked_bytes(M, N // 32), dtype=torch.uint8, device=device) if blocked
+                     else torch.empty((M, N // 32), dtype=torch.uint8, device=device))
     if mode & MXFP8_COLWISE:
         out.q_col = torch.empty((N, M), dtype=torch.uint8, device=device)
-        out.s_col = torch.empty((M // 32, N), dtype=torch.uint8, device=device)
+        out.s_col = (torch.zeros(blocked_bytes(N, M // 32), dtype=torch.uint8, device=device) if blocked
+                     else torch.empty((M // 32, N), dtype=torch.uint8, device=device))
     return out
 
 
+def _ld(t: Optional[torch.Tensor]) -> int:
+    # flat (blocked) scale buffers have no leading dimension
+    return t.stride(0) if t is not None and t.dim() == 2 else 0
+
+
 def _lds(o: MXFP8Cast):
-    return (o.q_row.stride(0) if o.q_row is not None else 0,
-            o.s_row.stride(0) if o.s_row is not None else 0,
-            o.q_col.stride(0) if o.q_col is not None else 0,
-            o.s_col.stride(0) if o.s_col is not None else 0)
+    return _ld(o.q_row), _ld(o.s_row), _ld(o.q_col), _ld(o.s_col)
 
 
 def init(stream=None) -> None:
@@ -110,11 +124,14 @@ class SwiGLUGrads:
     """Packed [dGate | dUp] MXFP8 gradients.
 
     q_row (M, 2N), s_row (M, N/16); q_col (2N, M) column-major, s_col (M/32, 2N).
+    With blocked scales, s_row and s_col are (2, bytes): one flat blocked
+    matrix per gradient.
     """
     q_row: Optional[torch.Tensor] = None
     s_row: Optional[torch.Tensor] = None
     q_col: Optional[torch.Tensor] = None
     s_col: Optional[torch.Tensor] = None
+    blocked: bool = False
 
     def dgate(self) -> MXFP8Cast:
         n = self._n()
@@ -130,9 +147,16 @@ class SwiGLUGrads:
     def _halves(self, h, n):
         r = []
         r.append(None if self.q_row is None else self.q_row[:, h * n:(h + 1) * n])
-        r.append(None if self.s_row is None else self.s_row[:, h * n // 32:(h + 1) * n // 32])
+        blocked = self.blocked
+        if blocked:
+            r.append(None if self.s_row is None else self.s_row[h])
+        else:
+            r.append(None if self.s_row is None else self.s_row[:, h * n // 32:(h + 1) * n // 32])
         r.append(None if self.q_col is None else self.q_col[h * n:(h + 1) * n])
-        r.append(None if self.s_col is None else self.s_col[:, h * n:(h + 1) * n])
+        if blocked:
+            r.append(None if self.s_col is None else self.s_col[h])
+        else:
+            r.append(None if self.s_col is None else self.s_col[:, h * n:(h + 1) * n])
         return r
 
 
@@ -149,29 +173,40 @@ def swiglu_bwd(dh: torch.Tensor, gate: torch.Tensor, up: Optional[torch.Tensor] 
         raise ValueError("dh, gate and up must have the same shape (gate/up the same strides)")
     M, N = gate.shape
     dev = gate.device
+    blocked = bool(mode & MXFP8_BLOCKED_SCALES)
     o = out
     if o is None:
-        o = SwiGLUGrads()
+        o = SwiGLUGrads(blocked=blocked)
         if mode & MXFP8_ROWWISE:
             o.q_row = torch.empty((M, 2 * N), dtype=torch.uint8, device=dev)
-            o.s_row = torch.empty((M, 2 * N // 32), dtype=torch.uint8, device=dev)
+            o.s_row = (torch.zeros((2, blocked_bytes(M, N // 32)), dtype=torch.uint8, device=dev) if blocked
+                       else torch.empty((M, 2 * N // 32), dtype=torch.uint8, device=dev))
         if mode & MXFP8_COLWISE:
             o.q_col = torch.empty((2 * N, M), dtype=torch.uint8, device=dev)
-            o.s_col = torch.empty((M // 32, 2 * N), dtype=torch.uint8, device=dev)
+            o.s_col = (torch.zeros((2, blocked_bytes(N, M // 32)), dtype=torch.uint8, device=dev) if blocked
+                       else torch.empty((M // 32, 2 * N), dtype=torch.uint8, device=dev))
     qr = o.q_row.data_ptr() if o.q_row is not None else None
     sr = o.s_row.data_ptr() if o.s_row is not None else None
     qc = o.q_col.data_ptr() if o.q_col is not None else None
     sc = o.s_col.data_ptr() if o.s_col is not None else None
     ld_qrow = o.q_row.stride(0) if o.q_row is not None else 0
-    ld_srow = o.s_row.stride(0) if o.s_row is not None else 0
     ld_qcol = o.q_col.stride(0) if o.q_col is not None else 0
-    ld_scol = o.s_col.stride(0) if o.s_col is not None else 0
+    if blocked:
+        # one flat blocked matrix per gradient
+        sr2 = None if sr is None else o.s_row[1].data_ptr()
+        sc2 = None if sc is None else o.s_col[1].data_ptr()
+        ld_srow = ld_scol = 0
+    else:
+        ld_srow = o.s_row.stride(0) if o.s_row is not None else 0
+        ld_scol = o.s_col.stride(0) if o.s_col is not None else 0
+        sr2 = None if sr is None else sr + N // 32
+        sc2 = None if sc is None else sc + N
     check(capi.mxfp8_swiglu_bwd(
         dh.data_ptr(), dh.stride(0), gate.data_ptr(), up.data_ptr(), gate.stride(0), M, N, mode,
         qr, None if qr is None else qr + N, ld_qrow,
-        sr, None if sr is None else sr + N // 32, ld_srow,
+        sr, sr2, ld_srow,
         qc, None if qc is None else qc + N * ld_qcol, ld_qcol,
-        sc, None if sc is None else sc + N, ld_scol,
+        sc, sc2, ld_scol,
         _stream(stream)), "mxfp8_swiglu_bwd")
     return o
 

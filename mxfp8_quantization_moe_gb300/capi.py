@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(_PKG, "lib", "libmxfp8.so")
 MXFP8_ROWWISE = 1
 MXFP8_COLWISE = 2
 MXFP8_BOTH = 3
+MXFP8_BLOCKED_SCALES = 8   # flag: scales in the blocked 128 x 4 tile layout
 
 STATUS_NAMES = {
     0: "MXFP8_OK", 1: "MXFP8_ERR_NULL", 2: "MXFP8_ERR_SHAPE", 3: "MXFP8_ERR_ALIGN",

@@ -215,7 +215,7 @@ constexpr int64_t kMaxDim = 0x7FFFFF00LL;  // TMA coordinates are signed 32-bit
 
 struct Spec {
     int op;               // mx::kQuant / kFwd / kBwd
-    int mode;
+    int mode;             // MXFP8_ROWWISE / COLWISE / BOTH, possibly | MXFP8_BLOCKED_SCALES
     int64_t M, N;
     const void *in[3];
     int64_t ld_in[3];
@@ -224,11 +224,17 @@ struct Spec {
     int64_t group_rows, group_stride;
 };
 
+// Bytes of a scale matrix of R rows and C columns in the blocked layout
+// (padded to multiples of 128 rows and 4 columns).
+int64_t blocked_bytes(int64_t R, int64_t C) { return (R + 127) / 128 * 128 * ((C + 3) / 4 * 4); }
+
 mxfp8_status validate(const Spec &s)
 {
     const int nin = s.op == mx::kQuant ? 1 : (s.op == mx::kFwd ? 2 : 3);
     const int nout = s.op == mx::kBwd ? 2 : 1;
-    if (s.mode < 1 || s.mode > 3) return MXFP8_ERR_MODE;
+    if ((s.mode & ~(3 | MXFP8_BLOCKED_SCALES)) != 0 || (s.mode & 3) == 0) return MXFP8_ERR_MODE;
+    const bool blocked = (s.mode & MXFP8_BLOCKED_SCALES) != 0;
+    if (blocked && s.group_stride != 0) return MXFP8_ERR_MODE;   // 2D only
     if (s.M < 0 || s.N < 0) return MXFP8_ERR_SHAPE;
     if (s.M == 0 || s.N == 0) return MXFP8_OK;
     if (s.M > kMaxDim || s.N > kMaxDim) return MXFP8_ERR_SHAPE;
@@ -248,17 +254,19 @@ mxfp8_status validate(const Spec &s)
         if (!aligned16(s.in[i]) || (s.ld_in[i] * 2) % 16 != 0) return MXFP8_ERR_ALIGN;
     }
     if (row) {
-        if (s.ld_qrow < s.N || s.ld_srow < s.N / 32) return MXFP8_ERR_LD;
-        if (!extent_ok(s.M, s.N, s.ld_qrow, 1) || !extent_ok(s.M, s.N / 32, s.ld_srow, 1))
+        if (s.ld_qrow < s.N || (!blocked && s.ld_srow < s.N / 32)) return MXFP8_ERR_LD;
+        if (!extent_ok(s.M, s.N, s.ld_qrow, 1) || (!blocked && !extent_ok(s.M, s.N / 32, s.ld_srow, 1)))
             return MXFP8_ERR_SHAPE;
         if (s.ld_qrow % 16 != 0) return MXFP8_ERR_ALIGN;
-        for (int o = 0; o < nout; ++o)
+        for (int o = 0; o < nout; ++o) {
             if (!aligned16(s.q_row[o])) return MXFP8_ERR_ALIGN;
+            if (blocked && (reinterpret_cast<uintptr_t>(s.s_row[o]) & 3u) != 0) return MXFP8_ERR_ALIGN;
+        }
     }
     if (col) {
         if (s.group_stride == 0) {  // 2D column-major
-            if (s.ld_qcol < s.M || s.ld_scol < s.N) return MXFP8_ERR_LD;
-            if (!extent_ok(s.N, s.M, s.ld_qcol, 1) || !extent_ok(s.M / 32, s.N, s.ld_scol, 1))
+            if (s.ld_qcol < s.M || (!blocked && s.ld_scol < s.N)) return MXFP8_ERR_LD;
+            if (!extent_ok(s.N, s.M, s.ld_qcol, 1) || (!blocked && !extent_ok(s.M / 32, s.N, s.ld_scol, 1)))
                 return MXFP8_ERR_SHAPE;
         }
         if (s.ld_qcol % 16 != 0) return MXFP8_ERR_ALIGN;
@@ -272,7 +280,12 @@ mxfp8_status validate(const Spec &s)
     for (int o = 0; o < nout; ++o) {
         if (row) {
             outs[n_outs++] = region(s.q_row[o], s.M, s.N, s.ld_qrow, 1);
-            outs[n_outs++] = region(s.s_row[o], s.M, s.N / 32, s.ld_srow, 1);
+            if (blocked) {
+                const int64_t b = blocked_bytes(s.M, s.N / 32);
+                outs[n_outs++] = region(s.s_row[o], 1, b, b, 1);
+            } else {
+                outs[n_outs++] = region(s.s_row[o], s.M, s.N / 32, s.ld_srow, 1);
+            }
         }
         if (col) {
             if (s.group_stride == 0) {
@@ -281,7 +294,12 @@ mxfp8_status validate(const Spec &s)
                 const int64_t E = s.M / s.group_rows;
                 outs[n_outs++] = region(s.q_col[o], E * s.N, s.group_rows, s.ld_qcol, 1);
             }
-            outs[n_outs++] = region(s.s_col[o], s.M / 32, s.N, s.ld_scol, 1);
+            if (blocked) {
+                const int64_t b = blocked_bytes(s.N, s.M / 32);
+                outs[n_outs++] = region(s.s_col[o], 1, b, b, 1);
+            } else {
+                outs[n_outs++] = region(s.s_col[o], s.M / 32, s.N, s.ld_scol, 1);
+            }
         }
     }
     for (int a = 0; a < n_outs; ++a) {
@@ -304,7 +322,8 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     if (st != MXFP8_OK) return st;
     if (!get_encoder()) return MXFP8_ERR_DEVICE;
     const int nin = s.op == mx::kQuant ? 1 : (s.op == mx::kFwd ? 2 : 3);
-    const mx::LaunchShape shape = mx::launch_shape(s.op, s.mode);
+    const int mode = s.mode & 3;
+    const mx::LaunchShape shape = mx::launch_shape(s.op, mode);
     const int tm = shape.tile_rows;
     CUtensorMap maps[3];
     std::memset(maps, 0, sizeof(maps));
@@ -330,6 +349,11 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     a.ld_scol = s.ld_scol;
     a.group_rows = s.group_rows > 0 ? s.group_rows : s.M;
     a.group_stride = s.group_stride;
+    // blocked scales: 128 x 4 tiles of the (M, N/32) row scales and of the
+    // (N, M/32) column scales
+    a.blocked = (s.mode & MXFP8_BLOCKED_SCALES) != 0;
+    a.srow_tiles_c = (s.N / 32 + 3) / 4;
+    a.scol_tiles_c = (s.M / 32 + 3) / 4;
     // whole 32-byte output blocks can go out as single 256-bit stores when
     // every block start is 32-byte aligned
     a.wide_row = (s.ld_qrow % 32) == 0;
@@ -355,9 +379,9 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     const int grid = static_cast<int>(supers < slots ? supers : slots);
     cudaError_t e;
     switch (s.op) {
-    case mx::kQuant: e = mx::launch_quant(s.mode, maps, a, grid, stream, dev); break;
-    case mx::kFwd: e = mx::launch_fwd(s.mode, maps, a, grid, stream, dev); break;
-    default: e = mx::launch_bwd(s.mode, maps, a, grid, stream, dev); break;
+    case mx::kQuant: e = mx::launch_quant(mode, maps, a, grid, stream, dev); break;
+    case mx::kFwd: e = mx::launch_fwd(mode, maps, a, grid, stream, dev); break;
+    default: e = mx::launch_bwd(mode, maps, a, grid, stream, dev); break;
     }
     return e == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
 }
@@ -385,7 +409,7 @@ const char *mxfp8_status_str(mxfp8_status s)
     case MXFP8_ERR_SHAPE: return "MXFP8_ERR_SHAPE: invalid or unsupported shape";
     case MXFP8_ERR_ALIGN: return "MXFP8_ERR_ALIGN: misaligned pointer or leading dimension";
     case MXFP8_ERR_LD: return "MXFP8_ERR_LD: leading dimension too small";
-    case MXFP8_ERR_MODE: return "MXFP8_ERR_MODE: scale mode must be 1, 2 or 3";
+    case MXFP8_ERR_MODE: return "MXFP8_ERR_MODE: scale mode must be 1, 2 or 3 (optionally | MXFP8_BLOCKED_SCALES)";
     case MXFP8_ERR_OVERLAP: return "MXFP8_ERR_OVERLAP: an output overlaps an input or another output";
     case MXFP8_ERR_LAUNCH: return "MXFP8_ERR_LAUNCH: kernel launch failed";
     case MXFP8_ERR_DEVICE: return "MXFP8_ERR_DEVICE: no usable sm_103 device or device set-up failed";

@@ -363,6 +363,14 @@ __device__ __forceinline__ void flush_row_scales(const KernelArgs &a, const uint
 #pragma unroll
         for (int o = 0; o < NOUT; ++o) {
             const uint8_t *src = gbuf + o * scale_group_bytes<TM, G>() + 4 * G * i;
+            if (a.blocked) {
+                // a tile's four blocks of a row are contiguous in the blocked
+                // layout (padding blocks of the last tile come out as 0)
+                for (int t = 0; t < gsize; ++t)
+                    *reinterpret_cast<uint32_t *>(a.s_row[o] + blocked_offset(row, blk0 + 4 * t, a.srow_tiles_c)) =
+                        *reinterpret_cast<const uint32_t *>(src + 4 * t);
+                continue;
+            }
             uint8_t *dst = a.s_row[o] + row * a.ld_srow + blk0;
             if (whole) {
                 if constexpr (G == 4)
@@ -650,9 +658,9 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             uint32_t b[2];
             store_codes<NOUT>(out, amax, q, live, a.wide_col != 0, b);
             if (live) {
+                const int64_t off = a.blocked ? blocked_offset(gcol, r0 >> 5, a.scol_tiles_c) : (r0 >> 5) * a.ld_scol + gcol;
 #pragma unroll
-                for (int o = 0; o < NOUT; ++o)
-                    a.s_col[o][(r0 >> 5) * a.ld_scol + gcol] = static_cast<uint8_t>(b[o]);
+                for (int o = 0; o < NOUT; ++o) a.s_col[o][off] = static_cast<uint8_t>(b[o]);
             }
         }
 

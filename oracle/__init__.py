@@ -71,6 +71,7 @@ def _load():
             "orc_swiglu_grads_f64": (None, [dbl, dbl, dbl, ctypes.POINTER(dbl), ctypes.POINTER(dbl)]),
             "orc_swiglu_fwd": (None, [vp, vp, i64, i64, vp, i64, i64, i64]),
             "orc_swiglu_bwd": (None, [vp, i64, vp, vp, i64, i64, vp, vp, i64, i64, i64]),
+            "orc_scales_blocked": (None, [vp, i64, i64, i64, i64, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -263,3 +264,18 @@ def swiglu_bwd(dh, gate, up, mode, rows=None, threads=None):
     dg, du = swiglu_bwd_grads(dh, gate, up, rows=rows, threads=threads)
     return (quant_2d(dg, mode, rows=rows, threads=threads),
             quant_2d(du, mode, rows=rows, threads=threads), dg, du)
+
+
+def scales_blocked(s: np.ndarray) -> np.ndarray:
+    """An (R, C) uint8 scale matrix in the blocked 128 x 4 tile layout
+    (zero-padded to multiples of 128 rows and 4 columns), flat.  For colwise
+    scales pass the (N, M/32) view, i.e. the transpose of the (M/32, N)
+    row-major scales."""
+    R, C = s.shape
+    rp, cp = -(-R // 128) * 128, -(-C // 4) * 4
+    out = np.empty(rp * cp, np.uint8)
+    st = s.strides
+    base = s
+    _load().orc_scales_blocked(base.ctypes.data, R, C, st[0], st[1], out.ctypes.data)
+    return out
+

@@ -29,6 +29,14 @@
  *    "Summary": the 3D quantizer takes (E, N, K) row-major bf16 and writes
  *    each expert's (N, K) slab column-major ("column major per expert"),
  *    blocks of 32 along N, scales (E, N/32, K).
+ *  - Scales in the blocked layout the block-scaled tensor-core GEMMs read
+ *    ("Add swiglu + MXFP8 fused CuTe DSL kernel", commit message: "the same
+ *    blocked tcgen05 layouts as the standalone quantizers"; "[mxfp8 moe
+ *    training] add compile support", review thread: scale matrices padded to
+ *    multiples of 128 rows and 4 columns).  The order inside a 128 x 4 tile
+ *    is not printed there; it is read as the published one for those GEMMs:
+ *    32 x 4 x 4, entry (r, c) of a tile at byte (r % 32) * 16 + (r / 32) * 4
+ *    + c, tiles row-major over the padded matrix.
  *
  * Every floating-point step is done in IEEE double with no contraction
  * (compile with -ffp-contract=off), no fast-math, and with plain loops in the
@@ -283,3 +291,25 @@ void orc_swiglu_bwd(const uint16_t *dh, int64_t ld_dh, const uint16_t *gate,
             dup[r * ld_out + c] = orc_bf16_from_double_via_fp32(du);
         }
 }
+
+/* ---------------------------------------------------------- blocked layout */
+
+/* The scale matrix S (R rows x C columns, entry (r, c) at
+ * s[r * rs + c * cs]) in the blocked layout: the matrix padded to
+ * R' = 128 * ceil(R / 128) rows and C' = 4 * ceil(C / 4) columns, cut into
+ * 128 x 4 tiles stored one after another row-major (512 bytes each); inside
+ * a tile, entry (r, c) at byte (r % 32) * 16 + (r / 32) * 4 + c.  Padding
+ * entries are 0.  `out` holds R' * C' bytes. */
+void orc_scales_blocked(const uint8_t *s, int64_t R, int64_t C, int64_t rs, int64_t cs, uint8_t *out)
+{
+    int64_t Rp = (R + 127) / 128 * 128;
+    int64_t Cp = (C + 3) / 4 * 4;
+    memset(out, 0, (size_t)(Rp * Cp));
+    for (int64_t r = 0; r < R; r++)
+        for (int64_t c = 0; c < C; c++) {
+            int64_t tile = (r / 128) * (Cp / 4) + (c / 4);
+            int64_t in_tile = (r % 32) * 16 + ((r % 128) / 32) * 4 + (c % 4);
+            out[tile * 512 + in_tile] = s[r * rs + c * cs];
+        }
+}
+

@@ -115,6 +115,8 @@ def test_interleaved_dgate_dup_halves_pass_validation():
 def test_valid_calls_reach_device_setup():
     assert q2d() == DEVICE
     assert capi.mxfp8_init(None) == DEVICE
+    # blocked scales ignore the scale leading dimensions
+    assert q2d(mode=11, ld_srow=0, ld_scol=0) == DEVICE
 
 
 def test_fwd_and_bwd_argument_errors():
