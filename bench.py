@@ -246,6 +246,8 @@ def main():
     ap.add_argument("--experts", type=int, default=64)
     ap.add_argument("--blocked", action="store_true",
                     help="with --cell: scales in the blocked 128 x 4 tile layout")
+    ap.add_argument("--keep-h", action="store_true",
+                    help="with --cell fwd_row / fwd_both: also write the bf16 activation")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -404,8 +406,8 @@ def run_cell(args):
             fn = lambda: mx.quant_2d(gate, mode, out=out)
         elif kind == "fwd":
             out = mx._alloc(M, N, mode, gate.device)
-            nbytes = cell_bytes("fwd", mode & 3, M, N)
-            fn = lambda: mx.swiglu_fwd(gate, up, mode, out=out)
+            nbytes = cell_bytes("fwd", mode & 3, M, N) + (2 * M * N if args.keep_h else 0)
+            fn = lambda: mx.swiglu_fwd(gate, up, mode, out=out, keep_h=args.keep_h)
         else:
             out = mx.swiglu_bwd(dh, gate, up, mode)
             nbytes = cell_bytes("bwd", mode & 3, M, N)
@@ -424,7 +426,8 @@ def run_cell(args):
     flags, fb = mx.device_status()
     peak, _ = peaks()
     med = statistics.median(us)
-    print(json.dumps({"cell": args.cell + ("+blocked" if args.blocked else ""), "rows": args.rows,
+    print(json.dumps({"cell": args.cell + ("+blocked" if args.blocked else "") + ("+h" if args.keep_h else ""),
+                      "rows": args.rows,
                       "us_median": round(med, 2),
                       "us_min": round(min(us), 2), "GBps": round(nbytes / med / 1e3, 1),
                       "frac_of_peak": round(nbytes / med / 1e3 / peak, 4), "bytes": nbytes,

@@ -129,6 +129,25 @@ mxfp8_status mxfp8_swiglu_fwd(const uint16_t *gate, const uint16_t *up, int64_t 
                               void *stream);
 
 /*
+ * The fused forward that also writes the bf16 activation h (M, N) row-major
+ * at h[r * ld_h + c], for recipes whose weight-gradient GEMMs take h in bf16
+ * ("Add swiglu + MXFP8 fused CuTe DSL kernel", section "Summary": the
+ * BF16-wgrad recipe, where the kernel emits rowwise-only casts and the
+ * activation is otherwise recomputed in bf16 at the autograd boundary).  The
+ * h written is the value the cast encoded: within one bf16 step of the
+ * correctly rounded activation (equal to it for all but about 1e-4 of the
+ * elements; see mxfp8_swiglu_fwd).  Needs the rowwise direction in `mode`
+ * (MXFP8_ERR_MODE otherwise); h non-NULL, 16-byte aligned, ld_h >= N with
+ * ld_h * 2 a multiple of 16; h may not overlap any other argument.  Every
+ * other argument as in mxfp8_swiglu_fwd.
+ */
+mxfp8_status mxfp8_swiglu_fwd_with_h(const uint16_t *gate, const uint16_t *up, int64_t ld_in,
+                                     int64_t M, int64_t N, int mode, uint16_t *h, int64_t ld_h,
+                                     uint8_t *q_row, int64_t ld_qrow, uint8_t *s_row, int64_t ld_srow,
+                                     uint8_t *q_col, int64_t ld_qcol, uint8_t *s_col, int64_t ld_scol,
+                                     void *stream);
+
+/*
  * Fused SwiGLU backward + MXFP8 cast.  From dh (M, N), gate and up:
  *   dgate = dh * up * sigmoid(gate) * (1 + gate * (1 - sigmoid(gate)))
  *   dup   = dh * gate * sigmoid(gate)

@@ -31,6 +31,7 @@ class MXFP8Cast:
     s_row: Optional[torch.Tensor] = None
     q_col: Optional[torch.Tensor] = None
     s_col: Optional[torch.Tensor] = None
+    h: Optional[torch.Tensor] = None      # the bf16 activation (forward with keep_h)
 
 
 def _stream(stream=None) -> int:
@@ -98,9 +99,10 @@ def quant_2d(x: torch.Tensor, mode: int = MXFP8_BOTH, out: Optional[MXFP8Cast] =
 
 
 def swiglu_fwd(gate: torch.Tensor, up: Optional[torch.Tensor] = None, mode: int = MXFP8_BOTH,
-               out: Optional[MXFP8Cast] = None, stream=None) -> MXFP8Cast:
+               out: Optional[MXFP8Cast] = None, stream=None, keep_h: bool = False) -> MXFP8Cast:
     """Fused SwiGLU + MXFP8 cast.  With ``up=None``, ``gate`` is the packed
-    [gate | up] (M, 2N) buffer."""
+    [gate | up] (M, 2N) buffer.  With ``keep_h`` (rowwise modes) the bf16
+    activation is returned too, in ``out.h``."""
     if up is None:
         _check_bf16_2d(gate, "gate_up")
         n = gate.shape[1] // 2
@@ -112,6 +114,15 @@ def swiglu_fwd(gate: torch.Tensor, up: Optional[torch.Tensor] = None, mode: int 
     M, N = gate.shape
     o = out if out is not None else _alloc(M, N, mode, gate.device)
     a, b, c, d = _lds(o)
+    if keep_h:
+        if o.h is None:
+            o.h = torch.empty((M, N), dtype=torch.bfloat16, device=gate.device)
+        check(capi.mxfp8_swiglu_fwd_with_h(gate.data_ptr(), up.data_ptr(), gate.stride(0), M, N, mode,
+                                           o.h.data_ptr(), o.h.stride(0),
+                                           _ptr(o.q_row), a, _ptr(o.s_row), b,
+                                           _ptr(o.q_col), c, _ptr(o.s_col), d, _stream(stream)),
+              "mxfp8_swiglu_fwd_with_h")
+        return o
     check(capi.mxfp8_swiglu_fwd(gate.data_ptr(), up.data_ptr(), gate.stride(0), M, N, mode,
                                 _ptr(o.q_row), a, _ptr(o.s_row), b,
                                 _ptr(o.q_col), c, _ptr(o.s_col), d, _stream(stream)),

@@ -44,6 +44,8 @@ SIGNATURES = {
     "mxfp8_selftest_activation": (_int, [_vp, _vp]),
     "mxfp8_swiglu_fwd_noalloc": (_int, [_vp, _vp, _i64, _i64, _i64, _int,
                                         _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]),
+    "mxfp8_swiglu_fwd_with_h": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _vp, _i64,
+                                       _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]),
 }
 
 
@@ -133,3 +135,10 @@ def mxfp8_swiglu_fwd_noalloc(gate, up, ld_in, M, N, mode, q_row, ld_qrow, s_row,
                              q_col, ld_qcol, s_col, ld_scol, stream) -> int:
     return _lib.mxfp8_swiglu_fwd_noalloc(gate, up, ld_in, M, N, mode, q_row, ld_qrow, s_row, ld_srow,
                                          q_col, ld_qcol, s_col, ld_scol, stream)
+
+
+def mxfp8_swiglu_fwd_with_h(gate, up, ld_in, M, N, mode, h, ld_h, q_row, ld_qrow, s_row, ld_srow,
+                            q_col, ld_qcol, s_col, ld_scol, stream) -> int:
+    return _lib.mxfp8_swiglu_fwd_with_h(gate, up, ld_in, M, N, mode, h, ld_h, q_row, ld_qrow, s_row, ld_srow,
+                                        q_col, ld_qcol, s_col, ld_scol, stream)
+

@@ -222,6 +222,9 @@ struct Spec {
     uint8_t *q_row[2], *s_row[2], *q_col[2], *s_col[2];
     int64_t ld_qrow, ld_srow, ld_qcol, ld_scol;
     int64_t group_rows, group_stride;
+    uint16_t *h;          // forward with the bf16 activation as an output
+    int64_t ld_h;
+    bool with_h;
 };
 
 // Bytes of a scale matrix of R rows and C columns in the blocked layout
@@ -243,6 +246,13 @@ mxfp8_status validate(const Spec &s)
     if (col && s.M % 32 != 0) return MXFP8_ERR_SHAPE;
     for (int i = 0; i < nin; ++i) {
         if (!s.in[i]) return MXFP8_ERR_NULL;
+    }
+    if (s.with_h) {
+        if (!row) return MXFP8_ERR_MODE;
+        if (!s.h) return MXFP8_ERR_NULL;
+        if (s.ld_h < s.N) return MXFP8_ERR_LD;
+        if (!extent_ok(s.M, s.N, s.ld_h, 2)) return MXFP8_ERR_SHAPE;
+        if (!aligned16(s.h) || (s.ld_h * 2) % 16 != 0) return MXFP8_ERR_ALIGN;
     }
     for (int o = 0; o < nout; ++o) {
         if (row && (!s.q_row[o] || !s.s_row[o])) return MXFP8_ERR_NULL;
@@ -277,6 +287,7 @@ mxfp8_status validate(const Spec &s)
     Region ins[3], outs[8];
     int n_outs = 0;
     for (int i = 0; i < nin; ++i) ins[i] = region(s.in[i], s.M, s.N, s.ld_in[i], 2);
+    if (s.with_h) outs[n_outs++] = region(s.h, s.M, s.N, s.ld_h, 2);
     for (int o = 0; o < nout; ++o) {
         if (row) {
             outs[n_outs++] = region(s.q_row[o], s.M, s.N, s.ld_qrow, 1);
@@ -352,6 +363,9 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     // blocked scales: 128 x 4 tiles of the (M, N/32) row scales and of the
     // (N, M/32) column scales
     a.blocked = (s.mode & MXFP8_BLOCKED_SCALES) != 0;
+    a.h_out = s.with_h ? s.h : nullptr;
+    a.ld_h = s.ld_h;
+    a.wide_h = s.with_h && (reinterpret_cast<uintptr_t>(s.h) & 31u) == 0 && (s.ld_h * 2) % 32 == 0;
     a.srow_tiles_c = (s.N / 32 + 3) / 4;
     a.scol_tiles_c = (s.M / 32 + 3) / 4;
     // whole 32-byte output blocks can go out as single 256-bit stores when
@@ -463,6 +477,29 @@ mxfp8_status mxfp8_swiglu_fwd(const uint16_t *gate, const uint16_t *up, int64_t 
     s.ld_srow = ld_srow;
     s.ld_qcol = ld_qcol;
     s.ld_scol = ld_scol;
+    return run(s, stream);
+}
+
+mxfp8_status mxfp8_swiglu_fwd_with_h(const uint16_t *gate, const uint16_t *up, int64_t ld_in, int64_t M,
+                                     int64_t N, int mode, uint16_t *h, int64_t ld_h, uint8_t *q_row,
+                                     int64_t ld_qrow, uint8_t *s_row, int64_t ld_srow, uint8_t *q_col,
+                                     int64_t ld_qcol, uint8_t *s_col, int64_t ld_scol, void *stream)
+{
+    Spec s = blank(mx::kFwd, mode, M, N);
+    s.in[0] = gate;
+    s.in[1] = up;
+    s.ld_in[0] = s.ld_in[1] = ld_in;
+    s.q_row[0] = q_row;
+    s.s_row[0] = s_row;
+    s.q_col[0] = q_col;
+    s.s_col[0] = s_col;
+    s.ld_qrow = ld_qrow;
+    s.ld_srow = ld_srow;
+    s.ld_qcol = ld_qcol;
+    s.ld_scol = ld_scol;
+    s.with_h = true;
+    s.h = h;
+    s.ld_h = ld_h;
     return run(s, stream);
 }
 

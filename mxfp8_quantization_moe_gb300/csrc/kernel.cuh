@@ -322,6 +322,22 @@ __device__ __forceinline__ void transpose_subtile(uint32_t slot, const uint32_t 
     __syncwarp();
 }
 
+// the lane's 32 bf16 values (16 words) to row `row`, columns c0..c0+31 of h
+__device__ __forceinline__ void store_h(const KernelArgs &a, const uint32_t (&v)[16], int64_t row, int64_t c0)
+{
+    uint16_t *dst = a.h_out + row * a.ld_h + c0;
+    if (a.wide_h) {
+        const uint32_t lo[8] = {v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]};
+        const uint32_t hi[8] = {v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15]};
+        st_global_v8(dst, lo);
+        st_global_v8(dst + 16, hi);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            __stcs(reinterpret_cast<uint4 *>(dst) + j, make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+    }
+}
+
 // encode the lane's block(s) and store the 32 codes at `q` (16-byte aligned;
 // one 256-bit store -- a whole sector -- when `wide` says 32-byte aligned);
 // returns the scale bytes in b[o]
@@ -610,6 +626,10 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             } else {
                 uint32_t out[2][16], amax[2];
                 block_values<OP>(a, stage_ptr, kTileBytes, roff, out, amax);
+                if constexpr (OP == kFwd) {
+                    // the activation itself, for callers that keep it in bf16
+                    if (a.h_out != nullptr && live) store_h(a, out[0], grow, c0);
+                }
                 uint8_t *q[2];
 #pragma unroll
                 for (int o = 0; o < NOUT; ++o) q[o] = a.q_row[o] + grow * a.ld_qrow + c0;

@@ -150,3 +150,26 @@ def test_3d_argument_errors():
     assert f(X, 2, 64, 64, Q + 8, S, None) == ALIGN
     assert f(X, 2, 64, 64, X + 64, S, None) == OVERLAP    # data over the input
     assert f(X, 2 ** 19, 8192, 64, Q, S, None) == SHAPE    # E * N beyond the TMA coordinate range
+
+
+def fwd_h(mode=1, h=0x60000000, ld_h=256, M=128, N=256, **kw):
+    return capi.mxfp8_swiglu_fwd_with_h(X, X + 0x1000000, N, M, N, mode, h, ld_h,
+                                        kw.get("q_row", Q), 256, S, 8, QC, 128, SC, 256, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(mode=2), MODE),                       # the activation comes from the row pass
+    (dict(h=0), NULL),
+    (dict(ld_h=128), LD),
+    (dict(h=0x60000000 + 4), ALIGN), (dict(ld_h=260), ALIGN),
+    (dict(h=Q + 256), OVERLAP),                 # h over the rowwise data
+    (dict(h=X + 64), OVERLAP),                  # h over gate
+])
+def test_fwd_with_h_argument_errors(kw, status):
+    assert fwd_h(**kw) == status
+
+
+@pytest.mark.skipif(not NO_GPU, reason="would launch on fake pointers")
+def test_fwd_with_h_valid_call_reaches_device_setup():
+    assert fwd_h(mode=3) == DEVICE
+

@@ -274,3 +274,30 @@ def test_status_clean_and_fallback_path_used():
     flags, fallbacks = device_status()
     assert flags == 0
     assert fallbacks > 0      # the every-gate tests exercise the double path
+
+
+@pytest.mark.parametrize("mode", [1, 3])
+def test_fwd_with_h_writes_the_encoded_activation(mode):
+    """The forward that also writes the bf16 activation: the casts as usual,
+    and h within one bf16 step of the oracle's correctly rounded activation
+    everywhere, equal to it in all but 1e-3 of the elements (the fast
+    activation's error bound, 33 units of 2^-24, over a bf16 step of 2^-8,
+    twice: 66 * 2^-16 ~ 1e-3); the codes are exactly the cast of that h."""
+    M, N = 1024, 576
+    gate, up, _ = rand_inputs(M, N, 31)
+    import mxfp8_quantization_moe_gb300 as mx
+    got = mx.swiglu_fwd(gate, up, mode, keep_h=True)
+    torch.cuda.synchronize()
+    want, h_want = O.swiglu_fwd(bits(gate), bits(up), mode)
+    compare({k: u8(getattr(got, k)) for k in want}, want, what="fwd-with-h")
+    h = bits(got.h)
+    hv = (h.astype(np.uint32) << 16).view(np.float32)
+    wv = (h_want.astype(np.uint32) << 16).view(np.float32)
+    diff = h != h_want
+    steps = np.abs(h.astype(np.int32) - h_want.astype(np.int32))[diff]
+    assert np.all((np.sign(hv[diff]) == np.sign(wv[diff])) & (steps == 1)), "more than one bf16 step"
+    assert diff.sum() <= 1e-3 * h.size, diff.sum()
+    print("h differs from the correctly rounded activation at", int(diff.sum()), "of", h.size)
+    # the rowwise codes are the standalone cast of the h written
+    q = O.quant_2d(h, O.ROWWISE)
+    assert np.array_equal(u8(got.q_row), q["q_row"]) and np.array_equal(u8(got.s_row), q["s_row"])
