@@ -28,6 +28,9 @@ ROWWISE = 1
 COLWISE = 2
 BOTH = 3
 
+SILU = 0      # activations of the gated forms
+GELU = 1
+
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "mxfp8_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
@@ -72,6 +75,12 @@ def _load():
             "orc_swiglu_fwd": (None, [vp, vp, i64, i64, vp, i64, i64, i64]),
             "orc_swiglu_bwd": (None, [vp, i64, vp, vp, i64, i64, vp, vp, i64, i64, i64]),
             "orc_scales_blocked": (None, [vp, i64, i64, i64, i64, vp]),
+            "orc_normal_cdf": (dbl, [dbl]),
+            "orc_normal_pdf": (dbl, [dbl]),
+            "orc_geglu_h_f64": (dbl, [dbl, dbl]),
+            "orc_geglu_grads_f64": (None, [dbl, dbl, dbl, ctypes.POINTER(dbl), ctypes.POINTER(dbl)]),
+            "orc_gated_fwd": (None, [ctypes.c_int, vp, vp, i64, i64, vp, i64, i64, i64]),
+            "orc_gated_bwd": (None, [ctypes.c_int, vp, i64, vp, vp, i64, i64, vp, vp, i64, i64, i64]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -142,6 +151,20 @@ def e4m3_value(c: int) -> float:
 
 def sigmoid(g: float) -> float:
     return float(lib().orc_sigmoid(g))
+
+
+def normal_cdf(g: float) -> float:
+    return _load().orc_normal_cdf(g)
+
+
+def geglu_h_f64(g: float, u: float) -> float:
+    return _load().orc_geglu_h_f64(g, u)
+
+
+def geglu_grads_f64(dh: float, g: float, u: float):
+    a, b = ctypes.c_double(), ctypes.c_double()
+    _load().orc_geglu_grads_f64(dh, g, u, ctypes.byref(a), ctypes.byref(b))
+    return a.value, b.value
 
 
 def swiglu_h_f64(g: float, u: float) -> float:
@@ -216,8 +239,9 @@ def quant_3d_colwise(x: np.ndarray, experts=None, threads: int | None = None):
     return q, s
 
 
-def swiglu_fwd_h(gate: np.ndarray, up: np.ndarray, rows=None, threads: int | None = None):
-    """bf16 h = bf16(fp32(silu(gate) * up)) for (M, N) gate/up (same row stride)."""
+def swiglu_fwd_h(gate: np.ndarray, up: np.ndarray, rows=None, threads: int | None = None, act: int = SILU):
+    """bf16 h = bf16(fp32(act(gate) * up)) for (M, N) gate/up (same row stride);
+    act = SILU (g sigma(g)) or GELU (g Phi(g))."""
     assert gate.dtype == np.uint16 and up.dtype == np.uint16 and gate.shape == up.shape
     assert gate.strides == up.strides and gate.strides[1] == 2
     M, N = gate.shape
@@ -227,15 +251,15 @@ def swiglu_fwd_h(gate: np.ndarray, up: np.ndarray, rows=None, threads: int | Non
     L = lib()
 
     def work(a, b):
-        L.orc_swiglu_fwd(_ptr(gate), _ptr(up), ld_in, N, _ptr(h), N, a, b)
+        L.orc_gated_fwd(act, _ptr(gate), _ptr(up), ld_in, N, _ptr(h), N, a, b)
 
     _run_ranges(work, r0, r1, threads or default_threads(), 1)
     return h
 
 
 def swiglu_bwd_grads(dh: np.ndarray, gate: np.ndarray, up: np.ndarray, rows=None,
-                     threads: int | None = None):
-    """bf16 (dgate, dup) for (M, N) inputs."""
+                     threads: int | None = None, act: int = SILU):
+    """bf16 (dgate, dup) for (M, N) inputs, activation ``act``."""
     assert gate.strides == up.strides and gate.strides[1] == 2 and dh.strides[1] == 2
     M, N = gate.shape
     ld_in = gate.strides[0] // 2
@@ -246,22 +270,22 @@ def swiglu_bwd_grads(dh: np.ndarray, gate: np.ndarray, up: np.ndarray, rows=None
     L = lib()
 
     def work(a, b):
-        L.orc_swiglu_bwd(_ptr(dh), ld_dh, _ptr(gate), _ptr(up), ld_in, N,
-                         _ptr(dg), _ptr(du), N, a, b)
+        L.orc_gated_bwd(act, _ptr(dh), ld_dh, _ptr(gate), _ptr(up), ld_in, N,
+                        _ptr(dg), _ptr(du), N, a, b)
 
     _run_ranges(work, r0, r1, threads or default_threads(), 1)
     return dg, du
 
 
-def swiglu_fwd(gate, up, mode, rows=None, threads=None):
+def swiglu_fwd(gate, up, mode, rows=None, threads=None, act=SILU):
     """Oracle of the fused forward: h, then the standalone 2D quantizer."""
-    h = swiglu_fwd_h(gate, up, rows=rows, threads=threads)
+    h = swiglu_fwd_h(gate, up, rows=rows, threads=threads, act=act)
     return quant_2d(h, mode, rows=rows, threads=threads), h
 
 
-def swiglu_bwd(dh, gate, up, mode, rows=None, threads=None):
+def swiglu_bwd(dh, gate, up, mode, rows=None, threads=None, act=SILU):
     """Oracle of the fused backward: dgate/dup, each through the 2D quantizer."""
-    dg, du = swiglu_bwd_grads(dh, gate, up, rows=rows, threads=threads)
+    dg, du = swiglu_bwd_grads(dh, gate, up, rows=rows, threads=threads, act=act)
     return (quant_2d(dg, mode, rows=rows, threads=threads),
             quant_2d(du, mode, rows=rows, threads=threads), dg, du)
 

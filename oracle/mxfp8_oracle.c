@@ -29,6 +29,13 @@
  *    "Summary": the 3D quantizer takes (E, N, K) row-major bf16 and writes
  *    each expert's (N, K) slab column-major ("column major per expert"),
  *    blocks of 32 along N, scales (E, N/32, K).
+ *  - Other gated activations through the same kernel ("Add swiglu + MXFP8
+ *    fused CuTe DSL kernel", section "API": the activation is a
+ *    compile-time policy of the one kernel source): GEGLU, h = gelu(g) * u
+ *    with the exact GELU g * Phi(g), Phi the standard normal CDF (the erf
+ *    form, not the tanh approximation; the pages name no variant, this is
+ *    the plainest reading).  Backward: dgate = dh * u * (Phi(g) + g phi(g)),
+ *    phi the normal density; dup = dh * gelu(g).
  *  - Scales in the blocked layout the block-scaled tensor-core GEMMs read
  *    ("Add swiglu + MXFP8 fused CuTe DSL kernel", commit message: "the same
  *    blocked tcgen05 layouts as the standalone quantizers"; "[mxfp8 moe
@@ -261,24 +268,57 @@ void orc_swiglu_grads_f64(double dh, double g, double u, double *dgate, double *
     *dup = dh * g * s;
 }
 
-/* h (bf16) for rows [r_begin, r_end): h[r * ld_h + c]. */
-void orc_swiglu_fwd(const uint16_t *gate, const uint16_t *up, int64_t ld_in,
-                    int64_t N, uint16_t *h, int64_t ld_h,
-                    int64_t r_begin, int64_t r_end)
+/* ------------------------------------------------------------- GEGLU */
+
+/* Phi(g) = P(Z <= g) for a standard normal Z = erfc(-g / sqrt 2) / 2 */
+double orc_normal_cdf(double g)
+{
+    return 0.5 * erfc(-g * 0.70710678118654752440);
+}
+
+/* phi(g) = exp(-g^2 / 2) / sqrt(2 pi) */
+double orc_normal_pdf(double g)
+{
+    return exp(-0.5 * g * g) * 0.39894228040143267794;
+}
+
+/* h = gelu(g) * u = (g * Phi(g)) * u */
+double orc_geglu_h_f64(double g, double u)
+{
+    return g * orc_normal_cdf(g) * u;
+}
+
+/* dgate = dh * u * (Phi(g) + g * phi(g)), dup = dh * g * Phi(g) */
+void orc_geglu_grads_f64(double dh, double g, double u, double *dgate, double *dup)
+{
+    double p = orc_normal_cdf(g);
+    *dgate = dh * u * (p + g * orc_normal_pdf(g));
+    *dup = dh * g * p;
+}
+
+/* ---------------------------------------------- gated forward / backward */
+
+#define ORC_ACT_SILU 0
+#define ORC_ACT_GELU 1
+
+/* h (bf16) for rows [r_begin, r_end): h[r * ld_h + c], activation `act`. */
+void orc_gated_fwd(int act, const uint16_t *gate, const uint16_t *up, int64_t ld_in,
+                   int64_t N, uint16_t *h, int64_t ld_h, int64_t r_begin, int64_t r_end)
 {
     for (int64_t r = r_begin; r < r_end; r++)
         for (int64_t c = 0; c < N; c++) {
             double g = orc_bf16_to_double(gate[r * ld_in + c]);
             double u = orc_bf16_to_double(up[r * ld_in + c]);
-            h[r * ld_h + c] = orc_bf16_from_double_via_fp32(orc_swiglu_h_f64(g, u));
+            double v = act == ORC_ACT_GELU ? orc_geglu_h_f64(g, u) : orc_swiglu_h_f64(g, u);
+            h[r * ld_h + c] = orc_bf16_from_double_via_fp32(v);
         }
 }
 
-/* dgate, dup (bf16) for rows [r_begin, r_end). */
-void orc_swiglu_bwd(const uint16_t *dh, int64_t ld_dh, const uint16_t *gate,
-                    const uint16_t *up, int64_t ld_in, int64_t N,
-                    uint16_t *dgate, uint16_t *dup, int64_t ld_out,
-                    int64_t r_begin, int64_t r_end)
+/* dgate, dup (bf16) for rows [r_begin, r_end), activation `act`. */
+void orc_gated_bwd(int act, const uint16_t *dh, int64_t ld_dh, const uint16_t *gate,
+                   const uint16_t *up, int64_t ld_in, int64_t N,
+                   uint16_t *dgate, uint16_t *dup, int64_t ld_out,
+                   int64_t r_begin, int64_t r_end)
 {
     for (int64_t r = r_begin; r < r_end; r++)
         for (int64_t c = 0; c < N; c++) {
@@ -286,10 +326,29 @@ void orc_swiglu_bwd(const uint16_t *dh, int64_t ld_dh, const uint16_t *gate,
             double g = orc_bf16_to_double(gate[r * ld_in + c]);
             double u = orc_bf16_to_double(up[r * ld_in + c]);
             double dg, du;
-            orc_swiglu_grads_f64(d, g, u, &dg, &du);
+            if (act == ORC_ACT_GELU)
+                orc_geglu_grads_f64(d, g, u, &dg, &du);
+            else
+                orc_swiglu_grads_f64(d, g, u, &dg, &du);
             dgate[r * ld_out + c] = orc_bf16_from_double_via_fp32(dg);
             dup[r * ld_out + c] = orc_bf16_from_double_via_fp32(du);
         }
+}
+
+/* the SwiGLU entry points of the gated forms */
+void orc_swiglu_fwd(const uint16_t *gate, const uint16_t *up, int64_t ld_in,
+                    int64_t N, uint16_t *h, int64_t ld_h,
+                    int64_t r_begin, int64_t r_end)
+{
+    orc_gated_fwd(ORC_ACT_SILU, gate, up, ld_in, N, h, ld_h, r_begin, r_end);
+}
+
+void orc_swiglu_bwd(const uint16_t *dh, int64_t ld_dh, const uint16_t *gate,
+                    const uint16_t *up, int64_t ld_in, int64_t N,
+                    uint16_t *dgate, uint16_t *dup, int64_t ld_out,
+                    int64_t r_begin, int64_t r_end)
+{
+    orc_gated_bwd(ORC_ACT_SILU, dh, ld_dh, gate, up, ld_in, N, dgate, dup, ld_out, r_begin, r_end);
 }
 
 /* ---------------------------------------------------------- blocked layout */
