@@ -248,6 +248,8 @@ def main():
                     help="with --cell: scales in the blocked 128 x 4 tile layout")
     ap.add_argument("--keep-h", action="store_true",
                     help="with --cell fwd_row / fwd_both: also write the bf16 activation")
+    ap.add_argument("--act", default="silu", choices=["silu", "gelu"],
+                    help="with --cell fwd_* / bwd_*: the gated activation (gelu: GEGLU)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -407,11 +409,11 @@ def run_cell(args):
         elif kind == "fwd":
             out = mx._alloc(M, N, mode, gate.device)
             nbytes = cell_bytes("fwd", mode & 3, M, N) + (2 * M * N if args.keep_h else 0)
-            fn = lambda: mx.swiglu_fwd(gate, up, mode, out=out, keep_h=args.keep_h)
+            fn = lambda: mx.swiglu_fwd(gate, up, mode, out=out, keep_h=args.keep_h, act=args.act)
         else:
-            out = mx.swiglu_bwd(dh, gate, up, mode)
+            out = mx.swiglu_bwd(dh, gate, up, mode, act=args.act)
             nbytes = cell_bytes("bwd", mode & 3, M, N)
-            fn = lambda: mx.swiglu_bwd(dh, gate, up, mode, out=out)
+            fn = lambda: mx.swiglu_bwd(dh, gate, up, mode, out=out, act=args.act)
     for _ in range(args.warmup):
         fn()
     torch.cuda.synchronize()
@@ -426,7 +428,8 @@ def run_cell(args):
     flags, fb = mx.device_status()
     peak, _ = peaks()
     med = statistics.median(us)
-    print(json.dumps({"cell": args.cell + ("+blocked" if args.blocked else "") + ("+h" if args.keep_h else ""),
+    print(json.dumps({"cell": args.cell + ("+blocked" if args.blocked else "") + ("+h" if args.keep_h else "")
+                      + ("+gelu" if args.act == "gelu" else ""),
                       "rows": args.rows,
                       "us_median": round(med, 2),
                       "us_min": round(min(us), 2), "GBps": round(nbytes / med / 1e3, 1),

@@ -209,10 +209,31 @@ mxfp8_status mxfp8_swiglu_fwd_noalloc(const uint16_t *gate, const uint16_t *up, 
                                       void *stream);
 
 /*
+ * GEGLU: the same fused forward and backward with the activation gelu(g) =
+ * g * Phi(g), Phi the standard normal CDF (exact erf form), in place of
+ * silu ("Add swiglu + MXFP8 fused CuTe DSL kernel", section "API": the
+ * activation is a compile-time policy of the one kernel).  h = gelu(gate) *
+ * up; dgate = dh * up * (Phi(gate) + gate * phi(gate)) with phi the normal
+ * density, dup = dh * gelu(gate).  Arguments, layouts, rules, errors and the
+ * tolerance are those of mxfp8_swiglu_fwd / mxfp8_swiglu_bwd.
+ */
+mxfp8_status mxfp8_geglu_fwd(const uint16_t *gate, const uint16_t *up, int64_t ld_in,
+                             int64_t M, int64_t N, int mode,
+                             uint8_t *q_row, int64_t ld_qrow, uint8_t *s_row, int64_t ld_srow,
+                             uint8_t *q_col, int64_t ld_qcol, uint8_t *s_col, int64_t ld_scol,
+                             void *stream);
+mxfp8_status mxfp8_geglu_bwd(const uint16_t *dh, int64_t ld_dh, const uint16_t *gate,
+                             const uint16_t *up, int64_t ld_in, int64_t M, int64_t N, int mode,
+                             uint8_t *dg_row, uint8_t *du_row, int64_t ld_qrow,
+                             uint8_t *dg_srow, uint8_t *du_srow, int64_t ld_srow,
+                             uint8_t *dg_col, uint8_t *du_col, int64_t ld_qcol,
+                             uint8_t *dg_scol, uint8_t *du_scol, int64_t ld_scol, void *stream);
+
+/*
  * Sticky device-side status of the current device.  Kernels never trap: a
  * pipeline wait that exceeds its limit (about a second) makes the kernel set
  * a flag bit and return.  flags: bit 0 consumer wait, bit 1 producer wait,
- * bit 2 drain wait, bit 3 self-test wait.  fallbacks: number of SwiGLU
+ * bit 2 drain wait, bit 3 self-test wait.  fallbacks: number of SwiGLU or GEGLU
  * elements the fused kernels recomputed exactly (values near a scale
  * boundary, gates outside the fast range, huge or non-finite blocks).
  * Synchronizes `stream`; with reset != 0 clears both afterwards.
@@ -230,6 +251,14 @@ mxfp8_status mxfp8_device_status(uint32_t *flags, uint64_t *fallbacks, int reset
  * kernels' recomputation windows are sized for.
  */
 mxfp8_status mxfp8_selftest_activation(float *out, void *stream);
+
+/*
+ * Self-test of the GEGLU fast path, like mxfp8_selftest_activation: for every
+ * bf16 pattern g, out[k*65536 + g] for k = 0 Phi(g), 1 gelu(g), 2 gelu'(g) =
+ * Phi(g) + g phi(g), as the fused GEGLU kernels compute them.  `out` is a
+ * device buffer of 3 * 65536 floats, 16-byte aligned.
+ */
+mxfp8_status mxfp8_selftest_activation_gelu(float *out, void *stream);
 
 /*
  * Failure-detection self-test: launches one thread that waits on a shared

@@ -99,10 +99,15 @@ def quant_2d(x: torch.Tensor, mode: int = MXFP8_BOTH, out: Optional[MXFP8Cast] =
 
 
 def swiglu_fwd(gate: torch.Tensor, up: Optional[torch.Tensor] = None, mode: int = MXFP8_BOTH,
-               out: Optional[MXFP8Cast] = None, stream=None, keep_h: bool = False) -> MXFP8Cast:
+               out: Optional[MXFP8Cast] = None, stream=None, keep_h: bool = False,
+               act: str = "silu") -> MXFP8Cast:
     """Fused SwiGLU + MXFP8 cast.  With ``up=None``, ``gate`` is the packed
     [gate | up] (M, 2N) buffer.  With ``keep_h`` (rowwise modes) the bf16
-    activation is returned too, in ``out.h``."""
+    activation is returned too, in ``out.h``.  ``act="gelu"`` gives GEGLU."""
+    if act not in ("silu", "gelu"):
+        raise ValueError("act must be 'silu' or 'gelu'")
+    if act == "gelu" and keep_h:
+        raise ValueError("keep_h is available for SwiGLU only")
     if up is None:
         _check_bf16_2d(gate, "gate_up")
         n = gate.shape[1] // 2
@@ -123,10 +128,10 @@ def swiglu_fwd(gate: torch.Tensor, up: Optional[torch.Tensor] = None, mode: int 
                                            _ptr(o.q_col), c, _ptr(o.s_col), d, _stream(stream)),
               "mxfp8_swiglu_fwd_with_h")
         return o
-    check(capi.mxfp8_swiglu_fwd(gate.data_ptr(), up.data_ptr(), gate.stride(0), M, N, mode,
-                                _ptr(o.q_row), a, _ptr(o.s_row), b,
-                                _ptr(o.q_col), c, _ptr(o.s_col), d, _stream(stream)),
-          "mxfp8_swiglu_fwd")
+    fn = capi.mxfp8_geglu_fwd if act == "gelu" else capi.mxfp8_swiglu_fwd
+    check(fn(gate.data_ptr(), up.data_ptr(), gate.stride(0), M, N, mode,
+             _ptr(o.q_row), a, _ptr(o.s_row), b,
+             _ptr(o.q_col), c, _ptr(o.s_col), d, _stream(stream)), fn.__name__)
     return o
 
 
@@ -172,9 +177,13 @@ class SwiGLUGrads:
 
 
 def swiglu_bwd(dh: torch.Tensor, gate: torch.Tensor, up: Optional[torch.Tensor] = None,
-               mode: int = MXFP8_BOTH, out: Optional[SwiGLUGrads] = None, stream=None) -> SwiGLUGrads:
+               mode: int = MXFP8_BOTH, out: Optional[SwiGLUGrads] = None, stream=None,
+               act: str = "silu") -> SwiGLUGrads:
     """Fused SwiGLU backward + MXFP8 cast of dgate and dup into packed
-    [dGate | dUp] outputs.  With ``up=None``, ``gate`` is the packed input."""
+    [dGate | dUp] outputs.  With ``up=None``, ``gate`` is the packed input.
+    ``act="gelu"`` gives the GEGLU backward."""
+    if act not in ("silu", "gelu"):
+        raise ValueError("act must be 'silu' or 'gelu'")
     if up is None:
         n = gate.shape[1] // 2
         gate, up = gate[:, :n], gate[:, n:]
@@ -212,13 +221,14 @@ def swiglu_bwd(dh: torch.Tensor, gate: torch.Tensor, up: Optional[torch.Tensor] 
         ld_scol = o.s_col.stride(0) if o.s_col is not None else 0
         sr2 = None if sr is None else sr + N // 32
         sc2 = None if sc is None else sc + N
-    check(capi.mxfp8_swiglu_bwd(
+    fn = capi.mxfp8_geglu_bwd if act == "gelu" else capi.mxfp8_swiglu_bwd
+    check(fn(
         dh.data_ptr(), dh.stride(0), gate.data_ptr(), up.data_ptr(), gate.stride(0), M, N, mode,
         qr, None if qr is None else qr + N, ld_qrow,
         sr, sr2, ld_srow,
         qc, None if qc is None else qc + N * ld_qcol, ld_qcol,
         sc, sc2, ld_scol,
-        _stream(stream)), "mxfp8_swiglu_bwd")
+        _stream(stream)), fn.__name__)
     return o
 
 

@@ -21,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIB_DIR, "libmxfp8.so")
 
-SOURCES = ["api.cu", "ops_quant.cu", "ops_fwd.cu", "ops_bwd.cu"]
+SOURCES = ["api.cu", "ops_quant.cu", "ops_fwd.cu", "ops_bwd.cu", "ops_fwd_gelu.cu", "ops_bwd_gelu.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE,
          "-Xcompiler", "-Wall"]

@@ -46,6 +46,12 @@ SIGNATURES = {
                                         _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]),
     "mxfp8_swiglu_fwd_with_h": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _vp, _i64,
                                        _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]),
+    "mxfp8_geglu_fwd": (_int, [_vp, _vp, _i64, _i64, _i64, _int,
+                               _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]),
+    "mxfp8_geglu_bwd": (_int, [_vp, _i64, _vp, _vp, _i64, _i64, _i64, _int,
+                               _vp, _vp, _i64, _vp, _vp, _i64,
+                               _vp, _vp, _i64, _vp, _vp, _i64, _vp]),
+    "mxfp8_selftest_activation_gelu": (_int, [_vp, _vp]),
 }
 
 
@@ -141,4 +147,22 @@ def mxfp8_swiglu_fwd_with_h(gate, up, ld_in, M, N, mode, h, ld_h, q_row, ld_qrow
                             q_col, ld_qcol, s_col, ld_scol, stream) -> int:
     return _lib.mxfp8_swiglu_fwd_with_h(gate, up, ld_in, M, N, mode, h, ld_h, q_row, ld_qrow, s_row, ld_srow,
                                         q_col, ld_qcol, s_col, ld_scol, stream)
+
+
+def mxfp8_geglu_fwd(gate, up, ld_in, M, N, mode, q_row, ld_qrow, s_row, ld_srow,
+                    q_col, ld_qcol, s_col, ld_scol, stream) -> int:
+    return _lib.mxfp8_geglu_fwd(gate, up, ld_in, M, N, mode, q_row, ld_qrow, s_row, ld_srow,
+                                q_col, ld_qcol, s_col, ld_scol, stream)
+
+
+def mxfp8_geglu_bwd(dh, ld_dh, gate, up, ld_in, M, N, mode,
+                    dg_row, du_row, ld_qrow, dg_srow, du_srow, ld_srow,
+                    dg_col, du_col, ld_qcol, dg_scol, du_scol, ld_scol, stream) -> int:
+    return _lib.mxfp8_geglu_bwd(dh, ld_dh, gate, up, ld_in, M, N, mode,
+                                dg_row, du_row, ld_qrow, dg_srow, du_srow, ld_srow,
+                                dg_col, du_col, ld_qcol, dg_scol, du_scol, ld_scol, stream)
+
+
+def mxfp8_selftest_activation_gelu(out, stream) -> int:
+    return _lib.mxfp8_selftest_activation_gelu(out, stream)
 

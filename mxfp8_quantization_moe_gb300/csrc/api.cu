@@ -23,23 +23,32 @@ namespace {
 using mx::KernelArgs;
 
 // ----------------------------------------------------- device-side state
-// Read-only sigmoid table (double, one entry per bf16 bit pattern), sticky
-// status bits and the count of elements settled by the double path.  Each
-// device that loads the library holds its own copy.
+// Read-only tables, one entry per bf16 bit pattern g (sigmoid(g) in double
+// and as a (hi, lo) float pair; (hi, lo) pairs of Phi(g) and gelu'(g)),
+// sticky status bits and the count of elements settled by the exact path.
+// Each device that loads the library holds its own copy.
 __device__ double g_sig_table[65536];
 __device__ float2 g_sig2_table[65536];
+__device__ float4 g_gelu_table[65536];
 __device__ unsigned g_status;
 __device__ unsigned long long g_fallbacks;
 
-__global__ void init_sigmoid_table_kernel(double *table, float2 *table2)
+__device__ __forceinline__ float2 float_pair(double v)
+{
+    const float hi = __double2float_rn(v);
+    return make_float2(hi, __double2float_rn(__dadd_rn(v, -static_cast<double>(hi))));
+}
+
+__global__ void init_sigmoid_table_kernel(double *table, float2 *table2, float4 *gelu_table)
 {
     const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= 65536u) return;
     const double g = static_cast<double>(__uint_as_float(i << 16));
     const double s = __drcp_rn(__dadd_rn(1.0, exp(-g)));  // 1 / (1 + e^-g)
     table[i] = s;
-    const float hi = __double2float_rn(s);
-    table2[i] = make_float2(hi, __double2float_rn(__dadd_rn(s, -static_cast<double>(hi))));
+    table2[i] = float_pair(s);
+    const float2 p = float_pair(mx::normal_cdf_double(g)), d = float_pair(mx::gelu_grad_double(g));
+    gelu_table[i] = make_float4(p.x, p.y, d.x, d.y);
 }
 
 __global__ void selftest_wait_kernel(unsigned *status, long long limit)
@@ -75,12 +84,31 @@ __global__ void selftest_activation_kernel(float *out)
     }
 }
 
+// The GEGLU fast path's gate-only factors for every bf16 pattern g (pairs of
+// consecutive patterns per thread): Phi(g), gelu(g) = g Phi(g) as the forward
+// forms it (the product (g * 1) Phi), gelu'(g) = Phi(g) + g phi(g).
+__global__ void selftest_activation_gelu_kernel(float *out)
+{
+    const uint32_t i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+    if (i >= 65536u) return;
+    const uint32_t gw = i | ((i + 1) << 16);
+    uint64_t E, DG, DU;
+    const uint64_t P = mx::normal_cdf2(gw, E);
+    mx::geglu_grads2(0x3F803F80u, gw, 0x3F803F80u, DG, DU);     // dh = u = 1: DG = gelu'(g)
+    const uint64_t V[3] = {P, mx::geglu_h2(gw, 0x3F803F80u), DG};
+    for (int k = 0; k < 3; ++k) {
+        out[k * 65536 + i] = mx::f2lo(V[k]);
+        out[k * 65536 + i + 1] = mx::f2hi(V[k]);
+    }
+}
+
 constexpr int kMaxDevices = 64;
 
 struct DeviceState {
     std::atomic<bool> ready{false};
     double *table = nullptr;
     float2 *table2 = nullptr;
+    float4 *gelu_table = nullptr;
     unsigned *status = nullptr;
     unsigned long long *fallbacks = nullptr;
     int sms = 0;
@@ -116,11 +144,13 @@ mxfp8_status ensure_device(cudaStream_t stream, int *dev_out, DeviceState **stat
     d.table = static_cast<double *>(p);
     if (cudaGetSymbolAddress(&p, g_sig2_table) != cudaSuccess) return MXFP8_ERR_DEVICE;
     d.table2 = static_cast<float2 *>(p);
+    if (cudaGetSymbolAddress(&p, g_gelu_table) != cudaSuccess) return MXFP8_ERR_DEVICE;
+    d.gelu_table = static_cast<float4 *>(p);
     if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return MXFP8_ERR_DEVICE;
     d.status = static_cast<unsigned *>(p);
     if (cudaGetSymbolAddress(&p, g_fallbacks) != cudaSuccess) return MXFP8_ERR_DEVICE;
     d.fallbacks = static_cast<unsigned long long *>(p);
-    init_sigmoid_table_kernel<<<256, 256, 0, stream>>>(d.table, d.table2);
+    init_sigmoid_table_kernel<<<256, 256, 0, stream>>>(d.table, d.table2, d.gelu_table);
     if (cudaGetLastError() != cudaSuccess) return MXFP8_ERR_DEVICE;
     if (cudaMemsetAsync(d.status, 0, sizeof(unsigned), stream) != cudaSuccess ||
         cudaMemsetAsync(d.fallbacks, 0, sizeof(unsigned long long), stream) != cudaSuccess)
@@ -225,6 +255,7 @@ struct Spec {
     uint16_t *h;          // forward with the bf16 activation as an output
     int64_t ld_h;
     bool with_h;
+    int act;              // mx::kSilu / kGelu (the fused ops)
 };
 
 // Bytes of a scale matrix of R rows and C columns in the blocked layout
@@ -384,6 +415,7 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     }
     a.sig_table = d->table;
     a.sig2_table = d->table2;
+    a.gelu_table = d->gelu_table;
     a.status = d->status;
     a.fallbacks = d->fallbacks;
     a.wait_limit = d->wait_limit;
@@ -394,8 +426,14 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     cudaError_t e;
     switch (s.op) {
     case mx::kQuant: e = mx::launch_quant(mode, maps, a, grid, stream, dev); break;
-    case mx::kFwd: e = mx::launch_fwd(mode, maps, a, grid, stream, dev); break;
-    default: e = mx::launch_bwd(mode, maps, a, grid, stream, dev); break;
+    case mx::kFwd:
+        e = s.act == mx::kGelu ? mx::launch_fwd_gelu(mode, maps, a, grid, stream, dev)
+                               : mx::launch_fwd(mode, maps, a, grid, stream, dev);
+        break;
+    default:
+        e = s.act == mx::kGelu ? mx::launch_bwd_gelu(mode, maps, a, grid, stream, dev)
+                               : mx::launch_bwd(mode, maps, a, grid, stream, dev);
+        break;
     }
     return e == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
 }
@@ -531,6 +569,56 @@ mxfp8_status mxfp8_swiglu_bwd(const uint16_t *dh, int64_t ld_dh, const uint16_t 
     return run(s, stream);
 }
 
+mxfp8_status mxfp8_geglu_fwd(const uint16_t *gate, const uint16_t *up, int64_t ld_in, int64_t M,
+                              int64_t N, int mode, uint8_t *q_row, int64_t ld_qrow, uint8_t *s_row,
+                              int64_t ld_srow, uint8_t *q_col, int64_t ld_qcol, uint8_t *s_col,
+                              int64_t ld_scol, void *stream)
+{
+    Spec s = blank(mx::kFwd, mode, M, N);
+    s.in[0] = gate;
+    s.in[1] = up;
+    s.ld_in[0] = s.ld_in[1] = ld_in;
+    s.q_row[0] = q_row;
+    s.s_row[0] = s_row;
+    s.q_col[0] = q_col;
+    s.s_col[0] = s_col;
+    s.ld_qrow = ld_qrow;
+    s.ld_srow = ld_srow;
+    s.ld_qcol = ld_qcol;
+    s.ld_scol = ld_scol;
+    s.act = mx::kGelu;
+    return run(s, stream);
+}
+
+mxfp8_status mxfp8_geglu_bwd(const uint16_t *dh, int64_t ld_dh, const uint16_t *gate,
+                              const uint16_t *up, int64_t ld_in, int64_t M, int64_t N, int mode,
+                              uint8_t *dg_row, uint8_t *du_row, int64_t ld_qrow, uint8_t *dg_srow,
+                              uint8_t *du_srow, int64_t ld_srow, uint8_t *dg_col, uint8_t *du_col,
+                              int64_t ld_qcol, uint8_t *dg_scol, uint8_t *du_scol, int64_t ld_scol,
+                              void *stream)
+{
+    Spec s = blank(mx::kBwd, mode, M, N);
+    s.in[0] = dh;
+    s.in[1] = gate;
+    s.in[2] = up;
+    s.ld_in[0] = ld_dh;
+    s.ld_in[1] = s.ld_in[2] = ld_in;
+    s.q_row[0] = dg_row;
+    s.q_row[1] = du_row;
+    s.s_row[0] = dg_srow;
+    s.s_row[1] = du_srow;
+    s.q_col[0] = dg_col;
+    s.q_col[1] = du_col;
+    s.s_col[0] = dg_scol;
+    s.s_col[1] = du_scol;
+    s.ld_qrow = ld_qrow;
+    s.ld_srow = ld_srow;
+    s.ld_qcol = ld_qcol;
+    s.ld_scol = ld_scol;
+    s.act = mx::kGelu;
+    return run(s, stream);
+}
+
 mxfp8_status mxfp8_quant_3d_colwise(const uint16_t *x, int64_t E, int64_t N, int64_t K, uint8_t *q,
                                     uint8_t *s, void *stream)
 {
@@ -587,6 +675,19 @@ mxfp8_status mxfp8_selftest_activation(float *out, void *stream)
     mxfp8_status r = ensure_device(st, &dev, &d);
     if (r != MXFP8_OK) return r;
     selftest_activation_kernel<<<128, 256, 0, st>>>(out);
+    return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
+}
+
+mxfp8_status mxfp8_selftest_activation_gelu(float *out, void *stream)
+{
+    if (!out) return MXFP8_ERR_NULL;
+    if (!aligned16(out)) return MXFP8_ERR_ALIGN;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int dev;
+    DeviceState *d;
+    mxfp8_status r = ensure_device(st, &dev, &d);
+    if (r != MXFP8_OK) return r;
+    selftest_activation_gelu_kernel<<<128, 256, 0, st>>>(out);
     return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
 }
 
@@ -716,6 +817,7 @@ extern "C" mxfp8_status mxfp8_swiglu_fwd_noalloc(const uint16_t *gate, const uin
     std::memset(&a, 0, sizeof(a));
     a.sig_table = d->table;
     a.sig2_table = d->table2;
+    a.gelu_table = d->gelu_table;
     a.fallbacks = d->fallbacks;
     a.status = d->status;
     const int64_t chunks = M * ((N + 7) / 8);

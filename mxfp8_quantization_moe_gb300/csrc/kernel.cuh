@@ -118,7 +118,7 @@ __device__ __forceinline__ void set_half16(uint32_t &w, int hi, uint32_t b)
 // rather than only the blocks whose amax sits at that mantissa pair, also
 // covers the other direction's blocks in "both" mode, and measured cheaper
 // than scanning the risky blocks.)  Returns the outputs' amax patterns.
-template <int OP>
+template <int OP, int ACT>
 __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t *stage, int tile_bytes_,
                                              const uint32_t (&roff)[4], uint32_t (&out)[2][16],
                                              uint32_t (&amax)[2])
@@ -142,22 +142,22 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
 #pragma unroll
             for (int p = 0; p < 4; ++p) out[0][4 * c + p] = in[0][p];
         } else if constexpr (OP == kFwd) {
-            gates_ok &= gates_fast8(in[0]);
+            gates_ok &= gates_fast8(in[0], Gated<ACT>::kMinGate2);
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
-                const uint64_t H = swiglu_h2(in[0][p], in[1][p]);
+                const uint64_t H = Gated<ACT>::h2(in[0][p], in[1][p]);
                 out[0][4 * c + p] = pack_bf16x2(f2lo(H), f2hi(H));
-                near |= static_cast<uint32_t>(near_mid2(H, kNearH)) << (4 * c + p);
+                near |= static_cast<uint32_t>(near_mid2(H, Gated<ACT>::kWinH)) << (4 * c + p);
             }
         } else {
-            gates_ok &= gates_fast8(in[1]);
+            gates_ok &= gates_fast8(in[1], Gated<ACT>::kMinGate2);
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
                 uint64_t DG, DU;
-                swiglu_grads2(in[0][p], in[1][p], in[2][p], DG, DU);
+                Gated<ACT>::grads2(in[0][p], in[1][p], in[2][p], DG, DU);
                 out[0][4 * c + p] = pack_bf16x2(f2lo(DG), f2hi(DG));
                 out[1][4 * c + p] = pack_bf16x2(f2lo(DU), f2hi(DU));
-                near |= static_cast<uint32_t>(near_mid2(DG, kNearDgate) | near_mid2(DU, kNearDup)) << (4 * c + p);
+                near |= static_cast<uint32_t>(near_mid2(DG, Gated<ACT>::kWinDgate) | near_mid2(DU, Gated<ACT>::kWinDup)) << (4 * c + p);
             }
         }
     }
@@ -178,10 +178,10 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
                         const float x0 = elem_in(stage, roff, e);
                         const float x1 = elem_in(stage + tile_bytes_, roff, e);
                         if constexpr (OP == kFwd) {
-                            set_half16(out[0][j], h, bf16_bits(swiglu_h_exact(a.sig2_table, x0, x1)));
+                            set_half16(out[0][j], h, bf16_bits(Gated<ACT>::h_exact(a, x0, x1)));
                         } else {
                             const float x2 = elem_in(stage + 2 * tile_bytes_, roff, e);
-                            const float2 r = swiglu_grads_exact(a.sig2_table, x0, x1, x2);
+                            const float2 r = Gated<ACT>::grads_exact(a, x0, x1, x2);
                             set_half16(out[0][j], h, bf16_bits(r.x));
                             set_half16(out[1][j], h, bf16_bits(r.y));
                         }
@@ -201,7 +201,7 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
 // finite -- the per-element form of the block rules, which is all they need)
 // and written at once over the chunk's inputs in the value slots, so only
 // one chunk of outputs lives in registers.  Returns the outputs' amax.
-template <int OP>
+template <int OP, int ACT>
 __device__ __forceinline__ void block_values_split(const KernelArgs &a, uint8_t *stage, int tile_bytes_,
                                                    const uint32_t (&roff)[4], uint32_t (&amax)[2])
 {
@@ -224,22 +224,22 @@ __device__ __forceinline__ void block_values_split(const KernelArgs &a, uint8_t 
         uint32_t near = 0;   // bit p: pair p of the chunk
         bool full;
         if constexpr (OP == kFwd) {
-            full = !gates_fast8(in[0]);
+            full = !gates_fast8(in[0], Gated<ACT>::kMinGate2);
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
-                const uint64_t H = swiglu_h2(in[0][p], in[1][p]);
+                const uint64_t H = Gated<ACT>::h2(in[0][p], in[1][p]);
                 o4[0][p] = pack_bf16x2(f2lo(H), f2hi(H));
-                near |= static_cast<uint32_t>(near_mid2(H, kNearH)) << p;
+                near |= static_cast<uint32_t>(near_mid2(H, Gated<ACT>::kWinH)) << p;
             }
         } else {
-            full = !gates_fast8(in[1]);
+            full = !gates_fast8(in[1], Gated<ACT>::kMinGate2);
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
                 uint64_t DG, DU;
-                swiglu_grads2(in[0][p], in[1][p], in[2][p], DG, DU);
+                Gated<ACT>::grads2(in[0][p], in[1][p], in[2][p], DG, DU);
                 o4[0][p] = pack_bf16x2(f2lo(DG), f2hi(DG));
                 o4[1][p] = pack_bf16x2(f2lo(DU), f2hi(DU));
-                near |= static_cast<uint32_t>(near_mid2(DG, kNearDgate) | near_mid2(DU, kNearDup)) << p;
+                near |= static_cast<uint32_t>(near_mid2(DG, Gated<ACT>::kWinDgate) | near_mid2(DU, Gated<ACT>::kWinDup)) << p;
             }
         }
         uint32_t cm[2];
@@ -259,10 +259,10 @@ __device__ __forceinline__ void block_values_split(const KernelArgs &a, uint8_t 
                         const float x0 = elem_in(stage, roff, e);
                         const float x1 = elem_in(stage + tile_bytes_, roff, e);
                         if constexpr (OP == kFwd) {
-                            set_half16(o4[0][p], h, bf16_bits(swiglu_h_exact(a.sig2_table, x0, x1)));
+                            set_half16(o4[0][p], h, bf16_bits(Gated<ACT>::h_exact(a, x0, x1)));
                         } else {
                             const float x2 = elem_in(stage + 2 * tile_bytes_, roff, e);
-                            const float2 r = swiglu_grads_exact(a.sig2_table, x0, x1, x2);
+                            const float2 r = Gated<ACT>::grads_exact(a, x0, x1, x2);
                             set_half16(o4[0][p], h, bf16_bits(r.x));
                             set_half16(o4[1][p], h, bf16_bits(r.y));
                         }
@@ -447,7 +447,7 @@ struct TileWalk {
 };
 
 // ------------------------------------------------------------------ kernel
-template <int OP, int MODE, int TM, int STAGES, int CTAS, int G>
+template <int OP, int MODE, int TM, int STAGES, int CTAS, int G, int ACT>
 __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
     mxfp8_tile_kernel(const __grid_constant__ CUtensorMap tm0,
                       const __grid_constant__ CUtensorMap tm1,
@@ -611,7 +611,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
                 // chunk of the two outputs lives in registers (measured: a
                 // gain for the backward, a loss for the forward)
                 uint32_t amax[2];
-                block_values_split<OP>(a, const_cast<uint8_t *>(stage_ptr), kTileBytes, roff, amax);
+                block_values_split<OP, ACT>(a, const_cast<uint8_t *>(stage_ptr), kTileBytes, roff, amax);
 #pragma unroll
                 for (int o = 0; o < NOUT; ++o) {
                     uint32_t v[2][16], am[2];
@@ -625,7 +625,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
                 __syncwarp();
             } else {
                 uint32_t out[2][16], amax[2];
-                block_values<OP>(a, stage_ptr, kTileBytes, roff, out, amax);
+                block_values<OP, ACT>(a, stage_ptr, kTileBytes, roff, out, amax);
                 if constexpr (OP == kFwd) {
                     // the activation itself, for callers that keep it in bf16
                     if (a.h_out != nullptr && live) store_h(a, out[0], grow, c0);
@@ -666,7 +666,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             if constexpr (kSplit || OP == kQuant)
                 block_settled<NOUT>(stage_ptr + kFirst * kTileBytes, kTileBytes, roff, out, amax);
             else
-                block_values<OP>(a, stage_ptr, kTileBytes, roff, out, amax);
+                block_values<OP, ACT>(a, stage_ptr, kTileBytes, roff, out, amax);
             int64_t grp = 0, rin = r0;
             if (a.group_stride != 0) {  // 3D: per-expert column-major output
                 grp = r0 / a.group_rows;

@@ -9,7 +9,7 @@ namespace mx {
 
 // Launch mxfp8_tile_kernel<OP, MODE> on `grid` CTAs.  The dynamic shared
 // memory limit of the instantiation is raised once per device.
-template <int OP, int MODE>
+template <int OP, int MODE, int ACT>
 cudaError_t launch_tiles(const CUtensorMap (&maps)[3], const KernelArgs &a, int grid,
                          cudaStream_t stream, int device)
 {
@@ -20,7 +20,7 @@ cudaError_t launch_tiles(const CUtensorMap (&maps)[3], const KernelArgs &a, int 
     constexpr size_t kSmem = smem_bytes<OP, kTM, kStages, kGroup>();
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
     static_assert(kCtas * (kSmem + 1024) <= 228 * 1024, "shared memory per SM");
-    auto kern = mxfp8_tile_kernel<OP, MODE, kTM, kStages, kCtas, kGroup>;
+    auto kern = mxfp8_tile_kernel<OP, MODE, kTM, kStages, kCtas, kGroup, ACT>;
     static std::atomic<unsigned long long> attr_done{0};
     const unsigned long long bit = 1ull << (device & 63);
     if (!(attr_done.load(std::memory_order_acquire) & bit)) {
@@ -60,22 +60,26 @@ inline LaunchShape launch_shape(int op, int mode)
     }
 }
 
-// per-op dispatch over the scale mode (one translation unit per op)
-cudaError_t launch_quant(int mode, const CUtensorMap (&maps)[3], const KernelArgs &a, int grid,
-                         cudaStream_t stream, int device);
-cudaError_t launch_fwd(int mode, const CUtensorMap (&maps)[3], const KernelArgs &a, int grid,
-                       cudaStream_t stream, int device);
-cudaError_t launch_bwd(int mode, const CUtensorMap (&maps)[3], const KernelArgs &a, int grid,
-                       cudaStream_t stream, int device);
+// per-op (and activation) dispatch over the scale mode, one translation unit
+// each
+#define MX_DECLARE_LAUNCH(NAME)                                                                  \
+    cudaError_t NAME(int mode, const CUtensorMap (&maps)[3], const KernelArgs &a, int grid,      \
+                     cudaStream_t stream, int device);
+MX_DECLARE_LAUNCH(launch_quant)
+MX_DECLARE_LAUNCH(launch_fwd)
+MX_DECLARE_LAUNCH(launch_bwd)
+MX_DECLARE_LAUNCH(launch_fwd_gelu)
+MX_DECLARE_LAUNCH(launch_bwd_gelu)
+#undef MX_DECLARE_LAUNCH
 
-#define MX_DEFINE_LAUNCH(NAME, OP)                                                               \
+#define MX_DEFINE_LAUNCH(NAME, OP, ACT)                                                          \
     cudaError_t NAME(int mode, const CUtensorMap (&maps)[3], const KernelArgs &a, int grid,      \
                      cudaStream_t stream, int device)                                            \
     {                                                                                            \
         switch (mode) {                                                                          \
-        case kRow: return launch_tiles<OP, kRow>(maps, a, grid, stream, device);                 \
-        case kCol: return launch_tiles<OP, kCol>(maps, a, grid, stream, device);                 \
-        case kBoth: return launch_tiles<OP, kBoth>(maps, a, grid, stream, device);               \
+        case kRow: return launch_tiles<OP, kRow, ACT>(maps, a, grid, stream, device);            \
+        case kCol: return launch_tiles<OP, kCol, ACT>(maps, a, grid, stream, device);            \
+        case kBoth: return launch_tiles<OP, kBoth, ACT>(maps, a, grid, stream, device);          \
         default: return cudaErrorInvalidValue;                                                   \
         }                                                                                        \
     }

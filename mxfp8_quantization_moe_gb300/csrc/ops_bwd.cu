@@ -3,5 +3,5 @@
 #include "launch.cuh"
 
 namespace mx {
-MX_DEFINE_LAUNCH(launch_bwd, kBwd)
+MX_DEFINE_LAUNCH(launch_bwd, kBwd, kSilu)
 }  // namespace mx

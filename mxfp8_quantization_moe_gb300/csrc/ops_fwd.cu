@@ -3,5 +3,5 @@
 #include "launch.cuh"
 
 namespace mx {
-MX_DEFINE_LAUNCH(launch_fwd, kFwd)
+MX_DEFINE_LAUNCH(launch_fwd, kFwd, kSilu)
 }  // namespace mx

@@ -3,5 +3,5 @@
 #include "launch.cuh"
 
 namespace mx {
-MX_DEFINE_LAUNCH(launch_quant, kQuant)
+MX_DEFINE_LAUNCH(launch_quant, kQuant, kSilu)
 }  // namespace mx

@@ -173,3 +173,33 @@ def test_fwd_with_h_argument_errors(kw, status):
 def test_fwd_with_h_valid_call_reaches_device_setup():
     assert fwd_h(mode=3) == DEVICE
 
+
+
+def test_geglu_entry_points_validate_like_swiglu():
+    f = capi.mxfp8_geglu_fwd
+    assert f(X, 0, 512, 64, 256, 1, Q, 256, S, 8, None, 0, None, 0, None) == NULL
+    assert f(X, X + 2, 512, 64, 256, 1, Q, 256, S, 8, None, 0, None, 0, None) == ALIGN
+    assert f(X, X + 256, 200, 64, 256, 1, Q, 256, S, 8, None, 0, None, 0, None) == LD
+    assert f(X, X + 256, 512, 64, 256, 4, Q, 256, S, 8, None, 0, None, 0, None) == MODE
+    assert f(X, X + 256, 512, 64, 256, 1, X + 1024, 256, S, 8, None, 0, None, 0, None) == OVERLAP
+    assert f(X, X + 256, 512, 0, 256, 1, Q, 256, S, 8, None, 0, None, 0, None) == OK   # empty
+    b = capi.mxfp8_geglu_bwd
+    assert b(0, 256, X, X + 256, 512, 64, 256, 1, Q, Q + 256, 512, S, S + 8, 16,
+             None, None, 0, None, None, 0, None) == NULL
+    assert b(X + 0x100000, 256, X, X + 256, 512, 64, 256, 2, None, None, 0, None, None, 0,
+             QC, QC + 256 * 64 - 16, 64, SC, SC + 256, 512, None) == OVERLAP
+    if NO_GPU:
+        assert f(X, X + 256, 512, 64, 256, 1, Q, 256, S, 8, None, 0, None, 0, None) == DEVICE
+        assert b(X + 0x100000, 256, X, X + 256, 512, 64, 256, 2, None, None, 0, None, None, 0,
+                 QC, QC + 256 * 64, 64, SC, SC + 256, 512, None) == DEVICE
+
+
+def test_python_binding_rejects_unknown_activation():
+    import mxfp8_quantization_moe_gb300 as mx
+    g = torch.zeros((32, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        mx.swiglu_fwd(g, g, 1, act="relu")
+    with pytest.raises(ValueError):
+        mx.swiglu_fwd(g, g, 1, act="gelu", keep_h=True)
+    with pytest.raises(ValueError):
+        mx.swiglu_bwd(g, g, g, 1, act="tanh")

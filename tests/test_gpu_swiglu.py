@@ -28,9 +28,9 @@ def _stream():
     return torch.cuda.current_stream().cuda_stream
 
 
-def fwd_gpu(gate, up, mode, blocks=None):
-    """Run the fused forward; return host outputs (only the 32-row blocks in
-    `blocks` when given, gathered on the device)."""
+def fwd_gpu(gate, up, mode, blocks=None, act="silu"):
+    """Run the fused forward (act "gelu": GEGLU); return host outputs (only
+    the 32-row blocks in `blocks` when given, gathered on the device)."""
     M, N = gate.shape
     o = {}
     if mode & 1:
@@ -39,9 +39,10 @@ def fwd_gpu(gate, up, mode, blocks=None):
         o["q_col"], o["s_col"] = Guarded((N, M)), Guarded((M // 32, N))
     p = lambda k: o[k].t.data_ptr() if k in o else None
     ld = lambda k: o[k].t.stride(0) if k in o else 0
-    st = capi.mxfp8_swiglu_fwd(gate.data_ptr(), up.data_ptr(), gate.stride(0), M, N, mode,
-                               p("q_row"), ld("q_row"), p("s_row"), ld("s_row"),
-                               p("q_col"), ld("q_col"), p("s_col"), ld("s_col"), _stream())
+    fn = capi.mxfp8_geglu_fwd if act == "gelu" else capi.mxfp8_swiglu_fwd
+    st = fn(gate.data_ptr(), up.data_ptr(), gate.stride(0), M, N, mode,
+            p("q_row"), ld("q_row"), p("s_row"), ld("s_row"),
+            p("q_col"), ld("q_col"), p("s_col"), ld("s_col"), _stream())
     assert st == 0, capi.STATUS_NAMES[st]
     torch.cuda.synchronize()
     for k, g in o.items():
@@ -70,7 +71,7 @@ def rows_of(blocks):
     return np.concatenate([np.arange(32 * b, 32 * b + 32) for b in blocks]).tolist()
 
 
-def bwd_gpu(dh, gate, up, mode, blocks=None):
+def bwd_gpu(dh, gate, up, mode, blocks=None, act="silu"):
     """Packed [dGate | dUp] outputs; returns per-tensor dicts (dgate, dup)."""
     M, N = gate.shape
     o = {}
@@ -82,7 +83,8 @@ def bwd_gpu(dh, gate, up, mode, blocks=None):
     sr = o["s_row"].t.data_ptr() if mode & 1 else None
     qc = o["q_col"].t.data_ptr() if mode & 2 else None
     sc = o["s_col"].t.data_ptr() if mode & 2 else None
-    st = capi.mxfp8_swiglu_bwd(
+    fn = capi.mxfp8_geglu_bwd if act == "gelu" else capi.mxfp8_swiglu_bwd
+    st = fn(
         dh.data_ptr(), dh.stride(0), gate.data_ptr(), up.data_ptr(), gate.stride(0), M, N, mode,
         qr, qr + N if qr else None, 2 * N if qr else 0,
         sr, sr + N // 32 if sr else None, N // 16 if sr else 0,
@@ -125,13 +127,17 @@ def _host_rows(t, blocks):
     return bits(t.index_select(0, sel))
 
 
-def oracle_fwd(gate, up, mode, blocks=None):
+ACTS = {"silu": O.SILU, "gelu": O.GELU}
+
+
+def oracle_fwd(gate, up, mode, blocks=None, act="silu"):
     """Oracle on the whole tensors, or on the stacked 32-row blocks."""
-    return O.swiglu_fwd(_host_rows(gate, blocks), _host_rows(up, blocks), mode)[0]
+    return O.swiglu_fwd(_host_rows(gate, blocks), _host_rows(up, blocks), mode, act=ACTS[act])[0]
 
 
-def oracle_bwd(dh, gate, up, mode, blocks=None):
-    r = O.swiglu_bwd(_host_rows(dh, blocks), _host_rows(gate, blocks), _host_rows(up, blocks), mode)
+def oracle_bwd(dh, gate, up, mode, blocks=None, act="silu"):
+    r = O.swiglu_bwd(_host_rows(dh, blocks), _host_rows(gate, blocks), _host_rows(up, blocks), mode,
+                     act=ACTS[act])
     return r[0], r[1]
 
 

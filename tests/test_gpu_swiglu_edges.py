@@ -1,6 +1,6 @@
-"""GPU parity of the fused SwiGLU kernels where their fast arithmetic is
-weakest; same tolerance as the other SwiGLU tests (scales bit-exact, codes
-within one, at most 1e-4 of them).
+"""GPU parity of the fused gated-activation kernels (SwiGLU and GEGLU) where
+their fast arithmetic is weakest; same tolerance as the other SwiGLU tests
+(scales bit-exact, codes within one, at most 1e-4 of them).
 
 * rounding midpoints: every row block and column block holds one element
   whose exact fp32 value lies a few ulps from the bf16 rounding midpoint
@@ -9,12 +9,13 @@ within one, at most 1e-4 of them).
 * tiny gates (bf16 subnormals up to 2^-60) against huge ups / dh, so that
   g * sigmoid(g) is far below the normal fp32 range while the result is not;
 * zero gates against non-finite ups, gates at the ends of the bf16 range.
-The input values are picked with plain numpy double arithmetic (only to find
-candidates); the expected outputs come from the oracle.
+The input values are picked with plain numpy / SciPy double arithmetic (only
+to find candidates); the expected outputs come from the oracle.
 """
 import numpy as np
 import pytest
 import torch
+from scipy.special import ndtr
 
 from test_gpu_swiglu import bwd_gpu, compare, fwd_gpu, oracle_bwd, oracle_fwd
 from mxfp8_quantization_moe_gb300 import device_status
@@ -44,6 +45,19 @@ def gates(lo=-64.0, hi=60.0, tiny=2.0 ** -20):
 
 def sigmoid(g):
     return 1.0 / (1.0 + np.exp(-g))
+
+
+def factors(act, g):
+    """(activation f(g), its derivative f'(g), the gate band around the
+    derivative's zero) for candidate search."""
+    if act == "gelu":
+        p = ndtr(g)
+        return g * p, p + g * np.exp(-0.5 * g * g) / np.sqrt(2 * np.pi), (g > -1.0) & (g < -0.5)
+    s = sigmoid(g)
+    return g * s, s * (1 + g * (1 - s)), (g > -1.6) & (g < -1.0)
+
+
+ACTS = ["silu", "gelu"]
 
 
 def mid_dist(x):
@@ -82,42 +96,43 @@ def small_background(rng, scale_exp):
             torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
 
 
-def fwd_midpoint_inputs(seed):
+def fwd_midpoint_inputs(seed, act="silu"):
     gb, g = gates()
-    gi, k = hits_1d(g * sigmoid(g))
+    f, _, _ = factors(act, g)
+    gi, k = hits_1d(f)
     rng = np.random.default_rng(seed)
     gate, up = small_background(rng, -6)       # |h| < 8 * 2^-6 off the diagonal
     r, c = diagonal_positions()
     j = np.arange(len(r)) % len(gi)
-    silu = g[gi[j]] * sigmoid(g[gi[j]]) * (1 + k[j] / 128.0)
+    hv = f[gi[j]] * (1 + k[j] / 128.0)
     # exponent of up: the hit's |h| lands in [1, 2^20)
-    e = rng.integers(0, 20, len(r)) - np.floor(np.log2(np.abs(silu))).astype(np.int64)
+    e = rng.integers(0, 20, len(r)) - np.floor(np.log2(np.abs(hv))).astype(np.int64)
     gate[r, c] = gb[gi[j]]
     up[r, c] = bf16(rng.integers(0, 2, len(r)), e, k[j])
     return to_dev(gate), to_dev(up)
 
 
+@pytest.mark.parametrize("act", ACTS)
 @pytest.mark.parametrize("seed", [0, 1])
-def test_fwd_amax_at_rounding_midpoints(seed):
-    gate, up = fwd_midpoint_inputs(seed)
+def test_fwd_amax_at_rounding_midpoints(seed, act):
+    gate, up = fwd_midpoint_inputs(seed, act)
     for mode in (1, 2, 3):
-        compare(fwd_gpu(gate, up, mode), oracle_fwd(gate, up, mode), what="fwd-midpoint")
+        compare(fwd_gpu(gate, up, mode, act=act), oracle_fwd(gate, up, mode, act=act), what="fwd-midpoint")
 
 
-def bwd_midpoint_inputs(seed, which):
+def bwd_midpoint_inputs(seed, which, act="silu"):
     rng = np.random.default_rng(seed)
     gb, g = gates()
-    s = sigmoid(g)
+    f, df, band = factors(act, g)
     if which == "dup":
-        gi, k = hits_1d(g * s)                       # dup = dh * (g s)
+        gi, k = hits_1d(f)                           # dup = dh * f(g)
         k2 = np.zeros_like(k)
     else:
-        # dgate = (dh u) * silu'(g): every gate against every pair of dh and
-        # u mantissas; the closest 2048, plus the closest 256 among the gates
-        # around silu's minimum (g near -1.28), where silu' is small and its
-        # fast value least accurate
-        dsilu = s * (1 + g * (1 - s))
-        band = (g > -1.6) & (g < -1.0)
+        # dgate = (dh u) * f'(g): every gate against every pair of dh and u
+        # mantissas; the closest 2048, plus the closest 256 among the gates
+        # around the zero of f' (silu: g near -1.28, gelu: g near -0.75),
+        # where f' is small and its fast value least accurate
+        dsilu = df
         a = np.repeat(np.arange(128), 128)
         b = np.tile(np.arange(128), 128)
         prod = (1 + a / 128.0) * (1 + b / 128.0)
@@ -141,25 +156,26 @@ def bwd_midpoint_inputs(seed, which):
     j = np.arange(len(r)) % len(gi)
     gate[r, c] = gb[gi[j]]
     if which == "dup":
-        f = np.abs(g[gi[j]] * s[gi[j]] * (1 + k[j] / 128.0))
-        e = rng.integers(0, 20, len(r)) - np.floor(np.log2(f)).astype(np.int64)
+        v = np.abs(f[gi[j]] * (1 + k[j] / 128.0))
+        e = rng.integers(0, 20, len(r)) - np.floor(np.log2(v)).astype(np.int64)
         dh[r, c] = bf16(rng.integers(0, 2, len(r)), e, k[j])
         up[r, c] = bf16(0, -12, 0)                   # keeps dgate small there
     else:
-        f = np.abs((1 + g[gi[j]] * (1 - s[gi[j]])) * s[gi[j]] * (1 + k[j] / 128.0) * (1 + k2[j] / 128.0))
-        e = rng.integers(0, 20, len(r)) - np.floor(np.log2(f)).astype(np.int64)
+        v = np.abs(df[gi[j]] * (1 + k[j] / 128.0) * (1 + k2[j] / 128.0))
+        e = rng.integers(0, 20, len(r)) - np.floor(np.log2(v)).astype(np.int64)
         e1 = e // 2
         dh[r, c] = bf16(rng.integers(0, 2, len(r)), e1, k[j])
         up[r, c] = bf16(rng.integers(0, 2, len(r)), e - e1, k2[j])
     return to_dev(dh), to_dev(gate), to_dev(up)
 
 
+@pytest.mark.parametrize("act", ACTS)
 @pytest.mark.parametrize("which", ["dgate", "dup"])
-def test_bwd_amax_at_rounding_midpoints(which):
-    dh, gate, up = bwd_midpoint_inputs(3, which)
+def test_bwd_amax_at_rounding_midpoints(which, act):
+    dh, gate, up = bwd_midpoint_inputs(3, which, act)
     for mode in (1, 2, 3):
-        dg, du = bwd_gpu(dh, gate, up, mode)
-        wg, wu = oracle_bwd(dh, gate, up, mode)
+        dg, du = bwd_gpu(dh, gate, up, mode, act=act)
+        wg, wu = oracle_bwd(dh, gate, up, mode, act=act)
         compare(dg, wg, what="dgate-midpoint(%s)" % which)
         compare(du, wu, what="dup-midpoint(%s)" % which)
 
@@ -187,26 +203,29 @@ def tiny_gate_inputs(seed):
     return gbits.reshape(M, N), xbits.reshape(M, N)
 
 
-def test_fwd_tiny_gates_huge_up():
+@pytest.mark.parametrize("act", ACTS)
+def test_fwd_tiny_gates_huge_up(act):
     gbits, ubits = tiny_gate_inputs(5)
     gate, up = to_dev(gbits), to_dev(ubits)
     for mode in (1, 2, 3):
-        compare(fwd_gpu(gate, up, mode), oracle_fwd(gate, up, mode), what="fwd-tiny-gate")
+        compare(fwd_gpu(gate, up, mode, act=act), oracle_fwd(gate, up, mode, act=act), what="fwd-tiny-gate")
 
 
-def test_bwd_tiny_gates_huge_dh():
+@pytest.mark.parametrize("act", ACTS)
+def test_bwd_tiny_gates_huge_dh(act):
     gbits, dbits = tiny_gate_inputs(6)
     rng = np.random.default_rng(7)
     ubits = torch.from_numpy(rng.standard_normal((M, N)).astype(np.float32)).to(torch.bfloat16)
     dh, gate, up = to_dev(dbits), to_dev(gbits), ubits.cuda()
     for mode in (1, 2, 3):
-        dg, du = bwd_gpu(dh, gate, up, mode)
-        wg, wu = oracle_bwd(dh, gate, up, mode)
+        dg, du = bwd_gpu(dh, gate, up, mode, act=act)
+        wg, wu = oracle_bwd(dh, gate, up, mode, act=act)
         compare(dg, wg, what="dgate-tiny-gate")
         compare(du, wu, what="dup-tiny-gate")
 
 
-def test_special_values_mixed_in():
+@pytest.mark.parametrize("act", ACTS)
+def test_special_values_mixed_in(act):
     """Zero gates against +-Inf / NaN ups (NaN blocks), gates at +-bf16 max
     and the smallest subnormal, a few gates below the fast range."""
     rng = np.random.default_rng(9)
@@ -216,15 +235,17 @@ def test_special_values_mixed_in():
     gv = g.view(torch.int16).numpy().view(np.uint16).copy()
     uv = u.view(torch.int16).numpy().view(np.uint16).copy()
     idx = rng.choice(M * N, 600, replace=False)
-    specials_g = np.array([0x0000, 0x8000, 0x7F7F, 0xFF7F, 0x0001, 0x8001, 0xC300, 0xC2FF, 0x42FF], np.uint16)
+    # ... and both sides of -8 (the end of the GEGLU fast range)
+    specials_g = np.array([0x0000, 0x8000, 0x7F7F, 0xFF7F, 0x0001, 0x8001, 0xC300, 0xC2FF, 0x42FF,
+                           0xC100, 0xC101, 0xC0FF], np.uint16)
     specials_u = np.array([0x7F80, 0xFF80, 0x7FC0, 0x0001, 0x7F7F, 0x3F80], np.uint16)
     gv.reshape(-1)[idx] = specials_g[np.arange(600) % len(specials_g)]
     uv.reshape(-1)[idx] = specials_u[(np.arange(600) // len(specials_g)) % len(specials_u)]
     gate, up, dhd = to_dev(gv), to_dev(uv), dh.cuda()
     for mode in (1, 2, 3):
-        compare(fwd_gpu(gate, up, mode), oracle_fwd(gate, up, mode), what="fwd-specials")
-        dg, du = bwd_gpu(dhd, gate, up, mode)
-        wg, wu = oracle_bwd(dhd, gate, up, mode)
+        compare(fwd_gpu(gate, up, mode, act=act), oracle_fwd(gate, up, mode, act=act), what="fwd-specials")
+        dg, du = bwd_gpu(dhd, gate, up, mode, act=act)
+        wg, wu = oracle_bwd(dhd, gate, up, mode, act=act)
         compare(dg, wg, what="dgate-specials")
         compare(du, wu, what="dup-specials")
     flags, _ = device_status()
