@@ -303,3 +303,61 @@ def scales_blocked(s: np.ndarray) -> np.ndarray:
     _load().orc_scales_blocked(base.ctypes.data, R, C, st[0], st[1], out.ctypes.data)
     return out
 
+
+def _check_group_ends(ends, R: int, align: int) -> np.ndarray:
+    ends = np.asarray(ends, np.int64)
+    starts = np.concatenate([[0], ends[:-1]])
+    assert ends.ndim == 1 and len(ends) >= 1 and ends[-1] == R
+    assert np.all(ends >= starts)
+    assert np.all(ends[:-1] % align == 0)
+    return starts
+
+
+def scales_blocked_m_groups(s: np.ndarray, group_end) -> np.ndarray:
+    """Row scales of a tensor whose rows form consecutive groups (token
+    groups of a grouped GEMM; ``group_end`` the cumulative end row of each
+    group, the last = R), in the blocked layout with every group starting on
+    a fresh 128-row tile: group g's rows go to padded rows starting at the
+    sum of the earlier groups' sizes rounded up to 128 ("[mxfp8 moe
+    training] add compile support": the M-groups scale swizzle and the upper
+    bound rows + 128 * groups of the padded rows).  The padded matrix has
+    (ceil(R/128) + G) * 128 rows (at least that bound) and the columns of
+    ``scales_blocked``; it is zero outside the groups' rows.  Flat."""
+    R, C = s.shape
+    G = len(group_end)
+    starts = _check_group_ends(group_end, R, 1)
+    padded = np.zeros(((-(-R // 128) + G) * 128, C), np.uint8)
+    o = 0
+    for a, b in zip(starts, group_end):
+        padded[o:o + (b - a)] = s[a:b]
+        o += -(-(b - a) // 128) * 128
+    return scales_blocked(padded)
+
+
+def scales_blocked_k_groups(s: np.ndarray, group_end) -> np.ndarray:
+    """Column scales, as the (N, M/32) matrix (the transpose of the (M/32, N)
+    row-major scales), of a tensor whose M rows form consecutive groups
+    (``group_end`` in rows of the tensor, multiples of 32 but the last = M):
+    the blocked layout with every group's M/32-columns starting on a fresh
+    4-column tile (the K-groups scale swizzle of the same page, upper bound
+    cols + 4 * groups).  The padded matrix has N rows (as ``scales_blocked``
+    pads them) and (ceil(M/128) + G) * 4 columns.  Flat."""
+    N, C = s.shape
+    G = len(group_end)
+    M = int(group_end[-1])
+    assert C == -(-M // 32)
+    starts = _check_group_ends(group_end, M, 32)
+    padded = np.zeros((N, (-(-M // 128) + G) * 4), np.uint8)
+    o = 0
+    for a, b in zip(starts, group_end):
+        ca, cb = a // 32, -(-b // 32)
+        padded[:, o:o + (cb - ca)] = s[:, ca:cb]
+        o += -(-(cb - ca) // 4) * 4
+    return scales_blocked(padded)
+
+
+def scales_blocked_per_expert(s: np.ndarray) -> np.ndarray:
+    """(E, R, C) scale matrices, one per expert, each in the blocked layout,
+    one after another (the per-group 3D scale swizzle of "[mxfp8 moe
+    training] add compile support").  Flat."""
+    return np.concatenate([scales_blocked(np.ascontiguousarray(m)) for m in s])
