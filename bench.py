@@ -248,6 +248,9 @@ def main():
                     help="with --cell: scales in the blocked 128 x 4 tile layout")
     ap.add_argument("--keep-h", action="store_true",
                     help="with --cell fwd_row / fwd_both: also write the bf16 activation")
+    ap.add_argument("--groups", type=int, default=0,
+                    help="with --cell quant_* / fwd_* / bwd_*: per-group blocked scales for this many "
+                         "token groups of random 32-row-aligned sizes")
     ap.add_argument("--act", default="silu", choices=["silu", "gelu"],
                     help="with --cell fwd_* / bwd_*: the gated activation (gelu: GEGLU)")
     args = ap.parse_args()
@@ -401,7 +404,22 @@ def run_cell(args):
     else:
         gate, up, dh = synthetic.large(M=args.rows, N=N_LARGE, device="cuda")
         M, N = gate.shape
-        if kind == "quant":
+        ends = None
+        if args.groups:
+            gen = torch.Generator().manual_seed(11)
+            cuts = torch.randperm(M // 32 - 1, generator=gen)[:args.groups - 1].add(1).sort().values * 32
+            ends = torch.cat([cuts, torch.tensor([M])]).to(torch.int32).cuda()
+        if kind == "quant" and ends is not None:
+            k = 2 if mode & 3 == 3 else 1
+            nbytes = 2 * M * N + k * (M * N + M * N // 32)
+            fn = lambda: mx.quant_2d_grouped(gate, ends, mode & 3)
+        elif kind == "fwd" and ends is not None:
+            nbytes = cell_bytes("fwd", mode & 3, M, N)
+            fn = lambda: mx.swiglu_fwd_grouped(gate, up, ends, mode & 3, act=args.act)
+        elif ends is not None:
+            nbytes = cell_bytes("bwd", mode & 3, M, N)
+            fn = lambda: mx.swiglu_bwd_grouped(dh, gate, up, ends, mode & 3, act=args.act)
+        elif kind == "quant":
             out = mx._alloc(M, N, mode, gate.device)
             k = 2 if mode & 3 == 3 else 1
             nbytes = 2 * M * N + k * (M * N + M * N // 32)
@@ -429,7 +447,8 @@ def run_cell(args):
     peak, _ = peaks()
     med = statistics.median(us)
     print(json.dumps({"cell": args.cell + ("+blocked" if args.blocked else "") + ("+h" if args.keep_h else "")
-                      + ("+gelu" if args.act == "gelu" else ""),
+                      + ("+gelu" if args.act == "gelu" else "")
+                      + ("+groups%d" % args.groups if args.groups else ""),
                       "rows": args.rows,
                       "us_median": round(med, 2),
                       "us_min": round(min(us), 2), "GBps": round(nbytes / med / 1e3, 1),

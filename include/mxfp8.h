@@ -182,6 +182,68 @@ mxfp8_status mxfp8_quant_3d_colwise(const uint16_t *x, int64_t E, int64_t N, int
                                     uint8_t *q, uint8_t *s, void *stream);
 
 /*
+ * Per-expert 3D quantizer, either or both directions from one read of x
+ * (E, N, K) bf16 row-major:
+ *  - rowwise (1x32 blocks along K): data (E, N, K) row-major, q_row[(e*N +
+ *    n)*K + k]; scales (E, N, K/32) row-major.  Needs K % 32 == 0.
+ *  - colwise (32x1 blocks along N): the layout of mxfp8_quant_3d_colwise.
+ *    Needs N % 32 == 0.
+ * With MXFP8_BLOCKED_SCALES each expert's scale matrix -- rowwise (N, K/32),
+ * colwise (K, N/32) (column k's blocks along its row) -- is laid out as in
+ * that flag's description, the experts one after another: E * R' * C' bytes
+ * per buffer (R', C' the padded rows and columns of one expert's matrix);
+ * needs N % 32 == 0 ("[mxfp8 moe training] add compile support": the
+ * per-group 3D scale swizzle, the 3D cast the perf analysis asks for).
+ * K % 8 == 0 always.
+ */
+mxfp8_status mxfp8_quant_3d(const uint16_t *x, int64_t E, int64_t N, int64_t K, int mode,
+                            uint8_t *q_row, uint8_t *s_row, uint8_t *q_col, uint8_t *s_col,
+                            void *stream);
+
+/*
+ * Per-group blocked scales for grouped-GEMM operands ("[mxfp8 moe training]
+ * add compile support": the M-groups and K-groups scale swizzles, padded
+ * rows + 128 * groups and cols + 4 * groups): the M rows of the input form
+ * G consecutive token groups, group_end[g] (device memory, int32) the end
+ * row of group g (cumulative; non-decreasing; every end but the last a
+ * multiple of 32; the last = M; 1 <= G <= 256).  The data outputs are those
+ * of the ungrouped calls; the scales always come out blocked (see
+ * MXFP8_BLOCKED_SCALES, which `mode` may carry or not):
+ *  - row scales (M-groups): group g's rows of the (M, N/32) matrix start on
+ *    a fresh 128-row tile, at the sum of the earlier groups' sizes rounded
+ *    up to 128; the buffer holds (ceil(M/128) + G) * 128 rows of
+ *    4 * ceil(N/128) bytes;
+ *  - column scales (K-groups): group g's columns of the (N, M/32) matrix
+ *    start on a fresh 4-column tile, at the sum of the earlier groups'
+ *    block counts rounded up to 4; the matrix has (ceil(M/128) + G) * 4
+ *    columns and 128 * ceil(N/128) rows.
+ * Entries outside the groups are not written: pass zero-filled buffers.
+ * The group ends are checked on the device (they are never read by the
+ * host, so the call does not synchronise): if they break a rule, no scale
+ * is written and status bit 4 is set (mxfp8_device_status).  Other
+ * arguments and errors as in mxfp8_quant_2d / mxfp8_swiglu_fwd /
+ * mxfp8_swiglu_bwd; `act` selects the gated activation (0 SwiGLU, 1 GEGLU;
+ * else MXFP8_ERR_MODE).
+ */
+mxfp8_status mxfp8_quant_2d_grouped(const uint16_t *x, int64_t ld_x, int64_t M, int64_t N, int mode,
+                                    const int32_t *group_end, int64_t num_groups,
+                                    uint8_t *q_row, int64_t ld_qrow, uint8_t *s_row,
+                                    uint8_t *q_col, int64_t ld_qcol, uint8_t *s_col, void *stream);
+mxfp8_status mxfp8_swiglu_fwd_grouped(const uint16_t *gate, const uint16_t *up, int64_t ld_in,
+                                      int64_t M, int64_t N, int mode, int act,
+                                      const int32_t *group_end, int64_t num_groups,
+                                      uint8_t *q_row, int64_t ld_qrow, uint8_t *s_row,
+                                      uint8_t *q_col, int64_t ld_qcol, uint8_t *s_col, void *stream);
+mxfp8_status mxfp8_swiglu_bwd_grouped(const uint16_t *dh, int64_t ld_dh,
+                                      const uint16_t *gate, const uint16_t *up, int64_t ld_in,
+                                      int64_t M, int64_t N, int mode, int act,
+                                      const int32_t *group_end, int64_t num_groups,
+                                      uint8_t *dg_row, uint8_t *du_row, int64_t ld_qrow,
+                                      uint8_t *dg_srow, uint8_t *du_srow,
+                                      uint8_t *dg_col, uint8_t *du_col, int64_t ld_qcol,
+                                      uint8_t *dg_scol, uint8_t *du_scol, void *stream);
+
+/*
  * Allocation-free forward, for callers that cannot call cudaMalloc at all:
  * code that must live inside a host framework's fixed device-memory arena,
  * or that runs where allocation is forbidden.  (The pages have no
@@ -233,9 +295,10 @@ mxfp8_status mxfp8_geglu_bwd(const uint16_t *dh, int64_t ld_dh, const uint16_t *
  * Sticky device-side status of the current device.  Kernels never trap: a
  * pipeline wait that exceeds its limit (about a second) makes the kernel set
  * a flag bit and return.  flags: bit 0 consumer wait, bit 1 producer wait,
- * bit 2 drain wait, bit 3 self-test wait.  fallbacks: number of SwiGLU or GEGLU
- * elements the fused kernels recomputed exactly (values near a scale
- * boundary, gates outside the fast range, huge or non-finite blocks).
+ * bit 2 drain wait, bit 3 self-test wait, bit 4 invalid group ends.
+ * fallbacks: number of SwiGLU or GEGLU elements the fused kernels
+ * recomputed exactly (values near a scale boundary, gates outside the fast
+ * range, huge or non-finite blocks).
  * Synchronizes `stream`; with reset != 0 clears both afterwards.
  * Either output pointer (host memory) may be NULL.
  */

@@ -248,6 +248,121 @@ def quant_3d_colwise(x: torch.Tensor, q: Optional[torch.Tensor] = None,
     return q, s
 
 
+def grouped_scale_bytes(M: int, N: int, num_groups: int):
+    """(row-scale bytes, column-scale bytes) of one cast with per-group
+    blocked scales (M-groups rows, K-groups columns) for M rows in
+    ``num_groups`` token groups."""
+    t = -(-M // 128) + num_groups
+    return t * 128 * (-(-N // 128) * 4), -(-N // 128) * 128 * t * 4
+
+
+def _groups(group_end: torch.Tensor):
+    if group_end.dtype != torch.int32 or group_end.dim() != 1 or not group_end.is_contiguous():
+        raise ValueError("group_end must be a contiguous 1-D int32 tensor of cumulative end rows")
+    return group_end.data_ptr(), group_end.numel()
+
+
+def _act_id(act: str) -> int:
+    if act not in ("silu", "gelu"):
+        raise ValueError("act must be 'silu' or 'gelu'")
+    return capi.ACT_GELU if act == "gelu" else capi.ACT_SILU
+
+
+def _alloc_grouped(M, N, mode, G, device, n_out=1):
+    rb, cb = grouped_scale_bytes(M, N, G)
+    shape = (lambda b: (n_out, b)) if n_out > 1 else (lambda b: (b,))
+    o = {}
+    if mode & MXFP8_ROWWISE:
+        o["q_row"] = torch.empty((M, n_out * N), dtype=torch.uint8, device=device)
+        o["s_row"] = torch.zeros(shape(rb), dtype=torch.uint8, device=device)
+    if mode & MXFP8_COLWISE:
+        o["q_col"] = torch.empty((n_out * N, M), dtype=torch.uint8, device=device)
+        o["s_col"] = torch.zeros(shape(cb), dtype=torch.uint8, device=device)
+    return o
+
+
+def quant_2d_grouped(x: torch.Tensor, group_end: torch.Tensor, mode: int = MXFP8_BOTH,
+                     stream=None) -> MXFP8Cast:
+    """MXFP8 cast of a bf16 (M, N) tensor whose rows form token groups
+    (``group_end``: int32 device tensor of cumulative end rows), scales in the
+    per-group blocked layouts (flat, zero-filled buffers)."""
+    _check_bf16_2d(x, "x")
+    M, N = x.shape
+    gp, G = _groups(group_end)
+    o = MXFP8Cast(**_alloc_grouped(M, N, mode, G, x.device))
+    check(capi.mxfp8_quant_2d_grouped(x.data_ptr(), x.stride(0), M, N, mode, gp, G,
+                                      _ptr(o.q_row), _ld(o.q_row), _ptr(o.s_row),
+                                      _ptr(o.q_col), _ld(o.q_col), _ptr(o.s_col), _stream(stream)),
+          "mxfp8_quant_2d_grouped")
+    return o
+
+
+def swiglu_fwd_grouped(gate: torch.Tensor, up: torch.Tensor, group_end: torch.Tensor,
+                       mode: int = MXFP8_BOTH, act: str = "silu", stream=None) -> MXFP8Cast:
+    """Fused gated activation + MXFP8 cast with per-group blocked scales."""
+    _check_bf16_2d(gate, "gate")
+    _check_bf16_2d(up, "up")
+    if gate.shape != up.shape or gate.stride() != up.stride():
+        raise ValueError("gate and up must have the same shape and strides")
+    M, N = gate.shape
+    gp, G = _groups(group_end)
+    o = MXFP8Cast(**_alloc_grouped(M, N, mode, G, gate.device))
+    check(capi.mxfp8_swiglu_fwd_grouped(gate.data_ptr(), up.data_ptr(), gate.stride(0), M, N, mode,
+                                        _act_id(act), gp, G, _ptr(o.q_row), _ld(o.q_row), _ptr(o.s_row),
+                                        _ptr(o.q_col), _ld(o.q_col), _ptr(o.s_col), _stream(stream)),
+          "mxfp8_swiglu_fwd_grouped")
+    return o
+
+
+def swiglu_bwd_grouped(dh: torch.Tensor, gate: torch.Tensor, up: torch.Tensor, group_end: torch.Tensor,
+                       mode: int = MXFP8_BOTH, act: str = "silu", stream=None) -> SwiGLUGrads:
+    """Fused gated-activation backward + MXFP8 cast into packed [dGate | dUp]
+    data, one per-group blocked scale buffer per gradient."""
+    for t, nm in ((dh, "dh"), (gate, "gate"), (up, "up")):
+        _check_bf16_2d(t, nm)
+    if gate.shape != up.shape or gate.stride() != up.stride() or dh.shape != gate.shape:
+        raise ValueError("dh, gate and up must have the same shape (gate/up the same strides)")
+    M, N = gate.shape
+    gp, G = _groups(group_end)
+    o = SwiGLUGrads(blocked=True, **_alloc_grouped(M, N, mode, G, gate.device, n_out=2))
+    qr = _ptr(o.q_row)
+    qc = _ptr(o.q_col)
+    ld_qcol = _ld(o.q_col)
+    check(capi.mxfp8_swiglu_bwd_grouped(
+        dh.data_ptr(), dh.stride(0), gate.data_ptr(), up.data_ptr(), gate.stride(0), M, N, mode,
+        _act_id(act), gp, G,
+        qr, None if qr is None else qr + N, _ld(o.q_row),
+        _ptr(None if o.s_row is None else o.s_row[0]), _ptr(None if o.s_row is None else o.s_row[1]),
+        qc, None if qc is None else qc + N * ld_qcol, ld_qcol,
+        _ptr(None if o.s_col is None else o.s_col[0]), _ptr(None if o.s_col is None else o.s_col[1]),
+        _stream(stream)), "mxfp8_swiglu_bwd_grouped")
+    return o
+
+
+def quant_3d(x: torch.Tensor, mode: int = MXFP8_BOTH, stream=None) -> MXFP8Cast:
+    """(E, N, K) bf16 expert weights -> rowwise q_row (E, N, K) + s_row
+    (E, N, K/32) and/or colwise q_col (E, K, N) [per-expert column-major] +
+    s_col (E, N/32, K); with MXFP8_BLOCKED_SCALES each expert's scales as one
+    blocked matrix, flat per expert: s_row (E, bytes), s_col (E, bytes)."""
+    if x.dtype != torch.bfloat16 or x.dim() != 3 or not x.is_contiguous() or not x.is_cuda:
+        raise ValueError("x must be a contiguous (E, N, K) bf16 CUDA tensor")
+    E, N, K = x.shape
+    blocked = bool(mode & MXFP8_BLOCKED_SCALES)
+    o = MXFP8Cast()
+    dev = x.device
+    if mode & MXFP8_ROWWISE:
+        o.q_row = torch.empty((E, N, K), dtype=torch.uint8, device=dev)
+        o.s_row = (torch.zeros((E, blocked_bytes(N, K // 32)), dtype=torch.uint8, device=dev) if blocked
+                   else torch.empty((E, N, K // 32), dtype=torch.uint8, device=dev))
+    if mode & MXFP8_COLWISE:
+        o.q_col = torch.empty((E, K, N), dtype=torch.uint8, device=dev)
+        o.s_col = (torch.zeros((E, blocked_bytes(K, N // 32)), dtype=torch.uint8, device=dev) if blocked
+                   else torch.empty((E, N // 32, K), dtype=torch.uint8, device=dev))
+    check(capi.mxfp8_quant_3d(x.data_ptr(), E, N, K, mode, _ptr(o.q_row), _ptr(o.s_row),
+                              _ptr(o.q_col), _ptr(o.s_col), _stream(stream)), "mxfp8_quant_3d")
+    return o
+
+
 def device_status(reset: bool = False, stream=None):
     """(flags, fallbacks) of the current device; synchronizes the stream."""
     st, flags, n = capi.mxfp8_device_status(reset, _stream(stream))

@@ -17,6 +17,7 @@ MXFP8_ROWWISE = 1
 MXFP8_COLWISE = 2
 MXFP8_BOTH = 3
 MXFP8_BLOCKED_SCALES = 8   # flag: scales in the blocked 128 x 4 tile layout
+ACT_SILU, ACT_GELU = 0, 1  # the gated activation of the *_grouped fused calls
 
 STATUS_NAMES = {
     0: "MXFP8_OK", 1: "MXFP8_ERR_NULL", 2: "MXFP8_ERR_SHAPE", 3: "MXFP8_ERR_ALIGN",
@@ -52,6 +53,14 @@ SIGNATURES = {
                                _vp, _vp, _i64, _vp, _vp, _i64,
                                _vp, _vp, _i64, _vp, _vp, _i64, _vp]),
     "mxfp8_selftest_activation_gelu": (_int, [_vp, _vp]),
+    "mxfp8_quant_3d": (_int, [_vp, _i64, _i64, _i64, _int, _vp, _vp, _vp, _vp, _vp]),
+    "mxfp8_quant_2d_grouped": (_int, [_vp, _i64, _i64, _i64, _int, _vp, _i64,
+                                      _vp, _i64, _vp, _vp, _i64, _vp, _vp]),
+    "mxfp8_swiglu_fwd_grouped": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _int, _vp, _i64,
+                                        _vp, _i64, _vp, _vp, _i64, _vp, _vp]),
+    "mxfp8_swiglu_bwd_grouped": (_int, [_vp, _i64, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp, _i64,
+                                        _vp, _vp, _i64, _vp, _vp,
+                                        _vp, _vp, _i64, _vp, _vp, _vp]),
 }
 
 
@@ -166,3 +175,26 @@ def mxfp8_geglu_bwd(dh, ld_dh, gate, up, ld_in, M, N, mode,
 def mxfp8_selftest_activation_gelu(out, stream) -> int:
     return _lib.mxfp8_selftest_activation_gelu(out, stream)
 
+
+def mxfp8_quant_3d(x, E, N, K, mode, q_row, s_row, q_col, s_col, stream) -> int:
+    return _lib.mxfp8_quant_3d(x, E, N, K, mode, q_row, s_row, q_col, s_col, stream)
+
+
+def mxfp8_quant_2d_grouped(x, ld_x, M, N, mode, group_end, num_groups, q_row, ld_qrow, s_row,
+                           q_col, ld_qcol, s_col, stream) -> int:
+    return _lib.mxfp8_quant_2d_grouped(x, ld_x, M, N, mode, group_end, num_groups, q_row, ld_qrow, s_row,
+                                       q_col, ld_qcol, s_col, stream)
+
+
+def mxfp8_swiglu_fwd_grouped(gate, up, ld_in, M, N, mode, act, group_end, num_groups,
+                             q_row, ld_qrow, s_row, q_col, ld_qcol, s_col, stream) -> int:
+    return _lib.mxfp8_swiglu_fwd_grouped(gate, up, ld_in, M, N, mode, act, group_end, num_groups,
+                                         q_row, ld_qrow, s_row, q_col, ld_qcol, s_col, stream)
+
+
+def mxfp8_swiglu_bwd_grouped(dh, ld_dh, gate, up, ld_in, M, N, mode, act, group_end, num_groups,
+                             dg_row, du_row, ld_qrow, dg_srow, du_srow,
+                             dg_col, du_col, ld_qcol, dg_scol, du_scol, stream) -> int:
+    return _lib.mxfp8_swiglu_bwd_grouped(dh, ld_dh, gate, up, ld_in, M, N, mode, act, group_end, num_groups,
+                                         dg_row, du_row, ld_qrow, dg_srow, du_srow,
+                                         dg_col, du_col, ld_qcol, dg_scol, du_scol, stream)

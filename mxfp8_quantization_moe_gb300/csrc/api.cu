@@ -256,11 +256,32 @@ struct Spec {
     int64_t ld_h;
     bool with_h;
     int act;              // mx::kSilu / kGelu (the fused ops)
+    const int32_t *group_end;   // per-group blocked scales: token groups' end rows (device)
+    int64_t num_groups;
+    bool per_expert;      // 3D with blocked scales: one blocked matrix per expert
 };
 
 // Bytes of a scale matrix of R rows and C columns in the blocked layout
 // (padded to multiples of 128 rows and 4 columns).
 int64_t blocked_bytes(int64_t R, int64_t C) { return (R + 127) / 128 * 128 * ((C + 3) / 4 * 4); }
+
+// Bytes of the row- and column-scale buffers in the blocked layouts: plain,
+// per token group (M-groups / K-groups: (ceil(M/128) + G) 128-row tiles of
+// the row scales, (ceil(M/128) + G) 4-column tiles of the column scales) or
+// per expert (3D, group_rows rows an expert).
+int64_t row_scale_bytes(const Spec &s)
+{
+    if (s.group_end) return ((s.M + 127) / 128 + s.num_groups) * 128 * ((s.N / 32 + 3) / 4 * 4);
+    if (s.per_expert) return s.M / s.group_rows * blocked_bytes(s.group_rows, s.N / 32);
+    return blocked_bytes(s.M, s.N / 32);
+}
+
+int64_t col_scale_bytes(const Spec &s)
+{
+    if (s.group_end) return (s.N + 127) / 128 * 128 * (((s.M + 127) / 128 + s.num_groups) * 4);
+    if (s.per_expert) return s.M / s.group_rows * blocked_bytes(s.N, s.group_rows / 32);
+    return blocked_bytes(s.N, s.M / 32);
+}
 
 mxfp8_status validate(const Spec &s)
 {
@@ -268,11 +289,19 @@ mxfp8_status validate(const Spec &s)
     const int nout = s.op == mx::kBwd ? 2 : 1;
     if ((s.mode & ~(3 | MXFP8_BLOCKED_SCALES)) != 0 || (s.mode & 3) == 0) return MXFP8_ERR_MODE;
     const bool blocked = (s.mode & MXFP8_BLOCKED_SCALES) != 0;
-    if (blocked && s.group_stride != 0) return MXFP8_ERR_MODE;   // 2D only
+    if (blocked && s.group_stride != 0 && !s.per_expert) return MXFP8_ERR_MODE;
+    if (s.act != mx::kSilu && s.act != mx::kGelu) return MXFP8_ERR_MODE;
     if (s.M < 0 || s.N < 0) return MXFP8_ERR_SHAPE;
+    if (s.group_end || s.num_groups != 0) {          // per token group
+        if (s.num_groups < 1 || s.num_groups > mx::kMaxGroups) return MXFP8_ERR_SHAPE;
+        if (!s.group_end) return MXFP8_ERR_NULL;
+        if ((reinterpret_cast<uintptr_t>(s.group_end) & 3u) != 0) return MXFP8_ERR_ALIGN;
+        if (s.M > 0x7FFFFFFFLL - 128 * (mx::kMaxGroups + 1)) return MXFP8_ERR_SHAPE;   // 32-bit shifts
+    }
     if (s.M == 0 || s.N == 0) return MXFP8_OK;
     if (s.M > kMaxDim || s.N > kMaxDim) return MXFP8_ERR_SHAPE;
     const bool row = s.mode & 1, col = s.mode & 2;
+    if (s.per_expert && blocked && s.group_rows % 32 != 0) return MXFP8_ERR_SHAPE;
     if (row && s.N % 32 != 0) return MXFP8_ERR_SHAPE;
     if (col && s.M % 32 != 0) return MXFP8_ERR_SHAPE;
     for (int i = 0; i < nin; ++i) {
@@ -323,7 +352,7 @@ mxfp8_status validate(const Spec &s)
         if (row) {
             outs[n_outs++] = region(s.q_row[o], s.M, s.N, s.ld_qrow, 1);
             if (blocked) {
-                const int64_t b = blocked_bytes(s.M, s.N / 32);
+                const int64_t b = row_scale_bytes(s);
                 outs[n_outs++] = region(s.s_row[o], 1, b, b, 1);
             } else {
                 outs[n_outs++] = region(s.s_row[o], s.M, s.N / 32, s.ld_srow, 1);
@@ -337,16 +366,18 @@ mxfp8_status validate(const Spec &s)
                 outs[n_outs++] = region(s.q_col[o], E * s.N, s.group_rows, s.ld_qcol, 1);
             }
             if (blocked) {
-                const int64_t b = blocked_bytes(s.N, s.M / 32);
+                const int64_t b = col_scale_bytes(s);
                 outs[n_outs++] = region(s.s_col[o], 1, b, b, 1);
             } else {
                 outs[n_outs++] = region(s.s_col[o], s.M / 32, s.N, s.ld_scol, 1);
             }
         }
     }
+    const Region groups = region(s.group_end, 1, 4 * s.num_groups, 4 * s.num_groups, 1);
     for (int a = 0; a < n_outs; ++a) {
         for (int i = 0; i < nin; ++i)
             if (regions_overlap(outs[a], ins[i])) return MXFP8_ERR_OVERLAP;
+        if (s.group_end && regions_overlap(outs[a], groups)) return MXFP8_ERR_OVERLAP;
         for (int b = a + 1; b < n_outs; ++b)
             if (regions_overlap(outs[a], outs[b])) return MXFP8_ERR_OVERLAP;
     }
@@ -399,6 +430,17 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     a.wide_h = s.with_h && (reinterpret_cast<uintptr_t>(s.h) & 31u) == 0 && (s.ld_h * 2) % 32 == 0;
     a.srow_tiles_c = (s.N / 32 + 3) / 4;
     a.scol_tiles_c = (s.M / 32 + 3) / 4;
+    if (a.blocked && s.group_end) {           // M-groups row scales, K-groups column scales
+        a.group_end = s.group_end;
+        a.num_groups = static_cast<int>(s.num_groups);
+        a.scol_tiles_c = (s.M + 127) / 128 + s.num_groups;
+    } else if (a.blocked && s.per_expert) {   // one blocked matrix per expert
+        a.uni_blocks = s.group_rows / 32;
+        a.uni_r = (s.group_rows + 127) / 128 * 128 - s.group_rows;
+        a.uni_crow = (s.N + 127) / 128 * 128;
+        a.uni_c = -(s.group_rows / 32);
+        a.scol_tiles_c = (s.group_rows / 32 + 3) / 4;
+    }
     // whole 32-byte output blocks can go out as single 256-bit stores when
     // every block start is 32-byte aligned
     a.wide_row = (s.ld_qrow % 32) == 0;
@@ -640,6 +682,108 @@ mxfp8_status mxfp8_quant_3d_colwise(const uint16_t *x, int64_t E, int64_t N, int
     sp.group_rows = N;
     sp.group_stride = slab;
     return run(sp, stream);
+}
+
+mxfp8_status mxfp8_quant_3d(const uint16_t *x, int64_t E, int64_t N, int64_t K, int mode, uint8_t *q_row,
+                            uint8_t *s_row, uint8_t *q_col, uint8_t *s_col, void *stream)
+{
+    if ((mode & ~(3 | MXFP8_BLOCKED_SCALES)) != 0 || (mode & 3) == 0) return MXFP8_ERR_MODE;
+    if (E < 0 || N < 0 || K < 0) return MXFP8_ERR_SHAPE;
+    if (E == 0 || N == 0 || K == 0) return MXFP8_OK;
+    if ((mode & MXFP8_COLWISE) && N % 32 != 0) return MXFP8_ERR_SHAPE;
+    int64_t rows;
+    if (!mul_ok(E, N, &rows) || rows > kMaxDim || K > kMaxDim) return MXFP8_ERR_SHAPE;
+    if (K % 8 != 0) return MXFP8_ERR_ALIGN;
+    int64_t slab;
+    if (!mul_ok(N, K, &slab)) return MXFP8_ERR_SHAPE;
+    Spec sp = blank(mx::kQuant, mode, rows, K);
+    sp.in[0] = x;
+    sp.ld_in[0] = K;
+    sp.q_row[0] = q_row;  // (E, N, K) row-major: the (E * N, K) matrix
+    sp.s_row[0] = s_row;
+    sp.ld_qrow = K;
+    sp.ld_srow = K / 32;
+    sp.q_col[0] = q_col;
+    sp.s_col[0] = s_col;
+    sp.ld_qcol = N;
+    sp.ld_scol = K;
+    sp.group_rows = N;
+    sp.group_stride = (mode & MXFP8_COLWISE) ? slab : 0;
+    sp.per_expert = (mode & MXFP8_BLOCKED_SCALES) != 0;
+    if (sp.group_stride == 0 && sp.per_expert && N % 32 != 0) return MXFP8_ERR_SHAPE;
+    return run(sp, stream);
+}
+
+mxfp8_status mxfp8_quant_2d_grouped(const uint16_t *x, int64_t ld_x, int64_t M, int64_t N, int mode,
+                                    const int32_t *group_end, int64_t num_groups, uint8_t *q_row,
+                                    int64_t ld_qrow, uint8_t *s_row, uint8_t *q_col, int64_t ld_qcol,
+                                    uint8_t *s_col, void *stream)
+{
+    Spec s = blank(mx::kQuant, mode | MXFP8_BLOCKED_SCALES, M, N);
+    if ((mode & ~(3 | MXFP8_BLOCKED_SCALES)) != 0) return MXFP8_ERR_MODE;
+    s.in[0] = x;
+    s.ld_in[0] = ld_x;
+    s.q_row[0] = q_row;
+    s.s_row[0] = s_row;
+    s.q_col[0] = q_col;
+    s.s_col[0] = s_col;
+    s.ld_qrow = ld_qrow;
+    s.ld_qcol = ld_qcol;
+    s.group_end = group_end;
+    s.num_groups = num_groups;
+    return run(s, stream);
+}
+
+mxfp8_status mxfp8_swiglu_fwd_grouped(const uint16_t *gate, const uint16_t *up, int64_t ld_in, int64_t M,
+                                      int64_t N, int mode, int act, const int32_t *group_end,
+                                      int64_t num_groups, uint8_t *q_row, int64_t ld_qrow, uint8_t *s_row,
+                                      uint8_t *q_col, int64_t ld_qcol, uint8_t *s_col, void *stream)
+{
+    Spec s = blank(mx::kFwd, mode | MXFP8_BLOCKED_SCALES, M, N);
+    if ((mode & ~(3 | MXFP8_BLOCKED_SCALES)) != 0) return MXFP8_ERR_MODE;
+    s.act = act;
+    s.in[0] = gate;
+    s.in[1] = up;
+    s.ld_in[0] = s.ld_in[1] = ld_in;
+    s.q_row[0] = q_row;
+    s.s_row[0] = s_row;
+    s.q_col[0] = q_col;
+    s.s_col[0] = s_col;
+    s.ld_qrow = ld_qrow;
+    s.ld_qcol = ld_qcol;
+    s.group_end = group_end;
+    s.num_groups = num_groups;
+    return run(s, stream);
+}
+
+mxfp8_status mxfp8_swiglu_bwd_grouped(const uint16_t *dh, int64_t ld_dh, const uint16_t *gate,
+                                      const uint16_t *up, int64_t ld_in, int64_t M, int64_t N, int mode,
+                                      int act, const int32_t *group_end, int64_t num_groups,
+                                      uint8_t *dg_row, uint8_t *du_row, int64_t ld_qrow, uint8_t *dg_srow,
+                                      uint8_t *du_srow, uint8_t *dg_col, uint8_t *du_col, int64_t ld_qcol,
+                                      uint8_t *dg_scol, uint8_t *du_scol, void *stream)
+{
+    Spec s = blank(mx::kBwd, mode | MXFP8_BLOCKED_SCALES, M, N);
+    if ((mode & ~(3 | MXFP8_BLOCKED_SCALES)) != 0) return MXFP8_ERR_MODE;
+    s.act = act;
+    s.in[0] = dh;
+    s.in[1] = gate;
+    s.in[2] = up;
+    s.ld_in[0] = ld_dh;
+    s.ld_in[1] = s.ld_in[2] = ld_in;
+    s.q_row[0] = dg_row;
+    s.q_row[1] = du_row;
+    s.s_row[0] = dg_srow;
+    s.s_row[1] = du_srow;
+    s.q_col[0] = dg_col;
+    s.q_col[1] = du_col;
+    s.s_col[0] = dg_scol;
+    s.s_col[1] = du_scol;
+    s.ld_qrow = ld_qrow;
+    s.ld_qcol = ld_qcol;
+    s.group_end = group_end;
+    s.num_groups = num_groups;
+    return run(s, stream);
 }
 
 mxfp8_status mxfp8_device_status(uint32_t *flags, uint64_t *fallbacks, int reset, void *stream)

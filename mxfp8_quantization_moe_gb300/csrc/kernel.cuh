@@ -91,7 +91,8 @@ template <int OP, int TM, int STAGES, int G>
 constexpr size_t smem_bytes()
 {
     return 1024 + static_cast<size_t>(STAGES) * OpTraits<OP>::kIn * tile_bytes<TM>() +
-           static_cast<size_t>(STAGES + 1) * OpTraits<OP>::kOut * scale_group_bytes<TM, G>() + 2 * STAGES * 8;
+           static_cast<size_t>(STAGES + 1) * OpTraits<OP>::kOut * scale_group_bytes<TM, G>() + 2 * STAGES * 8 +
+           kGroupTableBytes;
 }
 
 // ------------------------------------------------------------ block values
@@ -367,23 +368,37 @@ __device__ __forceinline__ void store_codes(const uint32_t (&out)[2][16], const 
 // otherwise.
 template <int NOUT, int TM, int G>
 __device__ __forceinline__ void flush_row_scales(const KernelArgs &a, const uint8_t *gbuf, int64_t tr, int64_t ug,
-                                                 int gsize, int lane)
+                                                 int gsize, int lane, const int32_t *gtab)
 {
+    constexpr int kBlocks = TM / 32;
     const int64_t row0 = tr * TM;
     const int64_t blk0 = ug * 4 * G;
     const int64_t nblk = a.N >> 5;
     const bool whole = a.wide_srow != 0 && gsize == G && blk0 + 4 * G <= nblk;
-    for (int i = lane; i < TM; i += 32) {
+    // per-group layouts: lane j finds the row shift of the band's 32-row
+    // block j, handed round while the warp walks the blocks
+    const bool grouped = a.blocked && (a.group_end != nullptr || a.uni_blocks > 0);
+    int32_t mine = 0;
+    if (grouped) {
+        if (a.group_end != nullptr && gtab[3 * kMaxGroups] == 0) return;   // invalid group ends
+        const int64_t brow = row0 + 32 * lane;
+        if (lane < kBlocks && brow < a.M) mine = static_cast<int32_t>(group_shift(a, gtab, brow).r);
+    }
+#pragma unroll
+    for (int j = 0; j < kBlocks; ++j) {
+        const int32_t rsh = grouped ? __shfl_sync(0xFFFFFFFFu, mine, j) : 0;
+        const int i = lane + 32 * j;
         const int64_t row = row0 + i;
-        if (row >= a.M) break;
+        if (row >= a.M) continue;
 #pragma unroll
         for (int o = 0; o < NOUT; ++o) {
             const uint8_t *src = gbuf + o * scale_group_bytes<TM, G>() + 4 * G * i;
             if (a.blocked) {
                 // a tile's four blocks of a row are contiguous in the blocked
                 // layout (padding blocks of the last tile come out as 0)
+                const int64_t brow = row + rsh;
                 for (int t = 0; t < gsize; ++t)
-                    *reinterpret_cast<uint32_t *>(a.s_row[o] + blocked_offset(row, blk0 + 4 * t, a.srow_tiles_c)) =
+                    *reinterpret_cast<uint32_t *>(a.s_row[o] + blocked_offset(brow, blk0 + 4 * t, a.srow_tiles_c)) =
                         *reinterpret_cast<const uint32_t *>(src + 4 * t);
                 continue;
             }
@@ -470,6 +485,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
     const uint32_t smem_base = smem_u32(smem);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = smem_u32(bars + STAGES);
+    int32_t *gtab = reinterpret_cast<int32_t *>(bars + 2 * STAGES);   // per-group layouts
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -481,6 +497,13 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
         }
         fence_barrier_init();
         fence_proxy_async_smem();
+    }
+    if (a.blocked && a.group_end != nullptr && warp == 0) {
+        const bool ok = build_group_table(a.group_end, a.num_groups, a.M, gtab, lane);
+        if (lane == 0) {
+            gtab[3 * kMaxGroups] = ok ? 1 : 0;
+            if (!ok && blockIdx.x == 0) atomicOr(a.status, kStatusBadGroups);
+        }
     }
     __syncthreads();
 
@@ -535,7 +558,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
                 if constexpr (MODE & kRow) {
                     if (done.last_in_group())
                         flush_row_scales<NOUT, TM, G>(a, sbuf0 + done.gslot * NOUT * scale_group_bytes<TM, G>(), done.tr,
-                                                      done.ug, done.gsize, lane);
+                                                      done.ug, done.gsize, lane, gtab);
                 }
                 done.next();
             }
@@ -562,7 +585,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             if constexpr (MODE & kRow) {
                 if (done.last_in_group() || j + 1 == it)
                     flush_row_scales<NOUT, TM, G>(a, sbuf0 + done.gslot * NOUT * scale_group_bytes<TM, G>(), done.tr,
-                                                  done.ug, done.i + 1, lane);
+                                                  done.ug, done.i + 1, lane, gtab);
             }
             done.next();
         }
@@ -677,7 +700,16 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             for (int o = 0; o < NOUT; ++o) q[o] = a.q_col[o] + grp * a.group_stride + gcol * a.ld_qcol + rin;
             uint32_t b[2];
             store_codes<NOUT>(out, amax, q, live, a.wide_col != 0, b);
-            if (live) {
+            if (a.blocked && (a.group_end != nullptr || a.uni_blocks > 0)) {
+                // per-group layouts (the same shift for the whole warp)
+                const bool ok = a.group_end == nullptr || gtab[3 * kMaxGroups] != 0;
+                if (live && ok) {
+                    const GroupShift gs = group_shift(a, gtab, r0);
+                    const int64_t off = blocked_offset(gcol + gs.crow, (r0 >> 5) + gs.c, a.scol_tiles_c);
+#pragma unroll
+                    for (int o = 0; o < NOUT; ++o) a.s_col[o][off] = static_cast<uint8_t>(b[o]);
+                }
+            } else if (live) {
                 const int64_t off = a.blocked ? blocked_offset(gcol, r0 >> 5, a.scol_tiles_c) : (r0 >> 5) * a.ld_scol + gcol;
 #pragma unroll
                 for (int o = 0; o < NOUT; ++o) a.s_col[o][off] = static_cast<uint8_t>(b[o]);

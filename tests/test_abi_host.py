@@ -203,3 +203,55 @@ def test_python_binding_rejects_unknown_activation():
         mx.swiglu_fwd(g, g, 1, act="gelu", keep_h=True)
     with pytest.raises(ValueError):
         mx.swiglu_bwd(g, g, g, 1, act="tanh")
+
+
+GE = 0x70000000         # fake device address of a group-end vector
+
+
+def q2d_grouped(M=128, N=256, mode=3, ge=GE, G=2, s_row=S, s_col=SC):
+    return capi.mxfp8_quant_2d_grouped(X, N, M, N, mode, ge, G, Q, N, s_row, QC, M, s_col, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(ge=0), NULL),
+    (dict(G=0), SHAPE), (dict(G=257), SHAPE),
+    (dict(ge=GE + 2), ALIGN),
+    (dict(mode=4), MODE),
+    (dict(s_row=S + 2), ALIGN),                  # blocked row scales: 4-byte aligned
+    (dict(ge=S + 64), OVERLAP),                  # group ends inside the row-scale buffer
+    (dict(M=0), OK),                             # empty
+])
+def test_grouped_argument_errors(kw, status):
+    assert q2d_grouped(**kw) == status
+
+
+def test_grouped_scale_buffer_sizes_enter_the_overlap_check():
+    # M = 128, N = 256, G = 2: row scales (1 + 2) * 128 rows * 8 bytes = 3072,
+    # column scales 256 rows * (1 + 2) * 4 = 3072 bytes
+    assert q2d_grouped(s_col=S + 3072 - 16) == OVERLAP
+    if NO_GPU:
+        assert q2d_grouped(s_col=S + 3072) == DEVICE
+
+
+def test_grouped_fused_entry_points_check_the_activation():
+    f = capi.mxfp8_swiglu_fwd_grouped
+    assert f(X, X + 256, 512, 64, 256, 1, 2, GE, 1, Q, 256, S, None, 0, None, None) == MODE
+    b = capi.mxfp8_swiglu_bwd_grouped
+    assert b(X + 0x100000, 256, X, X + 256, 512, 64, 256, 1, 5, GE, 1, Q, Q + 256, 512, S, S + 4096,
+             None, None, 0, None, None, None) == MODE
+    if NO_GPU:
+        assert f(X, X + 256, 512, 64, 256, 1, 1, GE, 1, Q, 256, S, None, 0, None, None) == DEVICE
+
+
+def test_quant_3d_argument_errors():
+    f = capi.mxfp8_quant_3d
+    assert f(X, 2, 64, 64, 0, Q, S, QC, SC, None) == MODE
+    assert f(X, 2, 64, 64, 16 | 1, Q, S, QC, SC, None) == MODE
+    assert f(X, 2, 48, 64, 2, Q, S, QC, SC, None) == SHAPE           # colwise: N % 32
+    assert f(X, 2, 48, 64, 1 | 8, Q, S, QC, SC, None) == SHAPE       # blocked: N % 32
+    assert f(X, 2, 64, 48, 1, Q, S, QC, SC, None) == SHAPE           # rowwise: K % 32
+    assert f(X, 2, 64, 60, 2, Q, S, QC, SC, None) == ALIGN           # K % 8
+    assert f(X, 0, 64, 64, 3, Q, S, QC, SC, None) == OK
+    assert f(X, 2, 64, 64, 1, 0, S, QC, SC, None) == NULL
+    if NO_GPU:
+        assert f(X, 2, 48, 64, 1, Q, S, QC, SC, None) == DEVICE      # rowwise plain: any N
