@@ -412,13 +412,16 @@ def run_cell(args):
         if kind == "quant" and ends is not None:
             k = 2 if mode & 3 == 3 else 1
             nbytes = 2 * M * N + k * (M * N + M * N // 32)
-            fn = lambda: mx.quant_2d_grouped(gate, ends, mode & 3)
+            out = mx.quant_2d_grouped(gate, ends, mode & 3)
+            fn = lambda: mx.quant_2d_grouped(gate, ends, mode & 3, out=out)
         elif kind == "fwd" and ends is not None:
             nbytes = cell_bytes("fwd", mode & 3, M, N)
-            fn = lambda: mx.swiglu_fwd_grouped(gate, up, ends, mode & 3, act=args.act)
+            out = mx.swiglu_fwd_grouped(gate, up, ends, mode & 3, act=args.act)
+            fn = lambda: mx.swiglu_fwd_grouped(gate, up, ends, mode & 3, act=args.act, out=out)
         elif ends is not None:
             nbytes = cell_bytes("bwd", mode & 3, M, N)
-            fn = lambda: mx.swiglu_bwd_grouped(dh, gate, up, ends, mode & 3, act=args.act)
+            out = mx.swiglu_bwd_grouped(dh, gate, up, ends, mode & 3, act=args.act)
+            fn = lambda: mx.swiglu_bwd_grouped(dh, gate, up, ends, mode & 3, act=args.act, out=out)
         elif kind == "quant":
             out = mx._alloc(M, N, mode, gate.device)
             k = 2 if mode & 3 == 3 else 1

@@ -282,14 +282,14 @@ def _alloc_grouped(M, N, mode, G, device, n_out=1):
 
 
 def quant_2d_grouped(x: torch.Tensor, group_end: torch.Tensor, mode: int = MXFP8_BOTH,
-                     stream=None) -> MXFP8Cast:
+                     out: Optional[MXFP8Cast] = None, stream=None) -> MXFP8Cast:
     """MXFP8 cast of a bf16 (M, N) tensor whose rows form token groups
     (``group_end``: int32 device tensor of cumulative end rows), scales in the
     per-group blocked layouts (flat, zero-filled buffers)."""
     _check_bf16_2d(x, "x")
     M, N = x.shape
     gp, G = _groups(group_end)
-    o = MXFP8Cast(**_alloc_grouped(M, N, mode, G, x.device))
+    o = out if out is not None else MXFP8Cast(**_alloc_grouped(M, N, mode, G, x.device))
     check(capi.mxfp8_quant_2d_grouped(x.data_ptr(), x.stride(0), M, N, mode, gp, G,
                                       _ptr(o.q_row), _ld(o.q_row), _ptr(o.s_row),
                                       _ptr(o.q_col), _ld(o.q_col), _ptr(o.s_col), _stream(stream)),
@@ -298,7 +298,8 @@ def quant_2d_grouped(x: torch.Tensor, group_end: torch.Tensor, mode: int = MXFP8
 
 
 def swiglu_fwd_grouped(gate: torch.Tensor, up: torch.Tensor, group_end: torch.Tensor,
-                       mode: int = MXFP8_BOTH, act: str = "silu", stream=None) -> MXFP8Cast:
+                       mode: int = MXFP8_BOTH, act: str = "silu", out: Optional[MXFP8Cast] = None,
+                       stream=None) -> MXFP8Cast:
     """Fused gated activation + MXFP8 cast with per-group blocked scales."""
     _check_bf16_2d(gate, "gate")
     _check_bf16_2d(up, "up")
@@ -306,7 +307,7 @@ def swiglu_fwd_grouped(gate: torch.Tensor, up: torch.Tensor, group_end: torch.Te
         raise ValueError("gate and up must have the same shape and strides")
     M, N = gate.shape
     gp, G = _groups(group_end)
-    o = MXFP8Cast(**_alloc_grouped(M, N, mode, G, gate.device))
+    o = out if out is not None else MXFP8Cast(**_alloc_grouped(M, N, mode, G, gate.device))
     check(capi.mxfp8_swiglu_fwd_grouped(gate.data_ptr(), up.data_ptr(), gate.stride(0), M, N, mode,
                                         _act_id(act), gp, G, _ptr(o.q_row), _ld(o.q_row), _ptr(o.s_row),
                                         _ptr(o.q_col), _ld(o.q_col), _ptr(o.s_col), _stream(stream)),
@@ -315,7 +316,8 @@ def swiglu_fwd_grouped(gate: torch.Tensor, up: torch.Tensor, group_end: torch.Te
 
 
 def swiglu_bwd_grouped(dh: torch.Tensor, gate: torch.Tensor, up: torch.Tensor, group_end: torch.Tensor,
-                       mode: int = MXFP8_BOTH, act: str = "silu", stream=None) -> SwiGLUGrads:
+                       mode: int = MXFP8_BOTH, act: str = "silu", out: Optional[SwiGLUGrads] = None,
+                       stream=None) -> SwiGLUGrads:
     """Fused gated-activation backward + MXFP8 cast into packed [dGate | dUp]
     data, one per-group blocked scale buffer per gradient."""
     for t, nm in ((dh, "dh"), (gate, "gate"), (up, "up")):
@@ -324,7 +326,7 @@ def swiglu_bwd_grouped(dh: torch.Tensor, gate: torch.Tensor, up: torch.Tensor, g
         raise ValueError("dh, gate and up must have the same shape (gate/up the same strides)")
     M, N = gate.shape
     gp, G = _groups(group_end)
-    o = SwiGLUGrads(blocked=True, **_alloc_grouped(M, N, mode, G, gate.device, n_out=2))
+    o = out if out is not None else SwiGLUGrads(blocked=True, **_alloc_grouped(M, N, mode, G, gate.device, n_out=2))
     qr = _ptr(o.q_row)
     qc = _ptr(o.q_col)
     ld_qcol = _ld(o.q_col)

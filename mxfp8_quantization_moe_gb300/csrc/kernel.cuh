@@ -361,6 +361,33 @@ __device__ __forceinline__ void store_codes(const uint32_t (&out)[2][16], const 
     }
 }
 
+// flush_row_scales (below) in the per-group blocked layouts: lane j finds the
+// row shift of the band's 32-row block j, handed round while the warp walks
+// the blocks.  Writes nothing if the group ends were found invalid.
+template <int NOUT, int TM, int G>
+__device__ __forceinline__ void flush_row_scales_grouped(const KernelArgs &a, const uint8_t *gbuf, int64_t row0,
+                                                      int64_t blk0, int gsize, int lane, const int32_t *gtab)
+{
+    constexpr int kBlocks = TM / 32;
+    if (a.group_end != nullptr && gtab[3 * kMaxGroups] == 0) return;
+    const int64_t brow0 = row0 + 32 * lane;
+    const int32_t mine = (lane < kBlocks && brow0 < a.M) ? static_cast<int32_t>(group_shift(a, gtab, brow0).r) : 0;
+#pragma unroll
+    for (int j = 0; j < kBlocks; ++j) {
+        const int32_t rsh = __shfl_sync(0xFFFFFFFFu, mine, j);
+        const int i = lane + 32 * j;
+        const int64_t row = row0 + i;
+        if (row >= a.M) continue;
+#pragma unroll
+        for (int o = 0; o < NOUT; ++o) {
+            const uint8_t *src = gbuf + o * scale_group_bytes<TM, G>() + 4 * G * i;
+            for (int t = 0; t < gsize; ++t)
+                *reinterpret_cast<uint32_t *>(a.s_row[o] + blocked_offset(row + rsh, blk0 + 4 * t, a.srow_tiles_c)) =
+                    *reinterpret_cast<const uint32_t *>(src + 4 * t);
+        }
+    }
+}
+
 // Row scales of one finished group of column tiles (tiles 0..gsize-1 of group
 // ug in row band tr), from its shared-memory buffer (4 G bytes a row) to s_row,
 // by the whole producer warp: one 4G-byte store per row where the group is
@@ -370,35 +397,25 @@ template <int NOUT, int TM, int G>
 __device__ __forceinline__ void flush_row_scales(const KernelArgs &a, const uint8_t *gbuf, int64_t tr, int64_t ug,
                                                  int gsize, int lane, const int32_t *gtab)
 {
-    constexpr int kBlocks = TM / 32;
     const int64_t row0 = tr * TM;
     const int64_t blk0 = ug * 4 * G;
     const int64_t nblk = a.N >> 5;
-    const bool whole = a.wide_srow != 0 && gsize == G && blk0 + 4 * G <= nblk;
-    // per-group layouts: lane j finds the row shift of the band's 32-row
-    // block j, handed round while the warp walks the blocks
-    const bool grouped = a.blocked && (a.group_end != nullptr || a.uni_blocks > 0);
-    int32_t mine = 0;
-    if (grouped) {
-        if (a.group_end != nullptr && gtab[3 * kMaxGroups] == 0) return;   // invalid group ends
-        const int64_t brow = row0 + 32 * lane;
-        if (lane < kBlocks && brow < a.M) mine = static_cast<int32_t>(group_shift(a, gtab, brow).r);
+    if (a.blocked && (a.group_end != nullptr || a.uni_blocks > 0)) {
+        flush_row_scales_grouped<NOUT, TM, G>(a, gbuf, row0, blk0, gsize, lane, gtab);
+        return;
     }
-#pragma unroll
-    for (int j = 0; j < kBlocks; ++j) {
-        const int32_t rsh = grouped ? __shfl_sync(0xFFFFFFFFu, mine, j) : 0;
-        const int i = lane + 32 * j;
+    const bool whole = a.wide_srow != 0 && gsize == G && blk0 + 4 * G <= nblk;
+    for (int i = lane; i < TM; i += 32) {
         const int64_t row = row0 + i;
-        if (row >= a.M) continue;
+        if (row >= a.M) break;
 #pragma unroll
         for (int o = 0; o < NOUT; ++o) {
             const uint8_t *src = gbuf + o * scale_group_bytes<TM, G>() + 4 * G * i;
             if (a.blocked) {
                 // a tile's four blocks of a row are contiguous in the blocked
                 // layout (padding blocks of the last tile come out as 0)
-                const int64_t brow = row + rsh;
                 for (int t = 0; t < gsize; ++t)
-                    *reinterpret_cast<uint32_t *>(a.s_row[o] + blocked_offset(brow, blk0 + 4 * t, a.srow_tiles_c)) =
+                    *reinterpret_cast<uint32_t *>(a.s_row[o] + blocked_offset(row, blk0 + 4 * t, a.srow_tiles_c)) =
                         *reinterpret_cast<const uint32_t *>(src + 4 * t);
                 continue;
             }
