@@ -435,6 +435,19 @@ __device__ __forceinline__ void flush_row_scales(const KernelArgs &a, const uint
     }
 }
 
+// A column-scale byte (two for the backward) in the per-group blocked
+// layouts; kept out of line, off the column pass's usual path.  Writes
+// nothing if the group ends were found invalid.
+static __device__ __noinline__ void store_col_scales_grouped(const KernelArgs &a, const int32_t *gtab, int64_t r0,
+                                                              int64_t gcol, int nout, uint32_t b0, uint32_t b1)
+{
+    if (a.group_end != nullptr && gtab[3 * kMaxGroups] == 0) return;
+    const GroupShift gs = group_shift(a, gtab, r0);
+    const int64_t off = blocked_offset(gcol + gs.crow, (r0 >> 5) + gs.c, a.scol_tiles_c);
+    a.s_col[0][off] = static_cast<uint8_t>(b0);
+    if (nout > 1) a.s_col[1][off] = static_cast<uint8_t>(b1);
+}
+
 // This CTA's tiles.  Column tiles are taken in groups of G consecutive ones
 // of a row band ("super-tiles" u = blockIdx.x, + gridDim.x, ...), tile by
 // tile; the walk keeps the row band tr, the group ug, the tile i within it,
@@ -502,7 +515,9 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
     const uint32_t smem_base = smem_u32(smem);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = smem_u32(bars + STAGES);
-    int32_t *gtab = reinterpret_cast<int32_t *>(bars + 2 * STAGES);   // per-group layouts
+    // per-group layouts: the last kGroupTableBytes, present only in launches
+    // that use them (grouped blocked scales)
+    int32_t *gtab = reinterpret_cast<int32_t *>(bars + 2 * STAGES);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -718,14 +733,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             uint32_t b[2];
             store_codes<NOUT>(out, amax, q, live, a.wide_col != 0, b);
             if (a.blocked && (a.group_end != nullptr || a.uni_blocks > 0)) {
-                // per-group layouts (the same shift for the whole warp)
-                const bool ok = a.group_end == nullptr || gtab[3 * kMaxGroups] != 0;
-                if (live && ok) {
-                    const GroupShift gs = group_shift(a, gtab, r0);
-                    const int64_t off = blocked_offset(gcol + gs.crow, (r0 >> 5) + gs.c, a.scol_tiles_c);
-#pragma unroll
-                    for (int o = 0; o < NOUT; ++o) a.s_col[o][off] = static_cast<uint8_t>(b[o]);
-                }
+                if (live) store_col_scales_grouped(a, gtab, r0, gcol, NOUT, b[0], b[1]);
             } else if (live) {
                 const int64_t off = a.blocked ? blocked_offset(gcol, r0 >> 5, a.scol_tiles_c) : (r0 >> 5) * a.ld_scol + gcol;
 #pragma unroll

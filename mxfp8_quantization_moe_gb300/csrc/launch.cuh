@@ -17,9 +17,12 @@ cudaError_t launch_tiles(const CUtensorMap (&maps)[3], const KernelArgs &a, int 
     constexpr int kStages = Tuning<OP, MODE>::kStages;
     constexpr int kCtas = Tuning<OP, MODE>::kCtas;
     constexpr int kGroup = Tuning<OP, MODE>::kGroup;
+    // the per-group table is reserved only for launches that use it
     constexpr size_t kSmem = smem_bytes<OP, kTM, kStages, kGroup>();
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
     static_assert(kCtas * (kSmem + 1024) <= 228 * 1024, "shared memory per SM");
+    const bool grouped = a.blocked && (a.group_end != nullptr || a.uni_blocks > 0);
+    const size_t smem = grouped ? kSmem : kSmem - kGroupTableBytes;
     auto kern = mxfp8_tile_kernel<OP, MODE, kTM, kStages, kCtas, kGroup, ACT>;
     static std::atomic<unsigned long long> attr_done{0};
     const unsigned long long bit = 1ull << (device & 63);
@@ -32,7 +35,7 @@ cudaError_t launch_tiles(const CUtensorMap (&maps)[3], const KernelArgs &a, int 
     void *args[] = {const_cast<CUtensorMap *>(&maps[0]), const_cast<CUtensorMap *>(&maps[1]),
                     const_cast<CUtensorMap *>(&maps[2]), const_cast<KernelArgs *>(&a)};
     return cudaLaunchKernel(reinterpret_cast<const void *>(kern), dim3(grid),
-                            dim3((warps_of<kTM>() + 1) * 32), args, kSmem, stream);
+                            dim3((warps_of<kTM>() + 1) * 32), args, smem, stream);
 }
 
 // tile rows, resident CTAs per SM and row-scale group of the instantiation
