@@ -21,7 +21,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIB_DIR, "libmxfp8.so")
 
-SOURCES = ["api.cu", "ops_quant.cu", "ops_fwd.cu", "ops_bwd.cu", "ops_fwd_gelu.cu", "ops_bwd_gelu.cu"]
+_OPS = ["ops_quant", "ops_fwd", "ops_bwd", "ops_fwd_gelu", "ops_bwd_gelu"]
+SOURCES = ["api.cu"] + [o + ".cu" for o in _OPS] + [o + "_grouped.cu" for o in _OPS]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE,
          "-Xcompiler", "-Wall"]

@@ -465,16 +465,29 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     const int64_t supers = ((s.M + tm - 1) / tm) * ((a.tiles_n + shape.group - 1) / shape.group);
     const int64_t slots = static_cast<int64_t>(d->sms) * shape.ctas_per_sm;
     const int grid = static_cast<int>(supers < slots ? supers : slots);
+    // per-group blocked scales run their own instantiations
+    const bool grouped = a.blocked && (a.group_end != nullptr || a.uni_blocks > 0);
     cudaError_t e;
     switch (s.op) {
-    case mx::kQuant: e = mx::launch_quant(mode, maps, a, grid, stream, dev); break;
+    case mx::kQuant:
+        e = grouped ? mx::launch_quant_grouped(mode, maps, a, grid, stream, dev)
+                    : mx::launch_quant(mode, maps, a, grid, stream, dev);
+        break;
     case mx::kFwd:
-        e = s.act == mx::kGelu ? mx::launch_fwd_gelu(mode, maps, a, grid, stream, dev)
-                               : mx::launch_fwd(mode, maps, a, grid, stream, dev);
+        if (s.act == mx::kGelu)
+            e = grouped ? mx::launch_fwd_gelu_grouped(mode, maps, a, grid, stream, dev)
+                        : mx::launch_fwd_gelu(mode, maps, a, grid, stream, dev);
+        else
+            e = grouped ? mx::launch_fwd_grouped(mode, maps, a, grid, stream, dev)
+                        : mx::launch_fwd(mode, maps, a, grid, stream, dev);
         break;
     default:
-        e = s.act == mx::kGelu ? mx::launch_bwd_gelu(mode, maps, a, grid, stream, dev)
-                               : mx::launch_bwd(mode, maps, a, grid, stream, dev);
+        if (s.act == mx::kGelu)
+            e = grouped ? mx::launch_bwd_gelu_grouped(mode, maps, a, grid, stream, dev)
+                        : mx::launch_bwd_gelu(mode, maps, a, grid, stream, dev);
+        else
+            e = grouped ? mx::launch_bwd_grouped(mode, maps, a, grid, stream, dev)
+                        : mx::launch_bwd(mode, maps, a, grid, stream, dev);
         break;
     }
     return e == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;

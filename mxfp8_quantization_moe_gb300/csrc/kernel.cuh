@@ -87,12 +87,12 @@ __host__ __device__ constexpr int scale_group_bytes() { return TM * 4 * G; }
 
 // shared memory: 1 KB alignment slack, the stages, the row-scale buffers
 // (a ring of STAGES + 1 groups, per output), the mbarriers
-template <int OP, int TM, int STAGES, int G>
+template <int OP, int TM, int STAGES, int G, bool GRP>
 constexpr size_t smem_bytes()
 {
     return 1024 + static_cast<size_t>(STAGES) * OpTraits<OP>::kIn * tile_bytes<TM>() +
            static_cast<size_t>(STAGES + 1) * OpTraits<OP>::kOut * scale_group_bytes<TM, G>() + 2 * STAGES * 8 +
-           kGroupTableBytes;
+           (GRP ? kGroupTableBytes : 0);
 }
 
 // ------------------------------------------------------------ block values
@@ -366,12 +366,14 @@ __device__ __forceinline__ void store_codes(const uint32_t (&out)[2][16], const 
 // the blocks.  Writes nothing if the group ends were found invalid.
 template <int NOUT, int TM, int G>
 __device__ __forceinline__ void flush_row_scales_grouped(const KernelArgs &a, const uint8_t *gbuf, int64_t row0,
-                                                      int64_t blk0, int gsize, int lane, const int32_t *gtab)
+                                                      int64_t blk0, int gsize, int lane, const int32_t *gtab,
+                                                      int &hint)
 {
     constexpr int kBlocks = TM / 32;
     if (a.group_end != nullptr && gtab[3 * kMaxGroups] == 0) return;
     const int64_t brow0 = row0 + 32 * lane;
-    const int32_t mine = (lane < kBlocks && brow0 < a.M) ? static_cast<int32_t>(group_shift(a, gtab, brow0).r) : 0;
+    const int32_t mine =
+        (lane < kBlocks && brow0 < a.M) ? static_cast<int32_t>(group_shift(a, gtab, brow0, hint).r) : 0;
 #pragma unroll
     for (int j = 0; j < kBlocks; ++j) {
         const int32_t rsh = __shfl_sync(0xFFFFFFFFu, mine, j);
@@ -393,15 +395,15 @@ __device__ __forceinline__ void flush_row_scales_grouped(const KernelArgs &a, co
 // by the whole producer warp: one 4G-byte store per row where the group is
 // whole and rows are aligned (`wide`), 4-byte stores or single bytes
 // otherwise.
-template <int NOUT, int TM, int G>
+template <int NOUT, int TM, int G, bool GRP>
 __device__ __forceinline__ void flush_row_scales(const KernelArgs &a, const uint8_t *gbuf, int64_t tr, int64_t ug,
-                                                 int gsize, int lane, const int32_t *gtab)
+                                                 int gsize, int lane, const int32_t *gtab, int &hint)
 {
     const int64_t row0 = tr * TM;
     const int64_t blk0 = ug * 4 * G;
     const int64_t nblk = a.N >> 5;
-    if (a.blocked && (a.group_end != nullptr || a.uni_blocks > 0)) {
-        flush_row_scales_grouped<NOUT, TM, G>(a, gbuf, row0, blk0, gsize, lane, gtab);
+    if constexpr (GRP) {
+        flush_row_scales_grouped<NOUT, TM, G>(a, gbuf, row0, blk0, gsize, lane, gtab, hint);
         return;
     }
     const bool whole = a.wide_srow != 0 && gsize == G && blk0 + 4 * G <= nblk;
@@ -433,19 +435,6 @@ __device__ __forceinline__ void flush_row_scales(const KernelArgs &a, const uint
             }
         }
     }
-}
-
-// A column-scale byte (two for the backward) in the per-group blocked
-// layouts; kept out of line, off the column pass's usual path.  Writes
-// nothing if the group ends were found invalid.
-static __device__ __noinline__ void store_col_scales_grouped(const KernelArgs &a, const int32_t *gtab, int64_t r0,
-                                                              int64_t gcol, int nout, uint32_t b0, uint32_t b1)
-{
-    if (a.group_end != nullptr && gtab[3 * kMaxGroups] == 0) return;
-    const GroupShift gs = group_shift(a, gtab, r0);
-    const int64_t off = blocked_offset(gcol + gs.crow, (r0 >> 5) + gs.c, a.scol_tiles_c);
-    a.s_col[0][off] = static_cast<uint8_t>(b0);
-    if (nout > 1) a.s_col[1][off] = static_cast<uint8_t>(b1);
 }
 
 // This CTA's tiles.  Column tiles are taken in groups of G consecutive ones
@@ -492,7 +481,7 @@ struct TileWalk {
 };
 
 // ------------------------------------------------------------------ kernel
-template <int OP, int MODE, int TM, int STAGES, int CTAS, int G, int ACT>
+template <int OP, int MODE, int TM, int STAGES, int CTAS, int G, int ACT, bool GRP>
 __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
     mxfp8_tile_kernel(const __grid_constant__ CUtensorMap tm0,
                       const __grid_constant__ CUtensorMap tm1,
@@ -515,8 +504,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
     const uint32_t smem_base = smem_u32(smem);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = smem_u32(bars + STAGES);
-    // per-group layouts: the last kGroupTableBytes, present only in launches
-    // that use them (grouped blocked scales)
+    // per-group layouts (GRP instantiations only): the group table
     int32_t *gtab = reinterpret_cast<int32_t *>(bars + 2 * STAGES);
 
     const int tid = threadIdx.x;
@@ -530,11 +518,13 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
         fence_barrier_init();
         fence_proxy_async_smem();
     }
-    if (a.blocked && a.group_end != nullptr && warp == 0) {
-        const bool ok = build_group_table(a.group_end, a.num_groups, a.M, gtab, lane);
-        if (lane == 0) {
-            gtab[3 * kMaxGroups] = ok ? 1 : 0;
-            if (!ok && blockIdx.x == 0) atomicOr(a.status, kStatusBadGroups);
+    if constexpr (GRP) {
+        if (a.group_end != nullptr && warp == 0) {
+            const bool ok = build_group_table(a.group_end, a.num_groups, a.M, gtab, lane);
+            if (lane == 0) {
+                gtab[3 * kMaxGroups] = ok ? 1 : 0;
+                if (!ok && blockIdx.x == 0) atomicOr(a.status, kStatusBadGroups);
+            }
         }
     }
     __syncthreads();
@@ -553,6 +543,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             if (NIN > 2) prefetch_tensormap(&tm2);
         }
         int it = 0;
+        int ghint = 0;     // group of this lane's last row-scale lookup
         bool failed = false;
         TileWalk<STAGES, G> done(tiles_n);   // the oldest tile not yet recycled
         for (TileWalk<STAGES, G> w(tiles_n); w.u < num_super; w.next(), ++it) {
@@ -589,8 +580,8 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
                 // group starting at tile it + 1 or later, loaded after this
                 if constexpr (MODE & kRow) {
                     if (done.last_in_group())
-                        flush_row_scales<NOUT, TM, G>(a, sbuf0 + done.gslot * NOUT * scale_group_bytes<TM, G>(), done.tr,
-                                                      done.ug, done.gsize, lane, gtab);
+                        flush_row_scales<NOUT, TM, G, GRP>(a, sbuf0 + done.gslot * NOUT * scale_group_bytes<TM, G>(), done.tr,
+                                                      done.ug, done.gsize, lane, gtab, ghint);
                 }
                 done.next();
             }
@@ -616,8 +607,8 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             }
             if constexpr (MODE & kRow) {
                 if (done.last_in_group() || j + 1 == it)
-                    flush_row_scales<NOUT, TM, G>(a, sbuf0 + done.gslot * NOUT * scale_group_bytes<TM, G>(), done.tr,
-                                                  done.ug, done.i + 1, lane, gtab);
+                    flush_row_scales<NOUT, TM, G, GRP>(a, sbuf0 + done.gslot * NOUT * scale_group_bytes<TM, G>(), done.tr,
+                                                  done.ug, done.i + 1, lane, gtab, ghint);
             }
             done.next();
         }
@@ -644,6 +635,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
 
     constexpr bool kSplit = (MODE == kBoth) && (OP != kQuant);  // values handed row -> col pass
     constexpr bool kWrites = kSplit || (MODE & kCol);           // generic writes into the stage
+    int chint = 0;   // group of this warp's last column-scale lookup
     for (TileWalk<STAGES, G> w(tiles_n); w.u < num_super; w.next()) {
         const int s = w.s;
         const bool fail = __any_sync(0xFFFFFFFFu, !mbar_wait_bounded(full0 + 8 * s, w.ph, a.wait_limit));
@@ -732,8 +724,15 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             for (int o = 0; o < NOUT; ++o) q[o] = a.q_col[o] + grp * a.group_stride + gcol * a.ld_qcol + rin;
             uint32_t b[2];
             store_codes<NOUT>(out, amax, q, live, a.wide_col != 0, b);
-            if (a.blocked && (a.group_end != nullptr || a.uni_blocks > 0)) {
-                if (live) store_col_scales_grouped(a, gtab, r0, gcol, NOUT, b[0], b[1]);
+            if constexpr (GRP) {
+                // per-group layouts (the same shift for the whole warp)
+                const bool ok = a.group_end == nullptr || gtab[3 * kMaxGroups] != 0;
+                const GroupShift gs = group_shift(a, gtab, r0, chint);
+                if (live && ok) {
+                    const int64_t off = blocked_offset(gcol + gs.crow, (r0 >> 5) + gs.c, a.scol_tiles_c);
+#pragma unroll
+                    for (int o = 0; o < NOUT; ++o) a.s_col[o][off] = static_cast<uint8_t>(b[o]);
+                }
             } else if (live) {
                 const int64_t off = a.blocked ? blocked_offset(gcol, r0 >> 5, a.scol_tiles_c) : (r0 >> 5) * a.ld_scol + gcol;
 #pragma unroll

@@ -9,7 +9,7 @@ namespace mx {
 
 // Launch mxfp8_tile_kernel<OP, MODE> on `grid` CTAs.  The dynamic shared
 // memory limit of the instantiation is raised once per device.
-template <int OP, int MODE, int ACT>
+template <int OP, int MODE, int ACT, bool GRP>
 cudaError_t launch_tiles(const CUtensorMap (&maps)[3], const KernelArgs &a, int grid,
                          cudaStream_t stream, int device)
 {
@@ -17,13 +17,10 @@ cudaError_t launch_tiles(const CUtensorMap (&maps)[3], const KernelArgs &a, int 
     constexpr int kStages = Tuning<OP, MODE>::kStages;
     constexpr int kCtas = Tuning<OP, MODE>::kCtas;
     constexpr int kGroup = Tuning<OP, MODE>::kGroup;
-    // the per-group table is reserved only for launches that use it
-    constexpr size_t kSmem = smem_bytes<OP, kTM, kStages, kGroup>();
+    constexpr size_t kSmem = smem_bytes<OP, kTM, kStages, kGroup, GRP>();
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
     static_assert(kCtas * (kSmem + 1024) <= 228 * 1024, "shared memory per SM");
-    const bool grouped = a.blocked && (a.group_end != nullptr || a.uni_blocks > 0);
-    const size_t smem = grouped ? kSmem : kSmem - kGroupTableBytes;
-    auto kern = mxfp8_tile_kernel<OP, MODE, kTM, kStages, kCtas, kGroup, ACT>;
+    auto kern = mxfp8_tile_kernel<OP, MODE, kTM, kStages, kCtas, kGroup, ACT, GRP>;
     static std::atomic<unsigned long long> attr_done{0};
     const unsigned long long bit = 1ull << (device & 63);
     if (!(attr_done.load(std::memory_order_acquire) & bit)) {
@@ -35,7 +32,7 @@ cudaError_t launch_tiles(const CUtensorMap (&maps)[3], const KernelArgs &a, int 
     void *args[] = {const_cast<CUtensorMap *>(&maps[0]), const_cast<CUtensorMap *>(&maps[1]),
                     const_cast<CUtensorMap *>(&maps[2]), const_cast<KernelArgs *>(&a)};
     return cudaLaunchKernel(reinterpret_cast<const void *>(kern), dim3(grid),
-                            dim3((warps_of<kTM>() + 1) * 32), args, smem, stream);
+                            dim3((warps_of<kTM>() + 1) * 32), args, kSmem, stream);
 }
 
 // tile rows, resident CTAs per SM and row-scale group of the instantiation
@@ -67,7 +64,9 @@ inline LaunchShape launch_shape(int op, int mode)
 // each
 #define MX_DECLARE_LAUNCH(NAME)                                                                  \
     cudaError_t NAME(int mode, const CUtensorMap (&maps)[3], const KernelArgs &a, int grid,      \
-                     cudaStream_t stream, int device);
+                     cudaStream_t stream, int device);                                           \
+    cudaError_t NAME##_grouped(int mode, const CUtensorMap (&maps)[3], const KernelArgs &a,      \
+                               int grid, cudaStream_t stream, int device);
 MX_DECLARE_LAUNCH(launch_quant)
 MX_DECLARE_LAUNCH(launch_fwd)
 MX_DECLARE_LAUNCH(launch_bwd)
@@ -75,14 +74,15 @@ MX_DECLARE_LAUNCH(launch_fwd_gelu)
 MX_DECLARE_LAUNCH(launch_bwd_gelu)
 #undef MX_DECLARE_LAUNCH
 
-#define MX_DEFINE_LAUNCH(NAME, OP, ACT)                                                          \
+// one translation unit per (op, activation) and per plain / grouped scales
+#define MX_DEFINE_LAUNCH(NAME, OP, ACT, GRP)                                                     \
     cudaError_t NAME(int mode, const CUtensorMap (&maps)[3], const KernelArgs &a, int grid,      \
                      cudaStream_t stream, int device)                                            \
     {                                                                                            \
         switch (mode) {                                                                          \
-        case kRow: return launch_tiles<OP, kRow, ACT>(maps, a, grid, stream, device);            \
-        case kCol: return launch_tiles<OP, kCol, ACT>(maps, a, grid, stream, device);            \
-        case kBoth: return launch_tiles<OP, kBoth, ACT>(maps, a, grid, stream, device);          \
+        case kRow: return launch_tiles<OP, kRow, ACT, GRP>(maps, a, grid, stream, device);       \
+        case kCol: return launch_tiles<OP, kCol, ACT, GRP>(maps, a, grid, stream, device);       \
+        case kBoth: return launch_tiles<OP, kBoth, ACT, GRP>(maps, a, grid, stream, device);     \
         default: return cudaErrorInvalidValue;                                                   \
         }                                                                                        \
     }
