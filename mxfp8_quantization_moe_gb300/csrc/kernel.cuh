@@ -111,6 +111,36 @@ __device__ __forceinline__ void set_half16(uint32_t &w, int hi, uint32_t b)
     w = hi ? ((w & 0xFFFFu) | (b << 16)) : ((w & 0xFFFF0000u) | b);
 }
 
+// Bit p: pair p of chunk c (in the slot, 16-byte offset roff_c) has a fast
+// value near a rounding midpoint -- the block_values test again, for the
+// rare blocks where some value is.
+template <int OP, int ACT>
+static __device__ __noinline__ uint32_t near_bits_chunk(const uint8_t *stage, int tile_bytes_, uint32_t roff_c)
+{
+    constexpr int NIN = OpTraits<OP>::kIn;
+    uint32_t in[3][4];
+#pragma unroll
+    for (int k = 0; k < NIN; ++k) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(stage + k * tile_bytes_ + roff_c);
+        in[k][0] = v.x;
+        in[k][1] = v.y;
+        in[k][2] = v.z;
+        in[k][3] = v.w;
+    }
+    uint32_t near = 0;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        if constexpr (OP == kFwd) {
+            near |= static_cast<uint32_t>(near_mid2(Gated<ACT>::h2(in[0][p], in[1][p]), Gated<ACT>::kWinH)) << p;
+        } else {
+            uint64_t DG, DU;
+            Gated<ACT>::grads2(in[0][p], in[1][p], in[2][p], DG, DU);
+            near |= static_cast<uint32_t>(near_mid2(DG, Gated<ACT>::kWinDgate) | near_mid2(DU, Gated<ACT>::kWinDup)) << p;
+        }
+    }
+    return near;
+}
+
 // Element values of the lane's block.  For the cast, the input itself; for
 // SwiGLU, the fast element op on the NIN input slots, then the exact
 // recomputation of every element that needs it: all 32 if a gate is outside
@@ -119,13 +149,18 @@ __device__ __forceinline__ void set_half16(uint32_t &w, int hi, uint32_t b)
 // rather than only the blocks whose amax sits at that mantissa pair, also
 // covers the other direction's blocks in "both" mode, and measured cheaper
 // than scanning the risky blocks.)  Returns the outputs' amax patterns.
-template <int OP, int ACT>
+template <int OP, int ACT, bool DIST = false>
 __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t *stage, int tile_bytes_,
                                              const uint32_t (&roff)[4], uint32_t (&out)[2][16],
                                              uint32_t (&amax)[2])
 {
     constexpr int NOUT = OpTraits<OP>::kOut;
     constexpr int NIN = OpTraits<OP>::kIn;
+    // near a rounding midpoint: a bit per pair, or (DIST, forward only) a
+    // running minimum of the values' distances, the pairs found again in the
+    // rare branch (measured: the faster for the forward's "both" row pass,
+    // the slower elsewhere)
+    uint32_t dmin = 0xFFFFFFFFu;
     uint32_t near = 0;     // bit j: pair j (elements 2j, 2j+1)
     bool gates_ok = true;
 #pragma unroll
@@ -148,7 +183,10 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
             for (int p = 0; p < 4; ++p) {
                 const uint64_t H = Gated<ACT>::h2(in[0][p], in[1][p]);
                 out[0][4 * c + p] = pack_bf16x2(f2lo(H), f2hi(H));
-                near |= static_cast<uint32_t>(near_mid2(H, Gated<ACT>::kWinH)) << (4 * c + p);
+                if constexpr (DIST)
+                    dmin = min(dmin, mid_dist2(H, Gated<ACT>::kWinH));
+                else
+                    near |= static_cast<uint32_t>(near_mid2(H, Gated<ACT>::kWinH)) << (4 * c + p);
             }
         } else {
             gates_ok &= gates_fast8(in[1], Gated<ACT>::kMinGate2);
@@ -169,7 +207,15 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
 #pragma unroll
         for (int o = 0; o < NOUT; ++o) full |= amax[o] >= kHugeAmax;
         if (full) near = 0xFFFFu;
-        if (__any_sync(0xFFFFFFFFu, near != 0u)) {
+        if (__any_sync(0xFFFFFFFFu, near != 0u || dmin == 0u)) {
+            if constexpr (DIST && OP == kFwd) {
+                // which pairs: those near a midpoint (their fast values
+                // evaluated again), unless the block is recomputed whole
+                if (!full && dmin == 0u) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) near |= near_bits_chunk<OP, ACT>(stage, tile_bytes_, roff[c]) << (4 * c);
+                }
+            }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 if ((near >> j) & 1u) {
@@ -672,7 +718,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
                 __syncwarp();
             } else {
                 uint32_t out[2][16], amax[2];
-                block_values<OP, ACT>(a, stage_ptr, kTileBytes, roff, out, amax);
+                block_values<OP, ACT, OP == kFwd && MODE == kBoth>(a, stage_ptr, kTileBytes, roff, out, amax);
                 if constexpr (OP == kFwd) {
                     // the activation itself, for callers that keep it in bf16
                     if (a.h_out != nullptr && live) store_h(a, out[0], grow, c0);
