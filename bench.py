@@ -232,6 +232,24 @@ def run_reference(args, world, rank):
 
 
 # -------------------------------------------------------------------- GPU
+def slowest_rank_seconds(elapsed: float, world: int, device) -> float:
+    """The job's time for a timed region: the slowest rank's (MAX over the
+    default process group; one rank: its own)."""
+    if world <= 1:
+        return elapsed
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([elapsed], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job rate: every rank processed its own units (weak scaling), so
+    the bytes of all ranks over the slowest rank's time."""
+    return bytes_per_rank * world / seconds / 1e9
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -332,11 +350,7 @@ def main():
     t_end.record(stream)
     barrier()
     clk = clocks.stop()
-    elapsed = t_start.elapsed_time(t_end) / 1e3
-    if world > 1:
-        t = torch.tensor([elapsed], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = slowest_rank_seconds(t_start.elapsed_time(t_end) / 1e3, world, "cuda")
     flags, fallbacks = mx.device_status()
     if flags:
         raise SystemExit("device status flags %#x after the timed region" % flags)
@@ -352,8 +366,7 @@ def main():
     dom = max(per_cell, key=lambda k: per_cell[k]["us"])
     dom_achieved = per_cell[dom]["GBps"]
 
-    total_bytes = step_bytes(M, N) * K * world
-    value = total_bytes / elapsed / 1e9
+    value = job_gbs(step_bytes(M, N) * K, world, elapsed)
 
     e2e = None
     if not args.no_e2e:
@@ -498,13 +511,8 @@ def run_e2e(args, mx, gate, up, dh, fwd_out, bwd_out, launch, barrier, world):
         step()
     b.record(stream)
     barrier()
-    el = a.elapsed_time(b) / 1e3
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([el], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        el = float(t.item())
-    val = step_bytes() * n * world / el / 1e9
+    el = slowest_rank_seconds(a.elapsed_time(b) / 1e3, world, "cuda")
+    val = job_gbs(step_bytes() * n, world, el)
     return {"value": round(val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": n, "ms_per_step": round(el / n * 1e3, 3)}
 
