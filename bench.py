@@ -260,6 +260,10 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-slabs", type=int, default=8,
+                    help="row slabs the end-to-end step is pipelined over")
+    ap.add_argument("--e2e-copy-streams", type=int, default=1,
+                    help="streams per copy direction in the end-to-end step")
     ap.add_argument("--ref-blocks", type=int, default=2)
     ap.add_argument("--cell", default=None,
                     help="time one cell only (fwd_row ... bwd_both, quant_row/col/both, quant3d) "
@@ -480,41 +484,115 @@ def run_cell(args):
 def run_e2e(args, mx, gate, up, dh, fwd_out, bwd_out, launch, barrier, world):
     """Same metric through the public API with host buffers: every step copies
     the inputs host->device from pinned memory, runs the six cells, and
-    copies every cast output back to pinned host memory."""
+    copies every cast output back to pinned host memory.  The step is
+    pipelined over row slabs on three streams (host->device copies, the
+    casts, device->host copies; events order each slab's stages and keep a
+    slab's buffers from being overwritten while the previous step still
+    reads them), so the two copy directions and the casts overlap.  Each
+    slab has its own outputs: rowwise data and both scale sets are the
+    slab's rows of the whole-tensor layouts; colwise data are column-major
+    per slab."""
     import torch
+    M, N = gate.shape
+    S = max(1, args.e2e_slabs)
+    while M % (32 * S):
+        S -= 1
+    Ms = M // S
+    dev = gate.device
     h_in = [t.cpu().pin_memory() for t in (gate, up, dh)]
-    outs = []
-    for m in (1, 2, 3):
-        o = fwd_out[m]
-        outs += [t for t in (o.q_row, o.s_row, o.q_col, o.s_col) if t is not None]
-        o = bwd_out[m]
-        outs += [t for t in (o.q_row, o.s_row, o.q_col, o.s_col) if t is not None]
-    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+
+    def alloc_slab():
+        f, b = {}, {}
+        for m in (1, 2, 3):
+            o = mx.MXFP8Cast()
+            if m & 1:
+                o.q_row = torch.empty((Ms, N), dtype=torch.uint8, device=dev)
+                o.s_row = torch.empty((Ms, N // 32), dtype=torch.uint8, device=dev)
+            if m & 2:
+                o.q_col = torch.empty((N, Ms), dtype=torch.uint8, device=dev)
+                o.s_col = torch.empty((Ms // 32, N), dtype=torch.uint8, device=dev)
+            f[m] = o
+            g = mx.SwiGLUGrads()
+            if m & 1:
+                g.q_row = torch.empty((Ms, 2 * N), dtype=torch.uint8, device=dev)
+                g.s_row = torch.empty((Ms, 2 * N // 32), dtype=torch.uint8, device=dev)
+            if m & 2:
+                g.q_col = torch.empty((2 * N, Ms), dtype=torch.uint8, device=dev)
+                g.s_col = torch.empty((Ms // 32, 2 * N), dtype=torch.uint8, device=dev)
+            b[m] = g
+        return f, b
+
+    slabs = [alloc_slab() for _ in range(S)]
+    outs = []       # per slab: device output tensors
+    for f, b in slabs:
+        outs.append([t for m in (1, 2, 3) for o in (f[m], b[m])
+                     for t in (o.q_row, o.s_row, o.q_col, o.s_col) if t is not None])
+    h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in o] for o in outs]
     h2d = sum(t.numel() * t.element_size() for t in h_in)
-    d2h = sum(t.numel() * t.element_size() for t in h_out)
-    stream = torch.cuda.current_stream()
+    d2h = sum(t.numel() * t.element_size() for o in h_out for t in o)
+    C = max(1, args.e2e_copy_streams)
+    s_ins = [torch.cuda.Stream() for _ in range(C)]
+    s_outs = [torch.cuda.Stream() for _ in range(C)]
+    s_run = torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(S)]
+    ev_run = [torch.cuda.Event() for _ in range(S)]
+    ev_out = [torch.cuda.Event() for _ in range(S)]
+    started = [False] * S
 
     def step():
-        for d, h in zip((gate, up, dh), h_in):
-            d.copy_(h, non_blocking=True)
-        for c in CELLS:
-            launch(*c)
-        for d, h in zip(outs, h_out):
-            h.copy_(d, non_blocking=True)
+        for k in range(S):
+            r0, r1 = k * Ms, (k + 1) * Ms
+            d_in = [t[r0:r1] for t in (gate, up, dh)]
+            s_in, s_out = s_ins[k % C], s_outs[k % C]
+            with torch.cuda.stream(s_in):
+                if started[k]:
+                    s_in.wait_event(ev_run[k])        # the previous step's casts read these rows
+                for d, h in zip(d_in, h_in):
+                    d.copy_(h[r0:r1], non_blocking=True)
+                ev_in[k].record(s_in)
+            with torch.cuda.stream(s_run):
+                s_run.wait_event(ev_in[k])
+                if started[k]:
+                    s_run.wait_event(ev_out[k])       # the previous step's copies read the outputs
+                f, b = slabs[k]
+                for kind, mode in CELLS:
+                    if kind == "fwd":
+                        mx.swiglu_fwd(d_in[0], d_in[1], mode, out=f[mode], stream=s_run)
+                    else:
+                        mx.swiglu_bwd(d_in[2], d_in[0], d_in[1], mode, out=b[mode], stream=s_run)
+                ev_run[k].record(s_run)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_run[k])
+                for d, h in zip(outs[k], h_out[k]):
+                    h.copy_(d, non_blocking=True)
+                ev_out[k].record(s_out)
+            started[k] = True
+
+    main = torch.cuda.current_stream()
+
+    def join():
+        for st in s_ins + [s_run] + s_outs:
+            main.wait_stream(st)
 
     step()
+    join()
     barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n = max(1, args.e2e_steps)
-    a.record(stream)
+    a.record(main)
+    for st in s_ins + [s_run] + s_outs:
+        st.wait_stream(main)
     for _ in range(n):
         step()
-    b.record(stream)
+    join()
+    b.record(main)
     barrier()
     el = slowest_rank_seconds(a.elapsed_time(b) / 1e3, world, "cuda")
     val = job_gbs(step_bytes() * n, world, el)
     return {"value": round(val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": n, "ms_per_step": round(el / n * 1e3, 3)}
+            "steps": n, "ms_per_step": round(el / n * 1e3, 3), "slabs": S,
+            "note": "pipelined over %d row slabs: %d host->device, 1 cast and %d device->host streams; "
+                    "per-slab outputs" % (S, C, C)}
 
 
 if __name__ == "__main__":
