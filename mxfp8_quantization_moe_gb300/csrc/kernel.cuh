@@ -91,7 +91,7 @@ template <int OP, int TM, int STAGES, int G, bool GRP>
 constexpr size_t smem_bytes()
 {
     return 1024 + static_cast<size_t>(STAGES) * OpTraits<OP>::kIn * tile_bytes<TM>() +
-           static_cast<size_t>(STAGES + 1) * OpTraits<OP>::kOut * scale_group_bytes<TM, G>() + 2 * STAGES * 8 +
+           static_cast<size_t>(STAGES + 1) * OpTraits<OP>::kOut * scale_group_bytes<TM, G>() + 4 * STAGES * 8 +
            (GRP ? kGroupTableBytes : 0);
 }
 
@@ -548,18 +548,23 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
     uint8_t *sbuf0 = smem + STAGES * NIN * kTileBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sbuf0 + (STAGES + 1) * NOUT * scale_group_bytes<TM, G>());
     const uint32_t smem_base = smem_u32(smem);
+    // one full and one empty barrier per stage and 64-column half: the
+    // warps of one half (the two sub-tile columns reading that TMA box) free
+    // it without waiting for the other half
     const uint32_t full0 = smem_u32(bars);
-    const uint32_t empty0 = smem_u32(bars + STAGES);
+    const uint32_t empty0 = smem_u32(bars + 2 * STAGES);
     // per-group layouts (GRP instantiations only): the group table
-    int32_t *gtab = reinterpret_cast<int32_t *>(bars + 2 * STAGES);
+    int32_t *gtab = reinterpret_cast<int32_t *>(bars + 4 * STAGES);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, kWarps);
+            for (int h = 0; h < 2; ++h) {
+                mbar_init(full0 + 8 * (2 * s + h), 1);
+                mbar_init(empty0 + 8 * (2 * s + h), kWarps / 2);
+            }
         }
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -594,32 +599,34 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
         TileWalk<STAGES, G> done(tiles_n);   // the oldest tile not yet recycled
         for (TileWalk<STAGES, G> w(tiles_n); w.u < num_super; w.next(), ++it) {
             const int s = w.s;
-            if (it >= STAGES) {
-                bool ok = lane == 0 ? mbar_wait_bounded(empty0 + 8 * s, w.ph ^ 1u, a.wait_limit) : true;
-                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-                if (!ok) {
-                    if (lane == 0) atomicOr(a.status, kStatusProducerWait);
-                    failed = true;
-                    break;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (it >= STAGES) {
+                    bool ok = lane == 0 ? mbar_wait_bounded(empty0 + 8 * (2 * s + h), w.ph ^ 1u, a.wait_limit) : true;
+                    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                    if (!ok) {
+                        if (lane == 0) {
+                            atomicOr(a.status, kStatusProducerWait);
+                            // half 0 of this tile is already in flight: wait for it
+                            if (h == 1 && !mbar_wait_bounded(full0 + 8 * (2 * s), w.ph, a.wait_limit))
+                                atomicOr(a.status, kStatusDrainWait);
+                        }
+                        failed = true;
+                        break;
+                    }
+                }
+                if (lane == 0) {
+                    const int32_t r0 = static_cast<int32_t>(w.tr * kTileM);
+                    const int32_t c0 = static_cast<int32_t>(w.tc() * kTileN) + h * kBoxN;
+                    const uint32_t bar = full0 + 8 * (2 * s + h);
+                    const uint32_t dst = smem_base + static_cast<uint32_t>(s * NIN) * kTileBytes + h * kBoxBytes;
+                    mbar_expect_tx(bar, NIN * kBoxBytes);
+                    tma_load_2d(dst, &tm0, c0, r0, bar);
+                    if (NIN > 1) tma_load_2d(dst + kTileBytes, &tm1, c0, r0, bar);
+                    if (NIN > 2) tma_load_2d(dst + 2 * kTileBytes, &tm2, c0, r0, bar);
                 }
             }
-            if (lane == 0) {
-                const int32_t r0 = static_cast<int32_t>(w.tr * kTileM);
-                const int32_t c0 = static_cast<int32_t>(w.tc() * kTileN);
-                const uint32_t bar = full0 + 8 * s;
-                const uint32_t dst = smem_base + static_cast<uint32_t>(s * NIN) * kTileBytes;
-                mbar_expect_tx(bar, NIN * kTileBytes);
-                tma_load_2d(dst, &tm0, c0, r0, bar);
-                tma_load_2d(dst + kBoxBytes, &tm0, c0 + kBoxN, r0, bar);
-                if (NIN > 1) {
-                    tma_load_2d(dst + kTileBytes, &tm1, c0, r0, bar);
-                    tma_load_2d(dst + kTileBytes + kBoxBytes, &tm1, c0 + kBoxN, r0, bar);
-                }
-                if (NIN > 2) {
-                    tma_load_2d(dst + 2 * kTileBytes, &tm2, c0, r0, bar);
-                    tma_load_2d(dst + 2 * kTileBytes + kBoxBytes, &tm2, c0 + kBoxN, r0, bar);
-                }
-            }
+            if (failed) break;
             if (it >= STAGES) {
                 // tile it - STAGES is finished (its stage was free); if it ends
                 // its group, the group's slot is written again only by a
@@ -641,11 +648,16 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             const uint32_t ph = static_cast<uint32_t>(j / STAGES) & 1u;
             bool ok;
             if (failed) {
-                ok = lane == 0 ? mbar_wait_bounded(full0 + 8 * s, ph, a.wait_limit) : true;
-                if (!ok && lane == 0) atomicOr(a.status, kStatusDrainWait);
+                // both halves of every issued tile
+                for (int h = 0; h < 2; ++h) {
+                    ok = lane == 0 ? mbar_wait_bounded(full0 + 8 * (2 * s + h), ph, a.wait_limit) : true;
+                    if (!ok && lane == 0) atomicOr(a.status, kStatusDrainWait);
+                }
                 continue;
             }
-            ok = lane == 0 ? mbar_wait_bounded(empty0 + 8 * s, ph, a.wait_limit) : true;
+            ok = lane == 0 ? (mbar_wait_bounded(empty0 + 8 * (2 * s), ph, a.wait_limit) &&
+                              mbar_wait_bounded(empty0 + 8 * (2 * s + 1), ph, a.wait_limit))
+                           : true;
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             if (!ok) {
                 if (lane == 0) atomicOr(a.status, kStatusProducerWait);
@@ -684,7 +696,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
     int chint = 0;   // group of this warp's last column-scale lookup
     for (TileWalk<STAGES, G> w(tiles_n); w.u < num_super; w.next()) {
         const int s = w.s;
-        const bool fail = __any_sync(0xFFFFFFFFu, !mbar_wait_bounded(full0 + 8 * s, w.ph, a.wait_limit));
+        const bool fail = __any_sync(0xFFFFFFFFu, !mbar_wait_bounded(full0 + 8 * (2 * s + (scb >> 1)), w.ph, a.wait_limit));
         if (fail) {
             if (lane == 0) atomicOr(a.status, kStatusConsumerWait);
             return;
@@ -788,7 +800,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
 
         if constexpr (kWrites) fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        if (lane == 0) mbar_arrive(empty0 + 8 * (2 * s + (scb >> 1)));
     }
 }
 
