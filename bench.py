@@ -46,16 +46,16 @@ PAGES_US = {("fwd", 1): 904.19, ("fwd", 2): 1022.98, ("fwd", 3): 1216.08,
 # captures summarised under profiles/ (small case scaled by the units
 # processed); valid only for the kernel sources they were taken on.
 TRAFFIC = {
-    "bwd_both": (10.549e9, "4713c68abc7254ec", "profiles/bwd_both_ncu.md"),
-    "bwd_both_gelu": (10.5519e9, "4713c68abc7254ec", "profiles/bwd_both_gelu_ncu.md"),
-    "bwd_col": (8.45358e9, "4713c68abc7254ec", "profiles/bwd_col_ncu.md"),
-    "bwd_row": (8.45322e9, "4713c68abc7254ec", "profiles/bwd_row_ncu.md"),
-    "fwd_both": (6.24369e9, "4713c68abc7254ec", "profiles/fwd_both_ncu.md"),
-    "fwd_col": (5.24769e9, "4713c68abc7254ec", "profiles/fwd_col_ncu.md"),
-    "fwd_row": (5.24158e9, "4713c68abc7254ec", "profiles/fwd_row_ncu.md"),
-    "fwd_row_gelu": (5.24792e9, "4713c68abc7254ec", "profiles/fwd_row_gelu_ncu.md"),
-    "quant3d": (7.83732e9, "4713c68abc7254ec", "profiles/quant3d_ncu.md"),
-    "quant_both": (3.98343e9, "4713c68abc7254ec", "profiles/quant_both_ncu.md"),
+    "bwd_both": (10.5487e9, "c7e824a0860e42f1", "profiles/bwd_both_ncu.md"),
+    "bwd_both_gelu": (10.5501e9, "c7e824a0860e42f1", "profiles/bwd_both_gelu_ncu.md"),
+    "bwd_col": (8.45228e9, "c7e824a0860e42f1", "profiles/bwd_col_ncu.md"),
+    "bwd_row": (8.45464e9, "c7e824a0860e42f1", "profiles/bwd_row_ncu.md"),
+    "fwd_both": (6.23935e9, "c7e824a0860e42f1", "profiles/fwd_both_ncu.md"),
+    "fwd_col": (5.24775e9, "c7e824a0860e42f1", "profiles/fwd_col_ncu.md"),
+    "fwd_row": (5.24539e9, "c7e824a0860e42f1", "profiles/fwd_row_ncu.md"),
+    "fwd_row_gelu": (5.24958e9, "c7e824a0860e42f1", "profiles/fwd_row_gelu_ncu.md"),
+    "quant3d": (7.84267e9, "c7e824a0860e42f1", "profiles/quant3d_ncu.md"),
+    "quant_both": (3.98362e9, "c7e824a0860e42f1", "profiles/quant_both_ncu.md"),
 }
 
 

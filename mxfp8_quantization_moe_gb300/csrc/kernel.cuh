@@ -548,9 +548,12 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
     uint8_t *sbuf0 = smem + STAGES * NIN * kTileBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sbuf0 + (STAGES + 1) * NOUT * scale_group_bytes<TM, G>());
     const uint32_t smem_base = smem_u32(smem);
-    // one full and one empty barrier per stage and 64-column half: the
-    // warps of one half (the two sub-tile columns reading that TMA box) free
-    // it without waiting for the other half
+    // a full and an empty barrier per stage and part: the SwiGLU fused ops
+    // split a stage into its two 64-column halves, so the warps reading one
+    // TMA box free it without waiting for the other half (measured: faster
+    // for them, slower for the compute-bound GEGLU and no gain for the cast)
+    constexpr int kParts = (ACT == kSilu && OP != kQuant) ? 2 : 1;
+    constexpr int kBoxesPerPart = 2 / kParts;
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = smem_u32(bars + 2 * STAGES);
     // per-group layouts (GRP instantiations only): the group table
@@ -561,9 +564,9 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < kParts; ++h) {
                 mbar_init(full0 + 8 * (2 * s + h), 1);
-                mbar_init(empty0 + 8 * (2 * s + h), kWarps / 2);
+                mbar_init(empty0 + 8 * (2 * s + h), kWarps / kParts);
             }
         }
         fence_barrier_init();
@@ -600,14 +603,14 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
         for (TileWalk<STAGES, G> w(tiles_n); w.u < num_super; w.next(), ++it) {
             const int s = w.s;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < kParts; ++h) {
                 if (it >= STAGES) {
                     bool ok = lane == 0 ? mbar_wait_bounded(empty0 + 8 * (2 * s + h), w.ph ^ 1u, a.wait_limit) : true;
                     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
                     if (!ok) {
                         if (lane == 0) {
                             atomicOr(a.status, kStatusProducerWait);
-                            // half 0 of this tile is already in flight: wait for it
+                            // part 0 of this tile is already in flight: wait for it
                             if (h == 1 && !mbar_wait_bounded(full0 + 8 * (2 * s), w.ph, a.wait_limit))
                                 atomicOr(a.status, kStatusDrainWait);
                         }
@@ -617,13 +620,17 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
                 }
                 if (lane == 0) {
                     const int32_t r0 = static_cast<int32_t>(w.tr * kTileM);
-                    const int32_t c0 = static_cast<int32_t>(w.tc() * kTileN) + h * kBoxN;
                     const uint32_t bar = full0 + 8 * (2 * s + h);
-                    const uint32_t dst = smem_base + static_cast<uint32_t>(s * NIN) * kTileBytes + h * kBoxBytes;
-                    mbar_expect_tx(bar, NIN * kBoxBytes);
-                    tma_load_2d(dst, &tm0, c0, r0, bar);
-                    if (NIN > 1) tma_load_2d(dst + kTileBytes, &tm1, c0, r0, bar);
-                    if (NIN > 2) tma_load_2d(dst + 2 * kTileBytes, &tm2, c0, r0, bar);
+                    mbar_expect_tx(bar, NIN * kBoxesPerPart * kBoxBytes);
+#pragma unroll
+                    for (int x = 0; x < kBoxesPerPart; ++x) {
+                        const int box = h * kBoxesPerPart + x;
+                        const int32_t c0 = static_cast<int32_t>(w.tc() * kTileN) + box * kBoxN;
+                        const uint32_t dst = smem_base + static_cast<uint32_t>(s * NIN) * kTileBytes + box * kBoxBytes;
+                        tma_load_2d(dst, &tm0, c0, r0, bar);
+                        if (NIN > 1) tma_load_2d(dst + kTileBytes, &tm1, c0, r0, bar);
+                        if (NIN > 2) tma_load_2d(dst + 2 * kTileBytes, &tm2, c0, r0, bar);
+                    }
                 }
             }
             if (failed) break;
@@ -648,15 +655,15 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             const uint32_t ph = static_cast<uint32_t>(j / STAGES) & 1u;
             bool ok;
             if (failed) {
-                // both halves of every issued tile
-                for (int h = 0; h < 2; ++h) {
+                // every part of every issued tile
+                for (int h = 0; h < kParts; ++h) {
                     ok = lane == 0 ? mbar_wait_bounded(full0 + 8 * (2 * s + h), ph, a.wait_limit) : true;
                     if (!ok && lane == 0) atomicOr(a.status, kStatusDrainWait);
                 }
                 continue;
             }
             ok = lane == 0 ? (mbar_wait_bounded(empty0 + 8 * (2 * s), ph, a.wait_limit) &&
-                              mbar_wait_bounded(empty0 + 8 * (2 * s + 1), ph, a.wait_limit))
+                              (kParts == 1 || mbar_wait_bounded(empty0 + 8 * (2 * s + 1), ph, a.wait_limit)))
                            : true;
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             if (!ok) {
@@ -696,7 +703,8 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
     int chint = 0;   // group of this warp's last column-scale lookup
     for (TileWalk<STAGES, G> w(tiles_n); w.u < num_super; w.next()) {
         const int s = w.s;
-        const bool fail = __any_sync(0xFFFFFFFFu, !mbar_wait_bounded(full0 + 8 * (2 * s + (scb >> 1)), w.ph, a.wait_limit));
+        const uint32_t part = kParts == 2 ? (scb >> 1) : 0u;     // the half this warp reads
+        const bool fail = __any_sync(0xFFFFFFFFu, !mbar_wait_bounded(full0 + 8 * (2 * s + part), w.ph, a.wait_limit));
         if (fail) {
             if (lane == 0) atomicOr(a.status, kStatusConsumerWait);
             return;
@@ -800,7 +808,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
 
         if constexpr (kWrites) fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + 8 * (2 * s + (scb >> 1)));
+        if (lane == 0) mbar_arrive(empty0 + 8 * (2 * s + part));
     }
 }
 
