@@ -453,6 +453,34 @@ __device__ __forceinline__ void flush_row_scales(const KernelArgs &a, const uint
         return;
     }
     const bool whole = a.wide_srow != 0 && gsize == G && blk0 + 4 * G <= nblk;
+    if constexpr (TM % 128 == 0) {
+        // bands of whole 128-row tiles: a lane's rows r, r + 32, r + 64,
+        // r + 96 fill one 16-byte chunk of a 128 x 4 tile -- one store per
+        // tile, where every row is inside the matrix and the buffers are
+        // 16-byte aligned (the layout itself only needs 4)
+        bool al16 = true;
+#pragma unroll
+        for (int o = 0; o < NOUT; ++o) al16 &= (reinterpret_cast<uintptr_t>(a.s_row[o]) & 15u) == 0;
+        if (a.blocked && al16 && row0 + TM <= a.M) {
+#pragma unroll
+            for (int q = 0; q < TM / 128; ++q) {
+                const int i0 = 128 * q + lane;
+#pragma unroll
+                for (int o = 0; o < NOUT; ++o) {
+                    const uint8_t *src = gbuf + o * scale_group_bytes<TM, G>() + 4 * G * i0;
+                    for (int t = 0; t < gsize; ++t) {
+                        uint4 v;
+                        v.x = *reinterpret_cast<const uint32_t *>(src + 4 * t);
+                        v.y = *reinterpret_cast<const uint32_t *>(src + 4 * G * 32 + 4 * t);
+                        v.z = *reinterpret_cast<const uint32_t *>(src + 4 * G * 64 + 4 * t);
+                        v.w = *reinterpret_cast<const uint32_t *>(src + 4 * G * 96 + 4 * t);
+                        *reinterpret_cast<uint4 *>(a.s_row[o] + blocked_offset(row0 + i0, blk0 + 4 * t, a.srow_tiles_c)) = v;
+                    }
+                }
+            }
+            return;
+        }
+    }
     for (int i = lane; i < TM; i += 32) {
         const int64_t row = row0 + i;
         if (row >= a.M) break;

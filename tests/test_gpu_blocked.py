@@ -127,3 +127,26 @@ def test_blocked_layout_drives_a_block_scaled_gemm():
     bad = np.ascontiguousarray(sa.reshape(-1, 4, 32, 4).transpose(0, 2, 1, 3)).reshape(-1)
     wrong = _scaled_mm(qa["q_row"], bad, qb["q_row"], sb)
     assert (np.abs(wrong - want) / scale).max() > 2.0 ** -4
+
+
+@pytest.mark.parametrize("mode", [1, 3])
+def test_blocked_row_scales_at_a_4_byte_offset(mode):
+    """Blocked row-scale buffers need only 4-byte alignment: scales at an
+    offset of 4 bytes from a 16-byte boundary (the kernels' whole-chunk
+    stores then step aside) must still equal the oracle's."""
+    M, N = 256, 512
+    gate, up = _input(M, N, 31), _input(M, N, 32)
+    plain, _ = O.swiglu_fwd(bits(gate), bits(up), mode)
+    nb = int(O.scales_blocked(plain["s_row"]).size)
+    raw = torch.zeros(nb + 16, dtype=torch.uint8, device="cuda")
+    s_row = raw[4:4 + nb]
+    q_row = torch.empty((M, N), dtype=torch.uint8, device="cuda")
+    o = mx.MXFP8Cast(q_row=q_row, s_row=s_row)
+    if mode & 2:
+        o.q_col = torch.empty((N, M), dtype=torch.uint8, device="cuda")
+        o.s_col = torch.zeros(int(O.scales_blocked(np.ascontiguousarray(plain["s_col"].T)).size),
+                              dtype=torch.uint8, device="cuda")
+    mx.swiglu_fwd(gate, up, mode | B, out=o)
+    torch.cuda.synchronize()
+    assert np.array_equal(u8(s_row), O.scales_blocked(plain["s_row"]))
+    compare_codes(u8(q_row), plain["q_row"], 1e-4, "q_row")
