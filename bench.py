@@ -46,16 +46,16 @@ PAGES_US = {("fwd", 1): 904.19, ("fwd", 2): 1022.98, ("fwd", 3): 1216.08,
 # captures summarised under profiles/ (small case scaled by the units
 # processed); valid only for the kernel sources they were taken on.
 TRAFFIC = {
-    "bwd_both": (10.5475e9, "1fecef06c148ef62", "profiles/bwd_both_ncu.md"),
-    "bwd_both_gelu": (10.5535e9, "1fecef06c148ef62", "profiles/bwd_both_gelu_ncu.md"),
-    "bwd_col": (8.4506e9, "1fecef06c148ef62", "profiles/bwd_col_ncu.md"),
-    "bwd_row": (8.45425e9, "1fecef06c148ef62", "profiles/bwd_row_ncu.md"),
-    "fwd_both": (6.23983e9, "1fecef06c148ef62", "profiles/fwd_both_ncu.md"),
-    "fwd_col": (5.24916e9, "1fecef06c148ef62", "profiles/fwd_col_ncu.md"),
-    "fwd_row": (5.24421e9, "1fecef06c148ef62", "profiles/fwd_row_ncu.md"),
-    "fwd_row_gelu": (5.24756e9, "1fecef06c148ef62", "profiles/fwd_row_gelu_ncu.md"),
-    "quant3d": (7.83875e9, "1fecef06c148ef62", "profiles/quant3d_ncu.md"),
-    "quant_both": (3.98363e9, "1fecef06c148ef62", "profiles/quant_both_ncu.md"),
+    "bwd_both": (10.5464e9, "4395adba18e2b023", "profiles/bwd_both_ncu.md"),
+    "bwd_both_gelu": (10.5531e9, "4395adba18e2b023", "profiles/bwd_both_gelu_ncu.md"),
+    "bwd_col": (8.45069e9, "4395adba18e2b023", "profiles/bwd_col_ncu.md"),
+    "bwd_row": (8.45232e9, "4395adba18e2b023", "profiles/bwd_row_ncu.md"),
+    "fwd_both": (6.24166e9, "4395adba18e2b023", "profiles/fwd_both_ncu.md"),
+    "fwd_col": (5.2498e9, "4395adba18e2b023", "profiles/fwd_col_ncu.md"),
+    "fwd_row": (5.2442e9, "4395adba18e2b023", "profiles/fwd_row_ncu.md"),
+    "fwd_row_gelu": (5.24757e9, "4395adba18e2b023", "profiles/fwd_row_gelu_ncu.md"),
+    "quant3d": (7.84612e9, "4395adba18e2b023", "profiles/quant3d_ncu.md"),
+    "quant_both": (3.98293e9, "4395adba18e2b023", "profiles/quant_both_ncu.md"),
 }
 
 
