@@ -46,16 +46,16 @@ PAGES_US = {("fwd", 1): 904.19, ("fwd", 2): 1022.98, ("fwd", 3): 1216.08,
 # captures summarised under profiles/ (small case scaled by the units
 # processed); valid only for the kernel sources they were taken on.
 TRAFFIC = {
-    "bwd_both": (10.5464e9, "4395adba18e2b023", "profiles/bwd_both_ncu.md"),
-    "bwd_both_gelu": (10.5531e9, "4395adba18e2b023", "profiles/bwd_both_gelu_ncu.md"),
-    "bwd_col": (8.45069e9, "4395adba18e2b023", "profiles/bwd_col_ncu.md"),
-    "bwd_row": (8.45232e9, "4395adba18e2b023", "profiles/bwd_row_ncu.md"),
-    "fwd_both": (6.24166e9, "4395adba18e2b023", "profiles/fwd_both_ncu.md"),
-    "fwd_col": (5.2498e9, "4395adba18e2b023", "profiles/fwd_col_ncu.md"),
-    "fwd_row": (5.2442e9, "4395adba18e2b023", "profiles/fwd_row_ncu.md"),
-    "fwd_row_gelu": (5.24757e9, "4395adba18e2b023", "profiles/fwd_row_gelu_ncu.md"),
-    "quant3d": (7.84612e9, "4395adba18e2b023", "profiles/quant3d_ncu.md"),
-    "quant_both": (3.98293e9, "4395adba18e2b023", "profiles/quant_both_ncu.md"),
+    "bwd_both": (10.5487e9, "8f4c355c349c31d3", "profiles/bwd_both_ncu.md"),
+    "bwd_both_gelu": (10.5502e9, "8f4c355c349c31d3", "profiles/bwd_both_gelu_ncu.md"),
+    "bwd_col": (8.4511e9, "8f4c355c349c31d3", "profiles/bwd_col_ncu.md"),
+    "bwd_row": (8.4546e9, "8f4c355c349c31d3", "profiles/bwd_row_ncu.md"),
+    "fwd_both": (6.24343e9, "8f4c355c349c31d3", "profiles/fwd_both_ncu.md"),
+    "fwd_col": (5.25023e9, "8f4c355c349c31d3", "profiles/fwd_col_ncu.md"),
+    "fwd_row": (5.24218e9, "8f4c355c349c31d3", "profiles/fwd_row_ncu.md"),
+    "fwd_row_gelu": (5.24924e9, "8f4c355c349c31d3", "profiles/fwd_row_gelu_ncu.md"),
+    "quant3d": (7.86352e9, "8f4c355c349c31d3", "profiles/quant3d_ncu.md"),
+    "quant_both": (3.98482e9, "8f4c355c349c31d3", "profiles/quant_both_ncu.md"),
 }
 
 

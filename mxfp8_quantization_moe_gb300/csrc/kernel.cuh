@@ -63,9 +63,9 @@ struct Tuning;
         static constexpr int kTM = TM, kStages = STAGES, kCtas = CTAS, kGroup = GROUP; \
         static_assert((TM / 32) * 4 + 1 <= 32, "at most 1024 threads per CTA");     \
     };
-MX_TUNE(kQuant, kRow, 224, 3, 1, 1)
-MX_TUNE(kQuant, kCol, 224, 3, 1, 1)
-MX_TUNE(kQuant, kBoth, 224, 3, 1, 4)
+MX_TUNE(kQuant, kRow, 192, 3, 1, 1)
+MX_TUNE(kQuant, kCol, 192, 3, 1, 1)
+MX_TUNE(kQuant, kBoth, 192, 3, 1, 4)
 MX_TUNE(kFwd, kRow, 128, 3, 1, 1)
 MX_TUNE(kFwd, kCol, 128, 3, 1, 1)
 MX_TUNE(kFwd, kBoth, 128, 3, 1, 4)
