@@ -504,6 +504,55 @@ Spec blank(int op, int mode, int64_t M, int64_t N)
     return s;
 }
 
+// The fused forward's and backward's arguments (activation `act`), as the
+// entry points take them.
+Spec fwd_spec(int act, const uint16_t *gate, const uint16_t *up, int64_t ld_in, int64_t M, int64_t N, int mode,
+              uint8_t *q_row, int64_t ld_qrow, uint8_t *s_row, int64_t ld_srow, uint8_t *q_col, int64_t ld_qcol,
+              uint8_t *s_col, int64_t ld_scol)
+{
+    Spec s = blank(mx::kFwd, mode, M, N);
+    s.act = act;
+    s.in[0] = gate;
+    s.in[1] = up;
+    s.ld_in[0] = s.ld_in[1] = ld_in;
+    s.q_row[0] = q_row;
+    s.s_row[0] = s_row;
+    s.q_col[0] = q_col;
+    s.s_col[0] = s_col;
+    s.ld_qrow = ld_qrow;
+    s.ld_srow = ld_srow;
+    s.ld_qcol = ld_qcol;
+    s.ld_scol = ld_scol;
+    return s;
+}
+
+Spec bwd_spec(int act, const uint16_t *dh, int64_t ld_dh, const uint16_t *gate, const uint16_t *up, int64_t ld_in,
+              int64_t M, int64_t N, int mode, uint8_t *dg_row, uint8_t *du_row, int64_t ld_qrow, uint8_t *dg_srow,
+              uint8_t *du_srow, int64_t ld_srow, uint8_t *dg_col, uint8_t *du_col, int64_t ld_qcol,
+              uint8_t *dg_scol, uint8_t *du_scol, int64_t ld_scol)
+{
+    Spec s = blank(mx::kBwd, mode, M, N);
+    s.act = act;
+    s.in[0] = dh;
+    s.in[1] = gate;
+    s.in[2] = up;
+    s.ld_in[0] = ld_dh;
+    s.ld_in[1] = s.ld_in[2] = ld_in;
+    s.q_row[0] = dg_row;
+    s.q_row[1] = du_row;
+    s.s_row[0] = dg_srow;
+    s.s_row[1] = du_srow;
+    s.q_col[0] = dg_col;
+    s.q_col[1] = du_col;
+    s.s_col[0] = dg_scol;
+    s.s_col[1] = du_scol;
+    s.ld_qrow = ld_qrow;
+    s.ld_srow = ld_srow;
+    s.ld_qcol = ld_qcol;
+    s.ld_scol = ld_scol;
+    return s;
+}
+
 }  // namespace
 
 extern "C" {
@@ -558,19 +607,9 @@ mxfp8_status mxfp8_swiglu_fwd(const uint16_t *gate, const uint16_t *up, int64_t 
                               int64_t ld_srow, uint8_t *q_col, int64_t ld_qcol, uint8_t *s_col,
                               int64_t ld_scol, void *stream)
 {
-    Spec s = blank(mx::kFwd, mode, M, N);
-    s.in[0] = gate;
-    s.in[1] = up;
-    s.ld_in[0] = s.ld_in[1] = ld_in;
-    s.q_row[0] = q_row;
-    s.s_row[0] = s_row;
-    s.q_col[0] = q_col;
-    s.s_col[0] = s_col;
-    s.ld_qrow = ld_qrow;
-    s.ld_srow = ld_srow;
-    s.ld_qcol = ld_qcol;
-    s.ld_scol = ld_scol;
-    return run(s, stream);
+    return run(fwd_spec(mx::kSilu, gate, up, ld_in, M, N, mode, q_row, ld_qrow, s_row, ld_srow, q_col, ld_qcol,
+                        s_col, ld_scol),
+               stream);
 }
 
 mxfp8_status mxfp8_swiglu_fwd_with_h(const uint16_t *gate, const uint16_t *up, int64_t ld_in, int64_t M,
@@ -578,18 +617,8 @@ mxfp8_status mxfp8_swiglu_fwd_with_h(const uint16_t *gate, const uint16_t *up, i
                                      int64_t ld_qrow, uint8_t *s_row, int64_t ld_srow, uint8_t *q_col,
                                      int64_t ld_qcol, uint8_t *s_col, int64_t ld_scol, void *stream)
 {
-    Spec s = blank(mx::kFwd, mode, M, N);
-    s.in[0] = gate;
-    s.in[1] = up;
-    s.ld_in[0] = s.ld_in[1] = ld_in;
-    s.q_row[0] = q_row;
-    s.s_row[0] = s_row;
-    s.q_col[0] = q_col;
-    s.s_col[0] = s_col;
-    s.ld_qrow = ld_qrow;
-    s.ld_srow = ld_srow;
-    s.ld_qcol = ld_qcol;
-    s.ld_scol = ld_scol;
+    Spec s = fwd_spec(mx::kSilu, gate, up, ld_in, M, N, mode, q_row, ld_qrow, s_row, ld_srow, q_col, ld_qcol, s_col,
+                      ld_scol);
     s.with_h = true;
     s.h = h;
     s.ld_h = ld_h;
@@ -603,25 +632,9 @@ mxfp8_status mxfp8_swiglu_bwd(const uint16_t *dh, int64_t ld_dh, const uint16_t 
                               int64_t ld_qcol, uint8_t *dg_scol, uint8_t *du_scol, int64_t ld_scol,
                               void *stream)
 {
-    Spec s = blank(mx::kBwd, mode, M, N);
-    s.in[0] = dh;
-    s.in[1] = gate;
-    s.in[2] = up;
-    s.ld_in[0] = ld_dh;
-    s.ld_in[1] = s.ld_in[2] = ld_in;
-    s.q_row[0] = dg_row;
-    s.q_row[1] = du_row;
-    s.s_row[0] = dg_srow;
-    s.s_row[1] = du_srow;
-    s.q_col[0] = dg_col;
-    s.q_col[1] = du_col;
-    s.s_col[0] = dg_scol;
-    s.s_col[1] = du_scol;
-    s.ld_qrow = ld_qrow;
-    s.ld_srow = ld_srow;
-    s.ld_qcol = ld_qcol;
-    s.ld_scol = ld_scol;
-    return run(s, stream);
+    return run(bwd_spec(mx::kSilu, dh, ld_dh, gate, up, ld_in, M, N, mode, dg_row, du_row, ld_qrow, dg_srow, du_srow,
+                        ld_srow, dg_col, du_col, ld_qcol, dg_scol, du_scol, ld_scol),
+               stream);
 }
 
 mxfp8_status mxfp8_geglu_fwd(const uint16_t *gate, const uint16_t *up, int64_t ld_in, int64_t M,
@@ -629,20 +642,9 @@ mxfp8_status mxfp8_geglu_fwd(const uint16_t *gate, const uint16_t *up, int64_t l
                               int64_t ld_srow, uint8_t *q_col, int64_t ld_qcol, uint8_t *s_col,
                               int64_t ld_scol, void *stream)
 {
-    Spec s = blank(mx::kFwd, mode, M, N);
-    s.in[0] = gate;
-    s.in[1] = up;
-    s.ld_in[0] = s.ld_in[1] = ld_in;
-    s.q_row[0] = q_row;
-    s.s_row[0] = s_row;
-    s.q_col[0] = q_col;
-    s.s_col[0] = s_col;
-    s.ld_qrow = ld_qrow;
-    s.ld_srow = ld_srow;
-    s.ld_qcol = ld_qcol;
-    s.ld_scol = ld_scol;
-    s.act = mx::kGelu;
-    return run(s, stream);
+    return run(fwd_spec(mx::kGelu, gate, up, ld_in, M, N, mode, q_row, ld_qrow, s_row, ld_srow, q_col, ld_qcol,
+                        s_col, ld_scol),
+               stream);
 }
 
 mxfp8_status mxfp8_geglu_bwd(const uint16_t *dh, int64_t ld_dh, const uint16_t *gate,
@@ -652,26 +654,9 @@ mxfp8_status mxfp8_geglu_bwd(const uint16_t *dh, int64_t ld_dh, const uint16_t *
                               int64_t ld_qcol, uint8_t *dg_scol, uint8_t *du_scol, int64_t ld_scol,
                               void *stream)
 {
-    Spec s = blank(mx::kBwd, mode, M, N);
-    s.in[0] = dh;
-    s.in[1] = gate;
-    s.in[2] = up;
-    s.ld_in[0] = ld_dh;
-    s.ld_in[1] = s.ld_in[2] = ld_in;
-    s.q_row[0] = dg_row;
-    s.q_row[1] = du_row;
-    s.s_row[0] = dg_srow;
-    s.s_row[1] = du_srow;
-    s.q_col[0] = dg_col;
-    s.q_col[1] = du_col;
-    s.s_col[0] = dg_scol;
-    s.s_col[1] = du_scol;
-    s.ld_qrow = ld_qrow;
-    s.ld_srow = ld_srow;
-    s.ld_qcol = ld_qcol;
-    s.ld_scol = ld_scol;
-    s.act = mx::kGelu;
-    return run(s, stream);
+    return run(bwd_spec(mx::kGelu, dh, ld_dh, gate, up, ld_in, M, N, mode, dg_row, du_row, ld_qrow, dg_srow, du_srow,
+                        ld_srow, dg_col, du_col, ld_qcol, dg_scol, du_scol, ld_scol),
+               stream);
 }
 
 mxfp8_status mxfp8_quant_3d_colwise(const uint16_t *x, int64_t E, int64_t N, int64_t K, uint8_t *q,
@@ -752,18 +737,9 @@ mxfp8_status mxfp8_swiglu_fwd_grouped(const uint16_t *gate, const uint16_t *up, 
                                       int64_t num_groups, uint8_t *q_row, int64_t ld_qrow, uint8_t *s_row,
                                       uint8_t *q_col, int64_t ld_qcol, uint8_t *s_col, void *stream)
 {
-    Spec s = blank(mx::kFwd, mode | MXFP8_BLOCKED_SCALES, M, N);
     if ((mode & ~(3 | MXFP8_BLOCKED_SCALES)) != 0) return MXFP8_ERR_MODE;
-    s.act = act;
-    s.in[0] = gate;
-    s.in[1] = up;
-    s.ld_in[0] = s.ld_in[1] = ld_in;
-    s.q_row[0] = q_row;
-    s.s_row[0] = s_row;
-    s.q_col[0] = q_col;
-    s.s_col[0] = s_col;
-    s.ld_qrow = ld_qrow;
-    s.ld_qcol = ld_qcol;
+    Spec s = fwd_spec(act, gate, up, ld_in, M, N, mode | MXFP8_BLOCKED_SCALES, q_row, ld_qrow, s_row, 0, q_col,
+                      ld_qcol, s_col, 0);
     s.group_end = group_end;
     s.num_groups = num_groups;
     return run(s, stream);
@@ -776,24 +752,9 @@ mxfp8_status mxfp8_swiglu_bwd_grouped(const uint16_t *dh, int64_t ld_dh, const u
                                       uint8_t *du_srow, uint8_t *dg_col, uint8_t *du_col, int64_t ld_qcol,
                                       uint8_t *dg_scol, uint8_t *du_scol, void *stream)
 {
-    Spec s = blank(mx::kBwd, mode | MXFP8_BLOCKED_SCALES, M, N);
     if ((mode & ~(3 | MXFP8_BLOCKED_SCALES)) != 0) return MXFP8_ERR_MODE;
-    s.act = act;
-    s.in[0] = dh;
-    s.in[1] = gate;
-    s.in[2] = up;
-    s.ld_in[0] = ld_dh;
-    s.ld_in[1] = s.ld_in[2] = ld_in;
-    s.q_row[0] = dg_row;
-    s.q_row[1] = du_row;
-    s.s_row[0] = dg_srow;
-    s.s_row[1] = du_srow;
-    s.q_col[0] = dg_col;
-    s.q_col[1] = du_col;
-    s.s_col[0] = dg_scol;
-    s.s_col[1] = du_scol;
-    s.ld_qrow = ld_qrow;
-    s.ld_qcol = ld_qcol;
+    Spec s = bwd_spec(act, dh, ld_dh, gate, up, ld_in, M, N, mode | MXFP8_BLOCKED_SCALES, dg_row, du_row, ld_qrow,
+                      dg_srow, du_srow, 0, dg_col, du_col, ld_qcol, dg_scol, du_scol, 0);
     s.group_end = group_end;
     s.num_groups = num_groups;
     return run(s, stream);
