@@ -102,3 +102,18 @@ def test_group_end_rules():
         O.scales_blocked_m_groups(s, [40, 30, 64])       # not non-decreasing
     with pytest.raises(AssertionError):
         O.scales_blocked_k_groups(np.ones((8, 2), np.uint8), [40, 64])   # K-groups need 32-row ends
+
+
+@pytest.mark.parametrize("M,N,ends", [(416, 160, [96, 96, 224, 416]), (1024, 288, [32, 160, 480, 992, 1024]),
+                                      (640, 4256, [640]), (400, 96, [64, 64, 320, 400])])
+def test_binding_allocates_the_oracle_layout_sizes(M, N, ends):
+    """The Python binding sizes its zero-filled scale buffers from a formula;
+    it must match the oracle's layouts byte for byte in length."""
+    import mxfp8_quantization_moe_gb300 as mx
+    rows = O.scales_blocked_m_groups(np.zeros((M, N // 32), np.uint8), ends).size
+    rb, cb = mx.grouped_scale_bytes(M, N, len(ends))
+    assert rb == rows
+    if all(e % 32 == 0 for e in ends):
+        cols = O.scales_blocked_k_groups(np.zeros((N, -(-M // 32)), np.uint8), ends).size
+        assert cb == cols
+    assert mx.blocked_bytes(M, N // 32) == O.scales_blocked(np.zeros((M, N // 32), np.uint8)).size
