@@ -37,9 +37,9 @@
  *  - No output may overlap an input or another output (strided regions with
  *    equal leading dimensions are checked exactly, so interleaved layouts
  *    such as [dGate | dUp] halves of one buffer are accepted).
- *  - Calls are thread-safe.  The first call on a device builds a 512 KB
- *    read-only sigmoid table in device memory (see mxfp8_init); do that
- *    before capturing a CUDA graph.
+ *  - Calls are thread-safe.  The first call on a device builds 2 MB of
+ *    read-only tables in device memory (see mxfp8_init); do that before
+ *    capturing a CUDA graph.
  */
 #ifndef MXFP8_H
 #define MXFP8_H
@@ -94,9 +94,11 @@ const char *mxfp8_status_str(mxfp8_status s);
 int mxfp8_version(void);
 
 /*
- * One-time set-up of the current device: fills the library's read-only table
- * of sigmoid(g) in double for every bf16 g (used by the exact-rounding path of
- * the SwiGLU kernels) and waits for it on `stream`.  Every entry point calls it
+ * One-time set-up of the current device: fills the library's read-only
+ * tables, one entry per bf16 pattern g -- sigmoid(g) in double and as a
+ * (hi, lo) float pair, and (hi, lo) pairs of Phi(g) and gelu'(g) (2 MB in
+ * all; used by the exact-rounding paths of the SwiGLU and GEGLU kernels) --
+ * and waits for them on `stream`.  Every entry point calls it
  * on its first use on a device; call it yourself before capturing a graph.
  * Returns MXFP8_ERR_CAPTURE if it would have to run inside a capture.
  */
