@@ -266,7 +266,8 @@ def main():
                     help="streams per copy direction in the end-to-end step")
     ap.add_argument("--ref-blocks", type=int, default=2)
     ap.add_argument("--cell", default=None,
-                    help="time one cell only (fwd_row ... bwd_both, quant_row/col/both, quant3d) "
+                    help="time one cell only (fwd_row ... bwd_both, quant_row/col/both, quant3d, "
+                         "quant3d_row/both) "
                          "on --rows rows; prints per-launch microseconds (for profiling)")
     ap.add_argument("--rows", type=int, default=M_LARGE)
     ap.add_argument("--experts", type=int, default=64)
@@ -415,7 +416,15 @@ def run_cell(args):
     mode = {"row": 1, "col": 2, "both": 3}.get(mname, 2)
     if args.blocked:
         mode |= mx.MXFP8_BLOCKED_SCALES
-    if kind == "quant3d":
+    if kind == "quant3d" and mname in ("row", "both") or (kind == "quant3d" and args.blocked):
+        # mxfp8_quant_3d: rowwise / colwise / both, plain or per-expert blocked scales
+        x = synthetic.experts(args.experts, device="cuda")
+        E, N, K = x.shape
+        k = 2 if mode & 3 == 3 else 1
+        nbytes = E * N * K * 2 + k * (E * N * K + E * N * K // 32)
+        out = mx.quant_3d(x, mode)
+        fn = lambda: mx.quant_3d(x, mode, out=out)
+    elif kind == "quant3d":
         x = synthetic.experts(args.experts, device="cuda")
         E, N, K = x.shape
         q = torch.empty((E, K, N), dtype=torch.uint8, device="cuda")

@@ -341,7 +341,8 @@ def swiglu_bwd_grouped(dh: torch.Tensor, gate: torch.Tensor, up: torch.Tensor, g
     return o
 
 
-def quant_3d(x: torch.Tensor, mode: int = MXFP8_BOTH, stream=None) -> MXFP8Cast:
+def quant_3d(x: torch.Tensor, mode: int = MXFP8_BOTH, out: Optional[MXFP8Cast] = None,
+             stream=None) -> MXFP8Cast:
     """(E, N, K) bf16 expert weights -> rowwise q_row (E, N, K) + s_row
     (E, N, K/32) and/or colwise q_col (E, K, N) [per-expert column-major] +
     s_col (E, N/32, K); with MXFP8_BLOCKED_SCALES each expert's scales as one
@@ -350,6 +351,10 @@ def quant_3d(x: torch.Tensor, mode: int = MXFP8_BOTH, stream=None) -> MXFP8Cast:
         raise ValueError("x must be a contiguous (E, N, K) bf16 CUDA tensor")
     E, N, K = x.shape
     blocked = bool(mode & MXFP8_BLOCKED_SCALES)
+    if out is not None:
+        check(capi.mxfp8_quant_3d(x.data_ptr(), E, N, K, mode, _ptr(out.q_row), _ptr(out.s_row),
+                                  _ptr(out.q_col), _ptr(out.s_col), _stream(stream)), "mxfp8_quant_3d")
+        return out
     o = MXFP8Cast()
     dev = x.device
     if mode & MXFP8_ROWWISE:
