@@ -42,21 +42,26 @@ PAGES_US = {("fwd", 1): 904.19, ("fwd", 2): 1022.98, ("fwd", 3): 1216.08,
             ("bwd", 1): 1321.98, ("bwd", 2): 1710.08, ("bwd", 3): 1859.09}
 
 
-# DRAM traffic (read + write bytes) of one full-size launch, from the ncu
-# captures summarised under profiles/ (small case scaled by the units
-# processed); valid only for the kernel sources they were taken on.
+# DRAM traffic (read + write bytes) of one full-size launch, estimated from
+# an ncu capture of a smaller launch of the same kernel (16384 rows, or 8
+# experts for the 3D cast) scaled by the units processed; keyed to the hash of
+# the kernel sources it was taken on (None once they change).  Write-back still
+# held in L2 when the captured kernel ends does not scale with the size, so the
+# full-size figure slightly understates the real traffic.
 TRAFFIC = {
-    "bwd_both": (10.5487e9, "8f4c355c349c31d3", "profiles/bwd_both_ncu.md"),
-    "bwd_both_gelu": (10.5502e9, "8f4c355c349c31d3", "profiles/bwd_both_gelu_ncu.md"),
-    "bwd_col": (8.4511e9, "8f4c355c349c31d3", "profiles/bwd_col_ncu.md"),
-    "bwd_row": (8.4546e9, "8f4c355c349c31d3", "profiles/bwd_row_ncu.md"),
-    "fwd_both": (6.24343e9, "8f4c355c349c31d3", "profiles/fwd_both_ncu.md"),
-    "fwd_col": (5.25023e9, "8f4c355c349c31d3", "profiles/fwd_col_ncu.md"),
-    "fwd_row": (5.24218e9, "8f4c355c349c31d3", "profiles/fwd_row_ncu.md"),
-    "fwd_row_gelu": (5.24924e9, "8f4c355c349c31d3", "profiles/fwd_row_gelu_ncu.md"),
-    "quant3d": (7.86352e9, "8f4c355c349c31d3", "profiles/quant3d_ncu.md"),
-    "quant_both": (3.98482e9, "8f4c355c349c31d3", "profiles/quant_both_ncu.md"),
+    "bwd_both": (10.5487e9, "8f4c355c349c31d3"),
+    "bwd_both_gelu": (10.5502e9, "8f4c355c349c31d3"),
+    "bwd_col": (8.4511e9, "8f4c355c349c31d3"),
+    "bwd_row": (8.4546e9, "8f4c355c349c31d3"),
+    "fwd_both": (6.24343e9, "8f4c355c349c31d3"),
+    "fwd_col": (5.25023e9, "8f4c355c349c31d3"),
+    "fwd_row": (5.24218e9, "8f4c355c349c31d3"),
+    "fwd_row_gelu": (5.24924e9, "8f4c355c349c31d3"),
+    "quant3d": (7.86352e9, "8f4c355c349c31d3"),
+    "quant_both": (3.98482e9, "8f4c355c349c31d3"),
 }
+TRAFFIC_KIND = ("estimate: ncu dram__bytes_read.sum + dram__bytes_write.sum of a 16384-row launch "
+                "scaled x8 to the full size; L2-resident write-back at kernel end does not scale")
 
 
 def kernel_source_hash() -> str:
@@ -177,7 +182,7 @@ def cpu_sample(rows: int, seed: int = 3):
     """A (rows, 8192) sample of the workload drawn on the host (same recipe)."""
     import numpy as np
     import torch
-    from mxfp8_quantization_moe_gb300 import synthetic
+    import synthetic
     g = torch.Generator().manual_seed(seed)
     t = [synthetic.normal_bf16((rows, N_LARGE), 1.0, g, "cpu") for _ in range(3)]
     return [x.view(torch.int16).numpy().view(np.uint16) for x in t]
@@ -197,12 +202,18 @@ def time_oracle(target_s: float, threads: int):
 
 
 def cpu_baseline(target_s: float):
+    """The oracle on all host cores, then on one thread (a smaller sample)."""
     threads = os.cpu_count() or 1
     rows, dt = time_oracle(target_s, threads)
     b = step_bytes(rows, N_LARGE)
+    rows1, dt1 = time_oracle(target_s / 2, 1)
+    b1 = step_bytes(rows1, N_LARGE)
     return {"value": b / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": "%d of 131072 rows (%d 32-row blocks) x 8192, all six cells, one pass, "
-                      "%.1f s on %d threads" % (rows, rows // 32, dt, threads)}
+                      "%.1f s on %d threads" % (rows, rows // 32, dt, threads),
+            "single_thread": {"value": b1 / dt1 / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": "%d of 131072 rows x 8192, all six cells, one pass, %.1f s"
+                                        % (rows1, dt1)}}
 
 
 def run_reference(args, world, rank):
@@ -250,6 +261,83 @@ def job_gbs(bytes_per_rank: float, world: int, seconds: float) -> float:
     return bytes_per_rank * world / seconds / 1e9
 
 
+# ------------------------------------------------------ every config's cells
+L2_FLUSH_BYTES = 512 * 2 ** 20       # > 2 x the 129 MB L2
+
+
+def time_launches(fn, steps: int, warmup: int, flush=None) -> float:
+    """Median CUDA-event time (us) of one launch of ``fn`` over ``steps``
+    launches after ``warmup`` untimed ones; ``flush`` runs before each timed
+    launch, outside its events."""
+    import torch
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in evs:
+        if flush is not None:
+            flush()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs)
+
+
+def quant3d_bytes(E: int, N: int, K: int) -> int:
+    return E * N * K * 2 + E * N * K + E * N * K // 32
+
+
+def measure_configs(mx, synthetic, peak: float, steps: int, warmup: int):
+    """Every workload of the pages' shape list, one cell at a time: the median
+    launch time over ``steps`` launches, inputs resident in HBM, L2 flushed
+    before each launch.  Keys: workload/cell."""
+    import torch
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = flush_buf.zero_
+    rows = {}
+
+    def record(key, fn, nbytes):
+        us = time_launches(fn, steps, warmup, flush)
+        rows[key] = {"us": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
+                     "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "bytes": nbytes}
+
+    def fused_cells(name, gate, up, dh, cells):
+        M, N = gate.shape
+        for kind, mode in cells:
+            if kind == "fwd":
+                o = mx._alloc(M, N, mode, gate.device)
+                fn = lambda o=o, mode=mode: mx.swiglu_fwd(gate, up, mode, out=o)
+            else:
+                o = mx.swiglu_bwd(dh, gate, up, mode)
+                fn = lambda o=o, mode=mode: mx.swiglu_bwd(dh, gate, up, mode, out=o)
+            record("%s/%s_%s" % (name, kind, MODE_NAME[mode]), fn, cell_bytes(kind, mode, M, N))
+            del o
+
+    buf, gate, up = synthetic.fwd_128x128(device="cuda")
+    fused_cells("fwd_128x128", gate, up, None, [("fwd", 1)])
+    g, u, d = synthetic.mixed(device="cuda")
+    fused_cells("mixed_4096x7168", g, u, d, [("fwd", 3), ("bwd", 3)])
+    del g, u, d
+    g, u, d = synthetic.outlier(device="cuda")
+    fused_cells("outlier_16384x7168", g, u, d, CELLS)
+    del g, u, d
+    x = synthetic.experts(64, device="cuda")
+    _, N, K = x.shape
+    for E in (1, 4, 16, 64):
+        xe = x[:E]
+        q = torch.empty((E, K, N), dtype=torch.uint8, device="cuda")
+        sc = torch.empty((E, N // 32, K), dtype=torch.uint8, device="cuda")
+        record("experts_E%d/quant3d_col" % E, lambda xe=xe, q=q, sc=sc: mx.quant_3d_colwise(xe, q, sc),
+               quant3d_bytes(E, N, K))
+        del q, sc
+    del x, flush_buf
+    torch.cuda.empty_cache()
+    return rows
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -265,6 +353,9 @@ def main():
     ap.add_argument("--e2e-copy-streams", type=int, default=1,
                     help="streams per copy direction in the end-to-end step")
     ap.add_argument("--ref-blocks", type=int, default=2)
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-config cell timings (every workload of the pages' shape list)")
+    ap.add_argument("--config-steps", type=int, default=20)
     ap.add_argument("--cell", default=None,
                     help="time one cell only (fwd_row ... bwd_both, quant_row/col/both, quant3d, "
                          "quant3d_row/both) "
@@ -304,7 +395,7 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
     import mxfp8_quantization_moe_gb300 as mx
-    from mxfp8_quantization_moe_gb300 import synthetic
+    import synthetic
 
     mx.init()
     gate, up, dh = synthetic.large(device="cuda", seed=synthetic.SEEDS["large_131072x8192"] + rank)
@@ -377,6 +468,15 @@ def main():
     if not args.no_e2e:
         e2e = run_e2e(args, mx, gate, up, dh, fwd_out, bwd_out, launch, barrier, world)
 
+    configs = None
+    if not args.no_configs and rank == 0:
+        del fwd_out, bwd_out
+        torch.cuda.empty_cache()
+        configs = measure_configs(mx, synthetic, peak, args.config_steps, max(3, args.warmup))
+        flags, _ = mx.device_status()
+        if flags:
+            raise SystemExit("device status flags %#x after the per-config timings" % flags)
+
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(elapsed / K * 1e3, 4), "higher_is_better": True,
@@ -390,13 +490,19 @@ def main():
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": dom_achieved, "peak": peak,
                      "peak_kind": "%s hbm_gbs (copy)" % peak_kind, "unit": "GB/s",
                      "frac": round(dom_achieved / peak, 4), "traffic": traffic_for(dom),
-                     "algorithmic_bytes": per_cell[dom]["bytes"]},
+                     "traffic_kind": TRAFFIC_KIND, "algorithmic_bytes": per_cell[dom]["bytes"]},
         "gpu_launches": K * len(CELLS),
         "fallback_elements": fallbacks,
         "clocks": clk,
     }
     if e2e:
         line["e2e"] = e2e
+    if configs:
+        line["configs"] = configs
+        line["configs_note"] = ("each workload of the pages' shape list, one cell at a time: median of %d "
+                                "CUDA-event launch times, inputs resident, L2 flushed (512 MB write) "
+                                "before each launch; 3D = the first E experts of the seed-4 draw"
+                                % args.config_steps)
     if cpu:
         line["cpu_baseline"] = cpu
     if rank == 0:
@@ -410,7 +516,7 @@ def run_cell(args):
     """Time one kernel alone (used for ncu captures and tuning sweeps)."""
     import torch
     import mxfp8_quantization_moe_gb300 as mx
-    from mxfp8_quantization_moe_gb300 import synthetic
+    import synthetic
     mx.init()
     kind, _, mname = args.cell.partition("_")
     mode = {"row": 1, "col": 2, "both": 3}.get(mname, 2)
@@ -601,7 +707,9 @@ def run_e2e(args, mx, gate, up, dh, fwd_out, bwd_out, launch, barrier, world):
     return {"value": round(val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": n, "ms_per_step": round(el / n * 1e3, 3), "slabs": S,
             "note": "pipelined over %d row slabs: %d host->device, 1 cast and %d device->host streams; "
-                    "per-slab outputs" % (S, C, C)}
+                    "per-slab outputs: rowwise data and both scale sets are the slab's rows of the "
+                    "whole-tensor layouts, colwise data is column-major per slab ((N, M/%d) each) rather "
+                    "than the (N, M) layout of one call" % (S, C, C, S)}
 
 
 if __name__ == "__main__":

@@ -251,9 +251,13 @@ mxfp8_status mxfp8_swiglu_bwd_grouped(const uint16_t *dh, int64_t ld_dh,
  * or that runs where allocation is forbidden.  (The pages have no
  * counterpart: this is the unfused order -- activation, then the standalone
  * cast -- with the activation kept in library-owned scratch.)
- * Same arguments, rules and results as mxfp8_swiglu_fwd: pass 1 writes the
- * bf16 activation h (computed exactly as the fused kernel computes it) into a
- * static scratch array, pass 2 casts h with the standalone quantizer.
+ * Same arguments and rules as mxfp8_swiglu_fwd: pass 1 writes the bf16
+ * activation h, every element correctly rounded (the fused kernel's exact
+ * path), into a static scratch array; pass 2 casts h with the standalone
+ * quantizer.  Results: scale bytes equal the fused forward's; data codes are
+ * the plain definition's bit for bit, where the fused forward's may differ
+ * by one code in rare elements (its fast activation is within one bf16 step
+ * of the exact one).
  *  - Scratch: 8,388,608 bf16 elements (16 MiB) reserved in every device that
  *    loads the library, held until the process exits.  Rows are padded to a
  *    multiple of 8 elements, so the limit is M * roundup(N, 8) <= 8,388,608;

@@ -10,7 +10,8 @@ import torch
 
 import oracle as O
 from gpu_util import bits, u8
-from mxfp8_quantization_moe_gb300 import capi, device_status, init, synthetic
+import synthetic
+from mxfp8_quantization_moe_gb300 import capi, device_status, init
 import mxfp8_quantization_moe_gb300 as mx
 from test_gpu_swiglu import compare, rand_inputs
 

@@ -17,7 +17,8 @@ import torch
 
 import oracle as O
 from gpu_util import Guarded, bits, compare_codes, u8
-from mxfp8_quantization_moe_gb300 import capi, device_status, synthetic
+import synthetic
+from mxfp8_quantization_moe_gb300 import capi, device_status
 
 pytestmark = pytest.mark.gpu
 
@@ -245,11 +246,22 @@ def test_mixed_4096x7168_both_full():
     print("differing codes:", n)
 
 
-def sample_blocks(M, count, seed):
+def sample_blocks(M, count, seed, edges=()):
+    """`count` random 32-row blocks, the first and last, and `edges`."""
     rng = np.random.default_rng(seed)
     nb = M // 32
     pick = set(rng.choice(nb, size=min(count, nb), replace=False).tolist()) | {0, nb - 1}
-    return sorted(pick)
+    return sorted(pick | {b for b in edges if 0 <= b < nb})
+
+
+def band_edges(M, tile_rows):
+    """32-row blocks on both sides of tile-row boundaries: near the start,
+    the middle and the end of the matrix, and the last (partial) band."""
+    nb, per = M // 32, tile_rows // 32
+    out = set()
+    for t in (1, 2, (M // tile_rows) // 2, M // tile_rows - 1, M // tile_rows):
+        out |= {t * per - 1, t * per}
+    return sorted(b for b in out if 0 <= b < nb)
 
 
 @pytest.mark.parametrize("mode", [1, 2, 3])
@@ -267,13 +279,51 @@ def test_outlier_16384x7168_sampled(mode):
 @pytest.mark.parametrize("mode", [1, 2, 3])
 def test_large_131072x8192_sampled(mode):
     gate, up, dh = synthetic.large(device="cuda")
-    rows = sample_blocks(gate.shape[0], 8, 10 + mode)
+    M = gate.shape[0]
+    # the forward's and the backward's tile heights (96, 128 rows)
+    rows = sample_blocks(M, 40, 10 + mode, band_edges(M, 96) + band_edges(M, 128))
     got = fwd_gpu(gate, up, mode, rows)
     n = compare(got, oracle_fwd(gate, up, mode, rows), what="large fwd")
     dg, du = bwd_gpu(dh, gate, up, mode, rows)
     wg, wu = oracle_bwd(dh, gate, up, mode, rows)
     n += compare(dg, wg, what="large dgate") + compare(du, wu, what="large dup")
     print("differing codes:", n)
+
+
+def _max_code_invariant(q, s, what):
+    """RCEIL puts every block's largest magnitude in (224, 448] after the
+    descale, so its largest code is 0x76..0x7E (for scale bytes 1..254);
+    q (blocks, 32) codes, s (blocks,) scale bytes, on the device."""
+    mag = (q & 0x7F).amax(dim=1)
+    normal = (s > 0) & (s < 255)
+    bad = normal & ((mag < 0x76) | (mag > 0x7E))
+    assert int(bad.sum()) == 0, "%s: %d blocks break the largest-code rule" % (what, int(bad.sum()))
+    nan_blocks = s == 255
+    assert bool(((q[nan_blocks] & 0x7F) == 0x7F).all()), what
+
+
+@pytest.mark.parametrize("kind", ["fwd", "bwd"])
+def test_large_131072x8192_every_block_invariant(kind):
+    """Every block of the (131072, 8192) casts, both directions, in the
+    launch the benchmark times: the largest-code rule of RCEIL scales."""
+    import mxfp8_quantization_moe_gb300 as mx
+    gate, up, dh = synthetic.large(device="cuda")
+    M, N = gate.shape
+    outs = []
+    if kind == "fwd":
+        o = mx.swiglu_fwd(gate, up, 3)
+        outs.append(("h", o.q_row, o.s_row, o.q_col, o.s_col))
+    else:
+        o = mx.swiglu_bwd(dh, gate, up, 3)
+        for name, c in (("dgate", o.dgate()), ("dup", o.dup())):
+            outs.append((name, c.q_row, c.s_row, c.q_col, c.s_col))
+    torch.cuda.synchronize()
+    for name, qr, sr, qc, sc in outs:
+        _max_code_invariant(qr.reshape(M * N // 32, 32), sr.reshape(-1), name + " rowwise")
+        # column-major data: column c's 32-row block b is q_col[c, 32b:32b+32]
+        _max_code_invariant(qc.reshape(N * M // 32, 32), sc.t().reshape(-1), name + " colwise")
+    flags, _ = device_status()
+    assert flags == 0
 
 
 def test_status_clean_and_fallback_path_used():

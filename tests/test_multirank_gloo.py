@@ -30,7 +30,7 @@ def _rank(rank, world, port, out_dir):
     os.environ["MASTER_PORT"] = str(port)
     dist.init_process_group("gloo", rank=rank, world_size=world)
     import bench
-    from mxfp8_quantization_moe_gb300 import synthetic
+    import synthetic
     local = [1.5, 2.0, 0.5][rank]
     t = bench.slowest_rank_seconds(local, world, "cpu")
     rate = bench.job_gbs(1e9, world, t)
