@@ -24,12 +24,14 @@ using mx::KernelArgs;
 
 // ----------------------------------------------------- device-side state
 // Read-only tables, one entry per bf16 bit pattern g (sigmoid(g) in double
-// and as a (hi, lo) float pair; (hi, lo) pairs of Phi(g) and gelu'(g)),
+// and as a (hi, lo) float pair; (hi, lo) pairs of Phi(g) and gelu'(g), and
+// the two in double),
 // sticky status bits and the count of elements settled by the exact path.
 // Each device that loads the library holds its own copy.
 __device__ double g_sig_table[65536];
 __device__ float2 g_sig2_table[65536];
 __device__ float4 g_gelu_table[65536];
+__device__ double2 g_gelu_dtable[65536];
 __device__ unsigned g_status;
 __device__ unsigned long long g_fallbacks;
 
@@ -39,16 +41,19 @@ __device__ __forceinline__ float2 float_pair(double v)
     return make_float2(hi, __double2float_rn(__dadd_rn(v, -static_cast<double>(hi))));
 }
 
-__global__ void init_sigmoid_table_kernel(double *table, float2 *table2, float4 *gelu_table)
+__global__ void init_sigmoid_table_kernel(double *table, float2 *table2, float4 *gelu_table, double2 *gelu_dtable)
 {
     const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= 65536u) return;
-    const double g = static_cast<double>(__uint_as_float(i << 16));
-    const double s = __drcp_rn(__dadd_rn(1.0, exp(-g)));  // 1 / (1 + e^-g)
+    const float gf = __uint_as_float(i << 16);
+    const double g = static_cast<double>(gf);
+    const double s = mx::sigmoid_double(gf);  // 1 / (1 + e^-g)
     table[i] = s;
     table2[i] = float_pair(s);
-    const float2 p = float_pair(mx::normal_cdf_double(g)), d = float_pair(mx::gelu_grad_double(g));
+    const double phi = mx::normal_cdf_double(g), dgelu = mx::gelu_grad_double(g);
+    const float2 p = float_pair(phi), d = float_pair(dgelu);
     gelu_table[i] = make_float4(p.x, p.y, d.x, d.y);
+    gelu_dtable[i] = make_double2(phi, dgelu);
 }
 
 __global__ void selftest_wait_kernel(unsigned *status, long long limit)
@@ -67,7 +72,8 @@ __global__ void selftest_wait_kernel(unsigned *status, long long limit)
 // The fast-path activation factors for every bf16 gate value, computed by the
 // same device functions the tile kernels inline (on pairs of adjacent
 // patterns): out[k * 65536 + g] for k = 0 sigmoid, 1 silu, 2 1-sigmoid,
-// 3 w = 1 + g(1-sigmoid), 4 silu' = sigmoid * w.
+// 3 w = 1 + g(1-sigmoid), 4 silu' = sigmoid * w, 5 2^120 e^g (the factor of
+// the wide-range values for gates below the fast range).
 __global__ void selftest_activation_kernel(float *out)
 {
     const uint32_t i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
@@ -77,8 +83,8 @@ __global__ void selftest_activation_kernel(float *out)
     const uint64_t S = mx::sigmoid2(G, T, 1.0f);
     const uint64_t SN = mx::mul2(T, S);
     const uint64_t W = mx::fma2(G, SN, mx::f2(1.0f, 1.0f));
-    const uint64_t V[5] = {S, mx::silu2_up(G), SN, W, mx::mul2(S, W)};
-    for (int k = 0; k < 5; ++k) {
+    const uint64_t V[6] = {S, mx::silu2_up(G), SN, W, mx::mul2(S, W), mx::exp_far2(G)};
+    for (int k = 0; k < 6; ++k) {
         out[k * 65536 + i] = mx::f2lo(V[k]);
         out[k * 65536 + i + 1] = mx::f2hi(V[k]);
     }
@@ -109,6 +115,7 @@ struct DeviceState {
     double *table = nullptr;
     float2 *table2 = nullptr;
     float4 *gelu_table = nullptr;
+    double2 *gelu_dtable = nullptr;
     unsigned *status = nullptr;
     unsigned long long *fallbacks = nullptr;
     int sms = 0;
@@ -146,11 +153,13 @@ mxfp8_status ensure_device(cudaStream_t stream, int *dev_out, DeviceState **stat
     d.table2 = static_cast<float2 *>(p);
     if (cudaGetSymbolAddress(&p, g_gelu_table) != cudaSuccess) return MXFP8_ERR_DEVICE;
     d.gelu_table = static_cast<float4 *>(p);
+    if (cudaGetSymbolAddress(&p, g_gelu_dtable) != cudaSuccess) return MXFP8_ERR_DEVICE;
+    d.gelu_dtable = static_cast<double2 *>(p);
     if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return MXFP8_ERR_DEVICE;
     d.status = static_cast<unsigned *>(p);
     if (cudaGetSymbolAddress(&p, g_fallbacks) != cudaSuccess) return MXFP8_ERR_DEVICE;
     d.fallbacks = static_cast<unsigned long long *>(p);
-    init_sigmoid_table_kernel<<<256, 256, 0, stream>>>(d.table, d.table2, d.gelu_table);
+    init_sigmoid_table_kernel<<<256, 256, 0, stream>>>(d.table, d.table2, d.gelu_table, d.gelu_dtable);
     if (cudaGetLastError() != cudaSuccess) return MXFP8_ERR_DEVICE;
     if (cudaMemsetAsync(d.status, 0, sizeof(unsigned), stream) != cudaSuccess ||
         cudaMemsetAsync(d.fallbacks, 0, sizeof(unsigned long long), stream) != cudaSuccess)
@@ -458,6 +467,7 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     a.sig_table = d->table;
     a.sig2_table = d->table2;
     a.gelu_table = d->gelu_table;
+    a.gelu_dtable = d->gelu_dtable;
     a.status = d->status;
     a.fallbacks = d->fallbacks;
     a.wait_limit = d->wait_limit;
@@ -882,8 +892,8 @@ __global__ void swiglu_activation_kernel(const uint16_t *__restrict__ gate,
             uint32_t ow[4];
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
-                const float h0 = mx::swiglu_h_exact(a.sig2_table, mx::bf16lo(gw[p]), mx::bf16lo(uw[p]));
-                const float h1 = mx::swiglu_h_exact(a.sig2_table, mx::bf16hi(gw[p]), mx::bf16hi(uw[p]));
+                const float h0 = mx::swiglu_h_exact(a.sig2_table, a.sig_table, mx::bf16lo(gw[p]), mx::bf16lo(uw[p]));
+                const float h1 = mx::swiglu_h_exact(a.sig2_table, a.sig_table, mx::bf16hi(gw[p]), mx::bf16hi(uw[p]));
                 ow[p] = mx::pack_bf16x2(h0, h1);
             }
             *reinterpret_cast<uint4 *>(o) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
@@ -891,7 +901,7 @@ __global__ void swiglu_activation_kernel(const uint16_t *__restrict__ gate,
             for (int64_t k = 0; c + k < N; ++k) {
                 const float gf = __uint_as_float(static_cast<uint32_t>(g[k]) << 16);
                 const float uf = __uint_as_float(static_cast<uint32_t>(u[k]) << 16);
-                const float hv = mx::swiglu_h_exact(a.sig2_table, gf, uf);
+                const float hv = mx::swiglu_h_exact(a.sig2_table, a.sig_table, gf, uf);
                 o[k] = static_cast<uint16_t>(mx::pack_bf16x2(hv, 0.0f) & 0xFFFFu);
             }
         }
@@ -936,6 +946,7 @@ extern "C" mxfp8_status mxfp8_swiglu_fwd_noalloc(const uint16_t *gate, const uin
     a.sig_table = d->table;
     a.sig2_table = d->table2;
     a.gelu_table = d->gelu_table;
+    a.gelu_dtable = d->gelu_dtable;
     a.fallbacks = d->fallbacks;
     a.status = d->status;
     const int64_t chunks = M * ((N + 7) / 8);

@@ -141,14 +141,52 @@ static __device__ __noinline__ uint32_t near_bits_chunk(const uint8_t *stage, in
     return near;
 }
 
+// One 8-element chunk's output words (both outputs) and the pairs that still
+// need the exact path.
+struct ChunkWords {
+    uint32_t o[2][4];
+    uint32_t need;
+};
+
+// settle_far_pair for every pair of the chunk at 16-byte offset roff_c of the
+// slots (inputs reloaded from the stage); kept out of line, like the exact
+// path: it runs only for chunks holding a gate outside the fast range.
+template <int OP, int ACT>
+static __device__ __noinline__ ChunkWords settle_far_chunk(const uint8_t *stage, int tile_bytes_, uint32_t roff_c,
+                                                           ChunkWords v)
+{
+    constexpr int NIN = OpTraits<OP>::kIn;
+    uint32_t in[3][4] = {};
+#pragma unroll
+    for (int k = 0; k < NIN; ++k) {
+        const uint4 x = *reinterpret_cast<const uint4 *>(stage + k * tile_bytes_ + roff_c);
+        in[k][0] = x.x;
+        in[k][1] = x.y;
+        in[k][2] = x.z;
+        in[k][3] = x.w;
+    }
+    v.need = 0;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const uint32_t w[3] = {in[0][p], in[1][p], in[2][p]};
+        uint32_t o2[2] = {v.o[0][p], v.o[1][p]};
+        if (settle_far_pair<OP, ACT>(w, o2)) v.need |= 1u << p;
+        v.o[0][p] = o2[0];
+        v.o[1][p] = o2[1];
+    }
+    return v;
+}
+
 // Element values of the lane's block.  For the cast, the input itself; for
-// SwiGLU, the fast element op on the NIN input slots, then the exact
-// recomputation of every element that needs it: all 32 if a gate is outside
-// the fast range or a block amax is huge or not finite, otherwise every pair
-// holding a value near a 0x60/0x61 rounding midpoint.  (Testing every value,
-// rather than only the blocks whose amax sits at that mantissa pair, also
-// covers the other direction's blocks in "both" mode, and measured cheaper
-// than scanning the risky blocks.)  Returns the outputs' amax patterns.
+// the gated ops, the fast element op on the NIN input slots, then, in the rare
+// branch: the wide-range values of the pairs whose gates leave the fast range
+// (settle_far_pair), and the exact recomputation of every element that needs
+// it -- all 32 if a block amax is huge or not finite, otherwise every pair
+// that settle_far_pair marks or that holds a value near a 0x60/0x61 rounding
+// midpoint.  (Testing every value, rather than only the blocks whose amax
+// sits at that mantissa pair, also covers the other direction's blocks in
+// "both" mode, and measured cheaper than scanning the risky blocks.)
+// Returns the outputs' amax patterns.
 template <int OP, int ACT, bool DIST = false>
 __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t *stage, int tile_bytes_,
                                              const uint32_t (&roff)[4], uint32_t (&out)[2][16],
@@ -203,11 +241,37 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
 #pragma unroll
     for (int o = 0; o < NOUT; ++o) amax[o] = amax32_lane(out[o]);
     if constexpr (OP != kQuant) {
-        bool full = !gates_ok;
+        bool full = false;
 #pragma unroll
         for (int o = 0; o < NOUT; ++o) full |= amax[o] >= kHugeAmax;
-        if (full) near = 0xFFFFu;
-        if (__any_sync(0xFFFFFFFFu, near != 0u || dmin == 0u)) {
+        if (__any_sync(0xFFFFFFFFu, near != 0u || dmin == 0u || full || !gates_ok)) {
+            if (!gates_ok) {
+                // pairs whose gates leave the fast range: the wide-range
+                // values, the pairs they cannot settle marked for the exact
+                // path; then the block rules again on the new values
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    ChunkWords v;
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) {
+                        v.o[0][p] = out[0][4 * c + p];
+                        v.o[1][p] = NOUT > 1 ? out[1][4 * c + p] : 0u;
+                    }
+                    v = settle_far_chunk<OP, ACT>(stage, tile_bytes_, roff[c], v);
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) {
+                        out[0][4 * c + p] = v.o[0][p];
+                        if constexpr (NOUT > 1) out[1][4 * c + p] = v.o[1][p];
+                    }
+                    near |= v.need << (4 * c);
+                }
+                full = false;
+#pragma unroll
+                for (int o = 0; o < NOUT; ++o) {
+                    amax[o] = amax32_lane(out[o]);
+                    full |= amax[o] >= kHugeAmax;
+                }
+            }
             if constexpr (DIST && OP == kFwd) {
                 // which pairs: those near a midpoint (their fast values
                 // evaluated again), unless the block is recomputed whole
@@ -216,6 +280,7 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
                     for (int c = 0; c < 4; ++c) near |= near_bits_chunk<OP, ACT>(stage, tile_bytes_, roff[c]) << (4 * c);
                 }
             }
+            if (full) near = 0xFFFFu;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 if ((near >> j) & 1u) {
@@ -243,9 +308,10 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
 }
 
 // The same for the row pass of "both" mode, chunk by chunk: each chunk's
-// values are settled (exact recomputation of its pairs near a midpoint, or of
-// all 8 if a gate is outside the fast range or a value is huge or not
-// finite -- the per-element form of the block rules, which is all they need)
+// values are settled (wide-range values for gates below the fast range, exact
+// recomputation of the pairs near a midpoint or marked by settle_far_pair, or
+// of all 8 if a value is huge or not finite -- the per-element form of the
+// block rules, which is all they need)
 // and written at once over the chunk's inputs in the value slots, so only
 // one chunk of outputs lives in registers.  Returns the outputs' amax.
 template <int OP, int ACT>
@@ -269,9 +335,9 @@ __device__ __forceinline__ void block_values_split(const KernelArgs &a, uint8_t 
         }
         uint32_t o4[2][4];
         uint32_t near = 0;   // bit p: pair p of the chunk
-        bool full;
+        bool far;
         if constexpr (OP == kFwd) {
-            full = !gates_fast8(in[0], Gated<ACT>::kMinGate2);
+            far = !gates_fast8(in[0], Gated<ACT>::kMinGate2);
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
                 const uint64_t H = Gated<ACT>::h2(in[0][p], in[1][p]);
@@ -279,7 +345,7 @@ __device__ __forceinline__ void block_values_split(const KernelArgs &a, uint8_t 
                 near |= static_cast<uint32_t>(near_mid2(H, Gated<ACT>::kWinH)) << p;
             }
         } else {
-            full = !gates_fast8(in[1], Gated<ACT>::kMinGate2);
+            far = !gates_fast8(in[1], Gated<ACT>::kMinGate2);
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
                 uint64_t DG, DU;
@@ -290,13 +356,37 @@ __device__ __forceinline__ void block_values_split(const KernelArgs &a, uint8_t 
             }
         }
         uint32_t cm[2];
+        bool full = false;
 #pragma unroll
         for (int o = 0; o < NOUT; ++o) {
             cm[o] = hmax_abs2(hmax_abs2(o4[o][0], o4[o][1]), hmax_abs2(o4[o][2], o4[o][3]));
             full |= (hmax_abs2(cm[o], __byte_perm(cm[o], 0, 0x1032)) & 0x7FFFu) >= kHugeAmax;
         }
-        if (full) near = 0xFu;
-        if (__any_sync(0xFFFFFFFFu, near != 0u)) {
+        if (__any_sync(0xFFFFFFFFu, near != 0u || far || full)) {
+            if (far) {
+                // pairs whose gates leave the fast range: the wide-range
+                // values (the pairs they cannot settle take the exact path)
+                ChunkWords v;
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    v.o[0][p] = o4[0][p];
+                    v.o[1][p] = NOUT > 1 ? o4[1][p] : 0u;
+                }
+                v = settle_far_chunk<OP, ACT>(stage, tile_bytes_, roff[c], v);
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    o4[0][p] = v.o[0][p];
+                    if constexpr (NOUT > 1) o4[1][p] = v.o[1][p];
+                }
+                near |= v.need;
+                full = false;
+#pragma unroll
+                for (int o = 0; o < NOUT; ++o) {
+                    cm[o] = hmax_abs2(hmax_abs2(o4[o][0], o4[o][1]), hmax_abs2(o4[o][2], o4[o][3]));
+                    full |= (hmax_abs2(cm[o], __byte_perm(cm[o], 0, 0x1032)) & 0x7FFFu) >= kHugeAmax;
+                }
+            }
+            if (full) near = 0xFu;
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
                 if ((near >> p) & 1u) {

@@ -7,7 +7,10 @@ scale byte could move).  The windows (64 fp32 ulps for h and dup, 512 for
 dgate) are sized, with a margin of at least 2, from error bounds on the
 gate-only factors: sigmoid and silu within 32 units of 2^-24, silu' within
 256.  The gate takes only 65536 values, so those bounds are checked here for
-all of them against the oracle's double-precision sigmoid.
+all of them against the oracle's double-precision sigmoid.  Gates below -64
+take the wide-range form, whose factor 2^120 e^g is checked the same way
+(within 8 units of 2^-24 wherever it is a normal fp32 number, zero only
+where e^g is below 2^-246).
 """
 import numpy as np
 import pytest
@@ -21,10 +24,10 @@ pytestmark = pytest.mark.gpu
 
 def test_fast_path_error_bounds_for_every_gate():
     init()
-    out = torch.empty(5 * 65536, dtype=torch.float32, device="cuda")
+    out = torch.empty(6 * 65536, dtype=torch.float32, device="cuda")
     assert capi.mxfp8_selftest_activation(out.data_ptr(), torch.cuda.current_stream().cuda_stream) == 0
     torch.cuda.synchronize()
-    v = out.view(5, 65536).cpu().numpy().astype(np.float64)
+    v = out.view(6, 65536).cpu().numpy().astype(np.float64)
     g = (np.arange(65536, dtype=np.uint64) << 16).astype(np.uint32).view(np.float32).astype(np.float64)
     fast = np.isfinite(g) & (g >= -64.0)
     gf = g[fast]
@@ -61,3 +64,24 @@ def test_fast_path_error_bounds_for_every_gate():
           ", ".join("%s %.2f" % (k, e.max()) for k, (e, _) in errs.items()))
     for k, (e, bound) in errs.items():
         assert np.all(np.isfinite(e)) and e.max() <= bound, (k, e.max(), bound)
+
+
+def test_wide_range_factor_for_every_gate_below_the_fast_range():
+    init()
+    out = torch.empty(6 * 65536, dtype=torch.float32, device="cuda")
+    assert capi.mxfp8_selftest_activation(out.data_ptr(), torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    v = out.view(6, 65536)[5].cpu().numpy().astype(np.float64)
+    g = (np.arange(65536, dtype=np.uint64) << 16).astype(np.uint32).view(np.float32).astype(np.float64)
+    far = np.isfinite(g) & (g <= -64.0)
+    gf, got = g[far], v[far]
+    with np.errstate(under="ignore"):
+        want = np.exp(gf) * 2.0 ** 120
+    normal = want >= 2.0 ** -125
+    rel = np.abs(got[normal] - want[normal]) / want[normal] / 2.0 ** -24
+    print("wide-range factor: max relative error %.2f units of 2^-24 over %d gates" % (rel.max(), normal.sum()))
+    assert rel.max() <= 8.0
+    # below the normal range it may flush to zero, and only there: e^g < 2^-246
+    small = ~normal
+    assert np.all((got[small] == 0.0) | (np.abs(got[small] - want[small]) <= 2.0 ** -126))
+    assert np.all(gf[got == 0.0] * np.log2(np.e) < -245.0)
