@@ -103,136 +103,100 @@ __device__ __forceinline__ void set_half16(uint32_t &w, int hi, uint32_t b)
     w = hi ? ((w & 0xFFFFu) | (b << 16)) : ((w & 0xFFFF0000u) | b);
 }
 
-// The pair's fast values (both outputs), as the common path computes them.
-template <int OP, int ACT>
-__device__ __forceinline__ void fast_pair(const uint32_t (&w)[3], uint64_t &V0, uint64_t &V1)
+// Element e (0..31) of the lane's sub-tile row in the slot at `slot_base`, as
+// fp32; roff[c] is the byte offset of chunk c (elements 8c..8c+7) of the row.
+__device__ __forceinline__ float elem_in(const uint8_t *slot_base, const uint32_t (&roff)[4], int e)
 {
-    if constexpr (OP == kFwd) {
-        V0 = Gated<ACT>::h2(w[0], w[1]);
-        V1 = 0;
-    } else {
-        Gated<ACT>::grads2(w[0], w[1], w[2], V0, V1);
-    }
+    const uint16_t b = *reinterpret_cast<const uint16_t *>(slot_base + roff[e >> 3] + 2 * (e & 7));
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
-// Which elements of a pair flagged by the midpoint test are near a midpoint
-// (bit 0 low, bit 1 high): the fast values evaluated again, each tested alone.
-template <int OP, int ACT>
-__device__ __forceinline__ uint32_t near_halves(const uint32_t (&w)[3])
+// word p (0..3) of the 16-byte chunk at roff_c of the slot at `slot_base`
+__device__ __forceinline__ uint32_t word_in(const uint8_t *slot_base, uint32_t roff_c, int p)
 {
-    uint64_t V0, V1;
-    fast_pair<OP, ACT>(w, V0, V1);
-    const uint32_t w0 = OP == kFwd ? Gated<ACT>::kWinH : Gated<ACT>::kWinDgate;
-    uint32_t m = (near_mid1(f2lo(V0), w0) ? 1u : 0u) | (near_mid1(f2hi(V0), w0) ? 2u : 0u);
-    if constexpr (OP != kFwd)
-        m |= (near_mid1(f2lo(V1), Gated<ACT>::kWinDup) ? 1u : 0u) | (near_mid1(f2hi(V1), Gated<ACT>::kWinDup) ? 2u : 0u);
-    return m;
+    return *reinterpret_cast<const uint32_t *>(slot_base + roff_c + 4 * p);
 }
 
-// the 16-byte chunk at offset roff_c of input slot k, as four words
-template <int NIN>
-__device__ __forceinline__ void load_chunk(const uint8_t *stage, int tile_bytes_, uint32_t roff_c, uint32_t (&in)[3][4])
-{
-#pragma unroll
-    for (int k = 0; k < 3; ++k) {
-        if (k < NIN) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(stage + k * tile_bytes_ + roff_c);
-            in[k][0] = v.x;
-            in[k][1] = v.y;
-            in[k][2] = v.z;
-            in[k][3] = v.w;
-        } else {
-            in[k][0] = in[k][1] = in[k][2] = in[k][3] = 0u;
-        }
-    }
-}
-
-// Exact recomputation of element e (0..7) of a chunk, into its output words
+// Bit p: pair p of chunk c (in the slot, 16-byte offset roff_c) has a fast
+// value near a rounding midpoint -- the block_values test again, for the
+// rare blocks where some value is.
 template <int OP, int ACT>
-__device__ __forceinline__ void exact_elem(const ExactTables &t, const uint32_t (&in)[3][4], int e, uint32_t &o0,
-                                           uint32_t &o1)
-{
-    const int p = e >> 1, h = e & 1;
-    const float x0 = h ? bf16hi(in[0][p]) : bf16lo(in[0][p]);
-    const float x1 = h ? bf16hi(in[1][p]) : bf16lo(in[1][p]);
-    if constexpr (OP == kFwd) {
-        set_half16(o0, h, bf16_bits(Gated<ACT>::h_exact(t, x0, x1)));
-    } else {
-        const float x2 = h ? bf16hi(in[2][p]) : bf16lo(in[2][p]);
-        const float2 r = Gated<ACT>::grads_exact(t, x0, x1, x2);
-        set_half16(o0, h, bf16_bits(r.x));
-        set_half16(o1, h, bf16_bits(r.y));
-    }
-}
-
-// The rare path of one 8-element chunk, kept out of line (the common path
-// only tests whether any lane of the warp needs it): for a chunk holding a
-// gate outside the fast range, the wide-range values of its pairs
-// (settle_far_pair); then the exact recomputation of every element of the
-// chunk if a value is huge or not finite, else of the elements that
-// settle_far_pair marks (both of their pair) or that lie near a rounding
-// midpoint (pairs flagged by the common path's test, split into their
-// elements).  v.o: the chunk's output words; near: bits of the flagged
-// pairs; far: the chunk holds a gate outside the fast range.  Returns the
-// settled words, and in v.n the count of exactly recomputed elements.
-struct ChunkWords {
-    uint32_t o[2][4];
-    uint32_t n;
-};
-
-template <int OP, int ACT>
-static __device__ __noinline__ ChunkWords settle_chunk(ExactTables t, const uint8_t *stage, int tile_bytes_,
-                                                       uint32_t roff_c, ChunkWords v, uint32_t near, bool far)
+static __device__ __noinline__ uint32_t near_bits_chunk(const uint8_t *stage, int tile_bytes_, uint32_t roff_c)
 {
     constexpr int NIN = OpTraits<OP>::kIn;
-    constexpr int NOUT = OpTraits<OP>::kOut;
     uint32_t in[3][4];
-    load_chunk<NIN>(stage, tile_bytes_, roff_c, in);
-    uint32_t both = 0;      // pairs whose two elements both take the exact path
-    if (far) {
-#pragma unroll 1
-        for (int p = 0; p < 4; ++p) {
-            const uint32_t w[3] = {in[0][p], in[1][p], in[2][p]};
-            uint32_t o2[2] = {v.o[0][p], v.o[1][p]};
-            if (settle_far_pair<OP, ACT>(w, o2)) both |= 1u << p;
-            v.o[0][p] = o2[0];
-            v.o[1][p] = o2[1];
-        }
-    }
-    bool full = false;
 #pragma unroll
-    for (int o = 0; o < NOUT; ++o) {
-        const uint32_t cm = hmax_abs2(hmax_abs2(v.o[o][0], v.o[o][1]), hmax_abs2(v.o[o][2], v.o[o][3]));
-        full |= (hmax_abs2(cm, __byte_perm(cm, 0, 0x1032)) & 0x7FFFu) >= kHugeAmax;
+    for (int k = 0; k < NIN; ++k) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(stage + k * tile_bytes_ + roff_c);
+        in[k][0] = v.x;
+        in[k][1] = v.y;
+        in[k][2] = v.z;
+        in[k][3] = v.w;
     }
-    uint32_t elems = 0;      // bit e: element e of the chunk
-    if (full) {
-        elems = 0xFFu;
-    } else {
-#pragma unroll 1
-        for (int p = 0; p < 4; ++p) {
-            if ((both >> p) & 1u) {
-                elems |= 3u << (2 * p);
-            } else if ((near >> p) & 1u) {
-                const uint32_t w[3] = {in[0][p], in[1][p], in[2][p]};
-                elems |= near_halves<OP, ACT>(w) << (2 * p);
-            }
+    uint32_t near = 0;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        if constexpr (OP == kFwd) {
+            near |= static_cast<uint32_t>(near_mid2(Gated<ACT>::h2(in[0][p], in[1][p]), Gated<ACT>::kWinH)) << p;
+        } else {
+            uint64_t DG, DU;
+            Gated<ACT>::grads2(in[0][p], in[1][p], in[2][p], DG, DU);
+            near |= static_cast<uint32_t>(near_mid2(DG, Gated<ACT>::kWinDgate) | near_mid2(DU, Gated<ACT>::kWinDup)) << p;
         }
     }
-#pragma unroll 1
-    for (int e = 0; e < 8; ++e)
-        if ((elems >> e) & 1u) exact_elem<OP, ACT>(t, in, e, v.o[0][e >> 1], v.o[1][e >> 1]);
-    v.n = __popc(elems);
-    return v;
+    return near;
+}
+
+// Which elements of a pair the midpoint test flagged are near a midpoint
+// (bit 0 the low element, bit 1 the high one): the pair's fast values
+// evaluated again and tested one by one.  w: the pair's input words in the
+// op's order (gate, up or dh, gate, up).
+template <int OP, int ACT>
+static __device__ __noinline__ uint32_t near_halves(uint32_t w0, uint32_t w1, uint32_t w2)
+{
+    if constexpr (OP == kFwd) {
+        const uint64_t H = Gated<ACT>::h2(w0, w1);
+        return (near_mid1(f2lo(H), Gated<ACT>::kWinH) ? 1u : 0u) | (near_mid1(f2hi(H), Gated<ACT>::kWinH) ? 2u : 0u);
+    } else {
+        uint64_t DG, DU;
+        Gated<ACT>::grads2(w0, w1, w2, DG, DU);
+        const bool lo = near_mid1(f2lo(DG), Gated<ACT>::kWinDgate) || near_mid1(f2lo(DU), Gated<ACT>::kWinDup);
+        const bool hi = near_mid1(f2hi(DG), Gated<ACT>::kWinDgate) || near_mid1(f2hi(DU), Gated<ACT>::kWinDup);
+        return (lo ? 1u : 0u) | (hi ? 2u : 0u);
+    }
+}
+
+// Exact recomputation of pair j (elements 2j, 2j+1 of the lane's block, the
+// ones in mask hm) into its output words.
+template <int OP, int ACT>
+__device__ __forceinline__ void exact_pair(const ExactTables &t, const uint8_t *stage, int tile_bytes_,
+                                           const uint32_t (&roff)[4], int j, uint32_t hm, uint32_t &o0, uint32_t &o1)
+{
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        if (((hm >> h) & 1u) == 0u) continue;
+        const int e = 2 * j + h;
+        const float x0 = elem_in(stage, roff, e);
+        const float x1 = elem_in(stage + tile_bytes_, roff, e);
+        if constexpr (OP == kFwd) {
+            set_half16(o0, h, bf16_bits(Gated<ACT>::h_exact(t, x0, x1)));
+        } else {
+            const float x2 = elem_in(stage + 2 * tile_bytes_, roff, e);
+            const float2 r = Gated<ACT>::grads_exact(t, x0, x1, x2);
+            set_half16(o0, h, bf16_bits(r.x));
+            set_half16(o1, h, bf16_bits(r.y));
+        }
+    }
 }
 
 // Element values of the lane's block.  For the cast, the input itself; for
 // the gated ops, the fast element op on the NIN input slots and the midpoint
 // test of every value (near_mid2: a value within its window of a 0x60/0x61
-// rounding midpoint, where a scale byte could step); then, for the warps with
-// a lane whose block holds a flagged value, a gate outside the fast range or
-// a huge or non-finite amax, settle_chunk on the chunks concerned (every
-// chunk when the amax is huge or not finite, to recompute the whole block).
+// rounding midpoint, where a scale byte could step); then, in the rare path,
+// the exact recomputation of every element that needs it: all 32 if a block
+// amax is huge or not finite, otherwise both elements of every pair holding a
+// gate outside the fast range (the exact path settles those on its
+// wide-range route) and the flagged elements of the pairs the test flagged.
 // (Testing every value, rather than only the blocks whose amax sits at that
 // mantissa pair, also covers the other direction's blocks in "both" mode, and
 // measured cheaper than scanning the risky blocks.)  DIST (forward only): the
@@ -246,18 +210,26 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
 {
     constexpr int NOUT = OpTraits<OP>::kOut;
     constexpr int NIN = OpTraits<OP>::kIn;
+    constexpr int kGate = OP == kFwd ? 0 : 1;
     uint32_t dmin = 0xFFFFFFFFu;
     uint32_t near = 0;     // bit j: pair j (elements 2j, 2j+1)
-    uint32_t farc = 0;     // bit c: chunk c holds a gate outside the fast range
+    bool gates_ok = true;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         uint32_t in[3][4];
-        load_chunk<NIN>(stage, tile_bytes_, roff[c], in);
+#pragma unroll
+        for (int k = 0; k < NIN; ++k) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(stage + k * tile_bytes_ + roff[c]);
+            in[k][0] = v.x;
+            in[k][1] = v.y;
+            in[k][2] = v.z;
+            in[k][3] = v.w;
+        }
         if constexpr (OP == kQuant) {
 #pragma unroll
             for (int p = 0; p < 4; ++p) out[0][4 * c + p] = in[0][p];
         } else if constexpr (OP == kFwd) {
-            farc |= gates_fast8(in[0], Gated<ACT>::kMinGate2) ? 0u : 1u << c;
+            gates_ok &= gates_fast8(in[0], Gated<ACT>::kMinGate2);
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
                 const uint64_t H = Gated<ACT>::h2(in[0][p], in[1][p]);
@@ -268,7 +240,7 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
                     near |= static_cast<uint32_t>(near_mid2(H, Gated<ACT>::kWinH)) << (4 * c + p);
             }
         } else {
-            farc |= gates_fast8(in[1], Gated<ACT>::kMinGate2) ? 0u : 1u << c;
+            gates_ok &= gates_fast8(in[1], Gated<ACT>::kMinGate2);
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
                 uint64_t DG, DU;
@@ -285,30 +257,36 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
         bool full = false;
 #pragma unroll
         for (int o = 0; o < NOUT; ++o) full |= amax[o] >= kHugeAmax;
-        if constexpr (DIST) near = dmin == 0u ? 0xFFFFu : 0u;   // the rare path tells which
-        if (__any_sync(0xFFFFFFFFu, near != 0u || full || farc != 0u)) {
+        if (__any_sync(0xFFFFFFFFu, near != 0u || dmin == 0u || full || !gates_ok)) {
+            uint32_t far = 0;    // pairs holding a gate outside the fast range
+            if (!gates_ok) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    far |= static_cast<uint32_t>(far_gate_pair<ACT>(word_in(stage + kGate * tile_bytes_, roff[j >> 2], j & 3))) << j;
+            }
+            if constexpr (DIST && OP == kFwd) {
+                // which pairs: those near a midpoint (their fast values
+                // evaluated again), unless the block is recomputed whole
+                if (!full && dmin == 0u) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) near |= near_bits_chunk<OP, ACT>(stage, tile_bytes_, roff[c]) << (4 * c);
+                }
+            }
+            if (full) near = 0xFFFFu;
             const ExactTables t = exact_tables(a);
             uint32_t n = 0;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                const uint32_t nc = (near >> (4 * c)) & 0xFu;
-                const bool fc = (farc >> c) & 1u;
-                // settle_chunk also recomputes a chunk holding a huge or
-                // non-finite value whole (the per-chunk form of the rule)
-                if (nc == 0u && !fc && !full) continue;
-                ChunkWords v;
 #pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    v.o[0][p] = out[0][4 * c + p];
-                    v.o[1][p] = NOUT > 1 ? out[1][4 * c + p] : 0u;
+            for (int j = 0; j < 16; ++j) {
+                if (((near | far) >> j) & 1u) {
+                    uint32_t hm = 3u;
+                    if (!full && ((far >> j) & 1u) == 0u) {
+                        const uint32_t cj = roff[j >> 2];
+                        hm = near_halves<OP, ACT>(word_in(stage, cj, j & 3), word_in(stage + tile_bytes_, cj, j & 3),
+                                                  NIN > 2 ? word_in(stage + 2 * tile_bytes_, cj, j & 3) : 0u);
+                    }
+                    exact_pair<OP, ACT>(t, stage, tile_bytes_, roff, j, hm, out[0][j], out[NOUT - 1][j]);
+                    n += __popc(hm);
                 }
-                v = settle_chunk<OP, ACT>(t, stage, tile_bytes_, roff[c], v, nc, fc);
-#pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    out[0][4 * c + p] = v.o[0][p];
-                    if constexpr (NOUT > 1) out[1][4 * c + p] = v.o[1][p];
-                }
-                n += v.n;
             }
             count_fallbacks_warp(a.fallbacks, n);
 #pragma unroll
@@ -318,42 +296,51 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
 }
 
 // The same for the row pass of "both" mode, chunk by chunk: each chunk's
-// values are settled (settle_chunk for the chunks that need it -- the
-// per-chunk form of the block rules, which is all they need) and written at
-// once over the chunk's inputs in the value slots, so only one chunk of
-// outputs lives in registers.  Returns the outputs' amax.
+// values are settled (the exact recomputation of its flagged elements, of
+// both elements of its pairs holding a gate outside the fast range, or of all
+// 8 if a value is huge or not finite -- the per-element form of the block
+// rules, which is all they need) and written at once over the chunk's inputs
+// in the value slots, so only one chunk of outputs lives in registers.
+// Returns the outputs' amax.
 template <int OP, int ACT>
 __device__ __forceinline__ void block_values_split(const KernelArgs &a, uint8_t *stage, int tile_bytes_,
                                                    const uint32_t (&roff)[4], uint32_t (&amax)[2])
 {
     constexpr int NOUT = OpTraits<OP>::kOut;
     constexpr int NIN = OpTraits<OP>::kIn;
+    constexpr int kGate = OP == kFwd ? 0 : 1;
     uint32_t acc[2] = {0u, 0u};   // running max of magnitudes (sign bits ignored)
     uint32_t nfb = 0;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         uint32_t in[3][4];
-        load_chunk<NIN>(stage, tile_bytes_, roff[c], in);
-        ChunkWords v;
+#pragma unroll
+        for (int k = 0; k < NIN; ++k) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(stage + k * tile_bytes_ + roff[c]);
+            in[k][0] = v.x;
+            in[k][1] = v.y;
+            in[k][2] = v.z;
+            in[k][3] = v.w;
+        }
+        uint32_t o4[2][4];
         uint32_t near = 0;   // bit p: pair p of the chunk
-        bool far;
+        bool far_chunk;
         if constexpr (OP == kFwd) {
-            far = !gates_fast8(in[0], Gated<ACT>::kMinGate2);
+            far_chunk = !gates_fast8(in[0], Gated<ACT>::kMinGate2);
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
                 const uint64_t H = Gated<ACT>::h2(in[0][p], in[1][p]);
-                v.o[0][p] = pack_bf16x2(f2lo(H), f2hi(H));
-                v.o[1][p] = 0u;
+                o4[0][p] = pack_bf16x2(f2lo(H), f2hi(H));
                 near |= static_cast<uint32_t>(near_mid2(H, Gated<ACT>::kWinH)) << p;
             }
         } else {
-            far = !gates_fast8(in[1], Gated<ACT>::kMinGate2);
+            far_chunk = !gates_fast8(in[1], Gated<ACT>::kMinGate2);
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
                 uint64_t DG, DU;
                 Gated<ACT>::grads2(in[0][p], in[1][p], in[2][p], DG, DU);
-                v.o[0][p] = pack_bf16x2(f2lo(DG), f2hi(DG));
-                v.o[1][p] = pack_bf16x2(f2lo(DU), f2hi(DU));
+                o4[0][p] = pack_bf16x2(f2lo(DG), f2hi(DG));
+                o4[1][p] = pack_bf16x2(f2lo(DU), f2hi(DU));
                 near |= static_cast<uint32_t>(near_mid2(DG, Gated<ACT>::kWinDgate) | near_mid2(DU, Gated<ACT>::kWinDup)) << p;
             }
         }
@@ -361,23 +348,36 @@ __device__ __forceinline__ void block_values_split(const KernelArgs &a, uint8_t 
         bool full = false;
 #pragma unroll
         for (int o = 0; o < NOUT; ++o) {
-            cm[o] = hmax_abs2(hmax_abs2(v.o[o][0], v.o[o][1]), hmax_abs2(v.o[o][2], v.o[o][3]));
+            cm[o] = hmax_abs2(hmax_abs2(o4[o][0], o4[o][1]), hmax_abs2(o4[o][2], o4[o][3]));
             full |= (hmax_abs2(cm[o], __byte_perm(cm[o], 0, 0x1032)) & 0x7FFFu) >= kHugeAmax;
         }
-        if (__any_sync(0xFFFFFFFFu, near != 0u || far || full)) {
-            if (near != 0u || far || full) {
-                v = settle_chunk<OP, ACT>(exact_tables(a), stage, tile_bytes_, roff[c], v, near, far);
-                nfb += v.n;
+        if (__any_sync(0xFFFFFFFFu, near != 0u || far_chunk || full)) {
+            uint32_t far = 0;
+            if (far_chunk) {
 #pragma unroll
-                for (int o = 0; o < NOUT; ++o)
-                    cm[o] = hmax_abs2(hmax_abs2(v.o[o][0], v.o[o][1]), hmax_abs2(v.o[o][2], v.o[o][3]));
+                for (int p = 0; p < 4; ++p) far |= static_cast<uint32_t>(far_gate_pair<ACT>(in[kGate][p])) << p;
             }
+            if (full) near = 0xFu;
+            const ExactTables t = exact_tables(a);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                if (((near | far) >> p) & 1u) {
+                    uint32_t hm = 3u;
+                    if (!full && ((far >> p) & 1u) == 0u)
+                        hm = near_halves<OP, ACT>(in[0][p], in[1][p], NIN > 2 ? in[2][p] : 0u);
+                    exact_pair<OP, ACT>(t, stage, tile_bytes_, roff, 4 * c + p, hm, o4[0][p], o4[NOUT - 1][p]);
+                    nfb += __popc(hm);
+                }
+            }
+#pragma unroll
+            for (int o = 0; o < NOUT; ++o)
+                cm[o] = hmax_abs2(hmax_abs2(o4[o][0], o4[o][1]), hmax_abs2(o4[o][2], o4[o][3]));
         }
 #pragma unroll
         for (int o = 0; o < NOUT; ++o) {
             acc[o] = hmax_abs2(acc[o], cm[o]);
             *reinterpret_cast<uint4 *>(stage + (NIN - NOUT + o) * tile_bytes_ + roff[c]) =
-                make_uint4(v.o[o][0], v.o[o][1], v.o[o][2], v.o[o][3]);
+                make_uint4(o4[o][0], o4[o][1], o4[o][2], o4[o][3]);
         }
     }
 #pragma unroll
