@@ -133,151 +133,27 @@ static __device__ __noinline__ uint32_t near_bits_chunk(const uint8_t *stage, in
     return near;
 }
 
-// Which elements of a pair the midpoint test flagged are near a midpoint
-// (bit 0 the low element, bit 1 the high one): the pair's fast values
-// evaluated again and tested one by one.  w: the pair's input words in the
-// op's order (gate, up or dh, gate, up).
-template <int OP, int ACT>
-__device__ __forceinline__ uint32_t near_halves(uint32_t w0, uint32_t w1, uint32_t w2)
+// Element e (0..31) of the lane's sub-tile row in the slot at `slot_base`, as
+// fp32; roff[c] is the byte offset of chunk c (elements 8c..8c+7) of the row.
+__device__ __forceinline__ float elem_in(const uint8_t *slot_base, const uint32_t (&roff)[4], int e)
 {
-    if constexpr (OP == kFwd) {
-        const uint64_t H = Gated<ACT>::h2(w0, w1);
-        return (near_mid1(f2lo(H), Gated<ACT>::kWinH) ? 1u : 0u) | (near_mid1(f2hi(H), Gated<ACT>::kWinH) ? 2u : 0u);
-    } else {
-        uint64_t DG, DU;
-        Gated<ACT>::grads2(w0, w1, w2, DG, DU);
-        const bool lo = near_mid1(f2lo(DG), Gated<ACT>::kWinDgate) || near_mid1(f2lo(DU), Gated<ACT>::kWinDup);
-        const bool hi = near_mid1(f2hi(DG), Gated<ACT>::kWinDgate) || near_mid1(f2hi(DU), Gated<ACT>::kWinDup);
-        return (lo ? 1u : 0u) | (hi ? 2u : 0u);
-    }
-}
-
-// One 8-element chunk's output words (both outputs) and the count of its
-// exactly recomputed elements.
-struct ChunkWords {
-    uint32_t o[2][4];
-    uint32_t n;
-};
-
-// The rare path of one chunk (inputs at 16-byte offset roff_c of the slots):
-// the exact recomputation of every element of the chunk if `full`, else of
-// both elements of every pair holding a gate outside the fast range (looked
-// for when `far`; the exact path settles gates below it on its wide-range
-// route) and of the elements near a midpoint in the pairs flagged in `near`.
-template <int OP, int ACT>
-__device__ __forceinline__ ChunkWords settle_chunk_body(const ExactTables &t, const uint8_t *stage, int tile_bytes_,
-                                                        uint32_t roff_c, ChunkWords v, uint32_t near, bool far,
-                                                        bool full)
-{
-    constexpr int NIN = OpTraits<OP>::kIn;
-    constexpr int kGate = OP == kFwd ? 0 : 1;
-    uint32_t in[3][4];
-#pragma unroll
-    for (int k = 0; k < 3; ++k) {
-        if (k < NIN) {
-            const uint4 x = *reinterpret_cast<const uint4 *>(stage + k * tile_bytes_ + roff_c);
-            in[k][0] = x.x;
-            in[k][1] = x.y;
-            in[k][2] = x.z;
-            in[k][3] = x.w;
-        } else {
-            in[k][0] = in[k][1] = in[k][2] = in[k][3] = 0u;
-        }
-    }
-    uint32_t farp = 0;
-    if (far) {
-#pragma unroll
-        for (int p = 0; p < 4; ++p) farp |= static_cast<uint32_t>(far_gate_pair<ACT>(in[kGate][p])) << p;
-    }
-    if (full) near = 0xFu;
-    v.n = 0;
-#pragma unroll 1
-    for (int p = 0; p < 4; ++p) {
-        if ((((near | farp) >> p) & 1u) == 0u) continue;
-        uint32_t hm = 3u;
-        if (!full && ((farp >> p) & 1u) == 0u) hm = near_halves<OP, ACT>(in[0][p], in[1][p], in[2][p]);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            if (((hm >> h) & 1u) == 0u) continue;
-            const float x0 = h ? bf16hi(in[0][p]) : bf16lo(in[0][p]);
-            const float x1 = h ? bf16hi(in[1][p]) : bf16lo(in[1][p]);
-            if constexpr (OP == kFwd) {
-                set_half16(v.o[0][p], h, bf16_bits(Gated<ACT>::h_exact(t, x0, x1)));
-            } else {
-                const float x2 = h ? bf16hi(in[2][p]) : bf16lo(in[2][p]);
-                const float2 r = Gated<ACT>::grads_exact(t, x0, x1, x2);
-                set_half16(v.o[0][p], h, bf16_bits(r.x));
-                set_half16(v.o[1][p], h, bf16_bits(r.y));
-            }
-            ++v.n;
-        }
-    }
-    return v;
-}
-
-// settle_chunk_body kept out of line (the split row pass calls it per chunk)
-template <int OP, int ACT>
-static __device__ __noinline__ ChunkWords settle_chunk(ExactTables t, const uint8_t *stage, int tile_bytes_,
-                                                       uint32_t roff_c, ChunkWords v, uint32_t near, uint32_t flags)
-{
-    return settle_chunk_body<OP, ACT>(t, stage, tile_bytes_, roff_c, v, near, (flags & 1u) != 0u,
-                                      (flags & 2u) != 0u);
-}
-
-// A block's output words and the count of its exactly recomputed elements.
-struct BlockWords {
-    uint32_t o[2][16];
-    uint32_t n;
-};
-
-// The rare path of a whole block, out of line: settle_chunk_body on every
-// chunk that needs it.  flags: bit 0 a gate outside the fast range somewhere
-// in the block, bit 1 the block amax is huge or not finite (recompute the
-// block whole), bit 2 (DIST) the midpoint test fired somewhere, the flagged
-// pairs to be found again.
-template <int OP, int ACT, bool DIST>
-static __device__ __noinline__ BlockWords settle_block(ExactTables t, const uint8_t *stage, int tile_bytes_,
-                                                       uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3,
-                                                       BlockWords v, uint32_t near, uint32_t flags)
-{
-    const uint32_t roff[4] = {r0, r1, r2, r3};
-    const bool far = (flags & 1u) != 0u, full = (flags & 2u) != 0u;
-    v.n = 0;
-#pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-        uint32_t nc = (near >> (4 * c)) & 0xFu;
-        if constexpr (DIST) {
-            if (!full && (flags & 4u) != 0u) nc = near_bits_chunk<OP, ACT>(stage, tile_bytes_, roff[c]);
-        }
-        if (nc == 0u && !far && !full) continue;
-        ChunkWords cw;
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            cw.o[0][p] = v.o[0][4 * c + p];
-            cw.o[1][p] = v.o[1][4 * c + p];
-        }
-        cw = settle_chunk_body<OP, ACT>(t, stage, tile_bytes_, roff[c], cw, nc, far, full);
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            v.o[0][4 * c + p] = cw.o[0][p];
-            v.o[1][4 * c + p] = cw.o[1][p];
-        }
-        v.n += cw.n;
-    }
-    return v;
+    const uint16_t b = *reinterpret_cast<const uint16_t *>(slot_base + roff[e >> 3] + 2 * (e & 7));
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
 // Element values of the lane's block.  For the cast, the input itself; for
 // the gated ops, the fast element op on the NIN input slots and the midpoint
 // test of every value (near_mid2: a value within its window of a 0x60/0x61
-// rounding midpoint, where a scale byte could step); then, for the warps with
-// a lane whose block holds a flagged value, a gate outside the fast range or
-// a huge or non-finite amax, the out-of-line settle_block.  (Testing every
-// value, rather than only the blocks whose amax sits at that mantissa pair,
-// also covers the other direction's blocks in "both" mode, and measured
-// cheaper than scanning the risky blocks.)  DIST (forward only): the test
-// keeps a running minimum of the values' distances instead of a bit per
-// pair.  Returns the outputs' amax patterns.
+// rounding midpoint, where a scale byte could step); then, in the rare path,
+// the exact recomputation of every element that needs it: all 32 if a block
+// amax is huge or not finite, otherwise every pair holding a flagged value or
+// a gate outside the fast range (the exact path settles gates below it on its
+// wide-range route).  (Testing every value, rather than only the blocks whose
+// amax sits at that mantissa pair, also covers the other direction's blocks
+// in "both" mode, and measured cheaper than scanning the risky blocks.)
+// DIST (forward only): the test keeps a running minimum of the values'
+// distances instead of a bit per pair, and the flagged pairs are found again
+// in the rare path.  Returns the outputs' amax patterns.
 template <int OP, int ACT, bool DIST = false>
 __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t *stage, int tile_bytes_,
                                              const uint32_t (&roff)[4], uint32_t (&out)[2][16],
@@ -285,6 +161,7 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
 {
     constexpr int NOUT = OpTraits<OP>::kOut;
     constexpr int NIN = OpTraits<OP>::kIn;
+    constexpr int kGate = OP == kFwd ? 0 : 1;
     uint32_t dmin = 0xFFFFFFFFu;
     uint32_t near = 0;     // bit j: pair j (elements 2j, 2j+1)
     bool gates_ok = true;
@@ -332,24 +209,44 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
 #pragma unroll
         for (int o = 0; o < NOUT; ++o) full |= amax[o] >= kHugeAmax;
         if (__any_sync(0xFFFFFFFFu, near != 0u || dmin == 0u || full || !gates_ok)) {
-            BlockWords bw;
+            if (!gates_ok) {
+                // the pairs holding a gate outside the fast range
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const uint32_t gw =
+                        *reinterpret_cast<const uint32_t *>(stage + kGate * tile_bytes_ + roff[j >> 2] + 4 * (j & 3));
+                    near |= static_cast<uint32_t>(far_gate_pair<ACT>(gw)) << j;
+                }
+            }
+            if constexpr (DIST && OP == kFwd) {
+                // which pairs: those near a midpoint (their fast values
+                // evaluated again), unless the block is recomputed whole
+                if (!full && dmin == 0u) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) near |= near_bits_chunk<OP, ACT>(stage, tile_bytes_, roff[c]) << (4 * c);
+                }
+            }
+            if (full) near = 0xFFFFu;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                bw.o[0][j] = out[0][j];
-                bw.o[1][j] = out[NOUT - 1][j];
-            }
-            const uint32_t flags = (gates_ok ? 0u : 1u) | (full ? 2u : 0u) | (dmin == 0u ? 4u : 0u);
-            if (near != 0u || flags != 0u)
-                bw = settle_block<OP, ACT, DIST>(exact_tables(a), stage, tile_bytes_, roff[0], roff[1], roff[2],
-                                                 roff[3], bw, near, flags);
-            else
-                bw.n = 0;
+                if ((near >> j) & 1u) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                out[0][j] = bw.o[0][j];
-                if constexpr (NOUT > 1) out[1][j] = bw.o[1][j];
+                    for (int h = 0; h < 2; ++h) {
+                        const int e = 2 * j + h;
+                        const float x0 = elem_in(stage, roff, e);
+                        const float x1 = elem_in(stage + tile_bytes_, roff, e);
+                        if constexpr (OP == kFwd) {
+                            set_half16(out[0][j], h, bf16_bits(Gated<ACT>::h_exact(a, x0, x1)));
+                        } else {
+                            const float x2 = elem_in(stage + 2 * tile_bytes_, roff, e);
+                            const float2 r = Gated<ACT>::grads_exact(a, x0, x1, x2);
+                            set_half16(out[0][j], h, bf16_bits(r.x));
+                            set_half16(out[1][j], h, bf16_bits(r.y));
+                        }
+                    }
+                }
             }
-            count_fallbacks_warp(a.fallbacks, bw.n);
+            count_fallbacks_warp(a.fallbacks, 2u * __popc(near));
 #pragma unroll
             for (int o = 0; o < NOUT; ++o) amax[o] = amax32_lane(out[o]);
         }
@@ -357,16 +254,18 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
 }
 
 // The same for the row pass of "both" mode, chunk by chunk: each chunk's
-// values are settled (settle_chunk for the chunks that need it: the
-// per-chunk form of the block rules, which is all they need) and written at
-// once over the chunk's inputs in the value slots, so only one chunk of
-// outputs lives in registers.  Returns the outputs' amax.
+// values are settled (exact recomputation of its pairs holding a flagged
+// value or a gate outside the fast range, or of all 8 if a value is huge or
+// not finite -- the per-element form of the block rules, which is all they
+// need) and written at once over the chunk's inputs in the value slots, so
+// only one chunk of outputs lives in registers.  Returns the outputs' amax.
 template <int OP, int ACT>
 __device__ __forceinline__ void block_values_split(const KernelArgs &a, uint8_t *stage, int tile_bytes_,
                                                    const uint32_t (&roff)[4], uint32_t (&amax)[2])
 {
     constexpr int NOUT = OpTraits<OP>::kOut;
     constexpr int NIN = OpTraits<OP>::kIn;
+    constexpr int kGate = OP == kFwd ? 0 : 1;
     uint32_t acc[2] = {0u, 0u};   // running max of magnitudes (sign bits ignored)
     uint32_t nfb = 0;
 #pragma unroll
@@ -410,25 +309,34 @@ __device__ __forceinline__ void block_values_split(const KernelArgs &a, uint8_t 
             full |= (hmax_abs2(cm[o], __byte_perm(cm[o], 0, 0x1032)) & 0x7FFFu) >= kHugeAmax;
         }
         if (__any_sync(0xFFFFFFFFu, near != 0u || far || full)) {
-            if (near != 0u || far || full) {
-                ChunkWords cw;
+            if (far) {
 #pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    cw.o[0][p] = o4[0][p];
-                    cw.o[1][p] = o4[NOUT - 1][p];
-                }
-                cw = settle_chunk<OP, ACT>(exact_tables(a), stage, tile_bytes_, roff[c], cw, near,
-                                           (far ? 1u : 0u) | (full ? 2u : 0u));
-#pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    o4[0][p] = cw.o[0][p];
-                    if constexpr (NOUT > 1) o4[1][p] = cw.o[1][p];
-                }
-                nfb += cw.n;
-#pragma unroll
-                for (int o = 0; o < NOUT; ++o)
-                    cm[o] = hmax_abs2(hmax_abs2(o4[o][0], o4[o][1]), hmax_abs2(o4[o][2], o4[o][3]));
+                for (int p = 0; p < 4; ++p) near |= static_cast<uint32_t>(far_gate_pair<ACT>(in[kGate][p])) << p;
             }
+            if (full) near = 0xFu;
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                if ((near >> p) & 1u) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int e = 8 * c + 2 * p + h;
+                        const float x0 = elem_in(stage, roff, e);
+                        const float x1 = elem_in(stage + tile_bytes_, roff, e);
+                        if constexpr (OP == kFwd) {
+                            set_half16(o4[0][p], h, bf16_bits(Gated<ACT>::h_exact(a, x0, x1)));
+                        } else {
+                            const float x2 = elem_in(stage + 2 * tile_bytes_, roff, e);
+                            const float2 r = Gated<ACT>::grads_exact(a, x0, x1, x2);
+                            set_half16(o4[0][p], h, bf16_bits(r.x));
+                            set_half16(o4[1][p], h, bf16_bits(r.y));
+                        }
+                    }
+                }
+            }
+            nfb += 2u * __popc(near);
+#pragma unroll
+            for (int o = 0; o < NOUT; ++o)
+                cm[o] = hmax_abs2(hmax_abs2(o4[o][0], o4[o][1]), hmax_abs2(o4[o][2], o4[o][3]));
         }
 #pragma unroll
         for (int o = 0; o < NOUT; ++o) {
