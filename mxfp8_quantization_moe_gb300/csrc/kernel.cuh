@@ -133,27 +133,68 @@ static __device__ __noinline__ uint32_t near_bits_chunk(const uint8_t *stage, in
     return near;
 }
 
-// Element e (0..31) of the lane's sub-tile row in the slot at `slot_base`, as
-// fp32; roff[c] is the byte offset of chunk c (elements 8c..8c+7) of the row.
-__device__ __forceinline__ float elem_in(const uint8_t *slot_base, const uint32_t (&roff)[4], int e)
+// The rare path of one pair of elements, out of line (scalar arguments and a
+// 64-bit result, so that calling it costs the common path nothing): the
+// pair's fast values evaluated again, then, element by element, the exact
+// (correctly rounded) value where the block is recomputed whole (`whole`: a
+// huge or non-finite value), where the gate lies outside the fast range (the
+// exact path settles gates below it on its wide-range route) or where a fast
+// value lies near a 0x60/0x61 rounding midpoint; the fast value elsewhere.
+// w0, w1, w2: the pair's input words in the op's order (gate, up or dh,
+// gate, up); ta, tb: the activation's exact-path tables.  Returns the output
+// words (the second output's in the high half).
+template <int OP, int ACT>
+static __device__ __noinline__ uint64_t settle_pair(const void *ta, const void *tb, uint32_t w0, uint32_t w1,
+                                                    uint32_t w2, bool whole)
 {
-    const uint16_t b = *reinterpret_cast<const uint16_t *>(slot_base + roff[e >> 3] + 2 * (e & 7));
-    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+    constexpr int kGate = OP == kFwd ? 0 : 1;
+    const uint32_t gw = kGate == 0 ? w0 : w1;
+    uint64_t V0, V1 = 0;
+    if constexpr (OP == kFwd)
+        V0 = Gated<ACT>::h2(w0, w1);
+    else
+        Gated<ACT>::grads2(w0, w1, w2, V0, V1);
+    float v0[2] = {f2lo(V0), f2hi(V0)}, v1[2] = {f2lo(V1), f2hi(V1)};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t gb = h ? gw >> 16 : gw & 0xFFFFu;
+        bool need = whole || far_gate<ACT>(gb);
+        if constexpr (OP == kFwd)
+            need |= near_mid1(v0[h], Gated<ACT>::kWinH);
+        else
+            need |= near_mid1(v0[h], Gated<ACT>::kWinDgate) || near_mid1(v1[h], Gated<ACT>::kWinDup);
+        if (need) {
+            const float x0 = h ? bf16hi(w0) : bf16lo(w0), x1 = h ? bf16hi(w1) : bf16lo(w1);
+            if constexpr (OP == kFwd) {
+                v0[h] = Gated<ACT>::h_exact(ta, tb, x0, x1);
+            } else {
+                const float2 r = Gated<ACT>::grads_exact(ta, tb, x0, x1, h ? bf16hi(w2) : bf16lo(w2));
+                v0[h] = r.x;
+                v1[h] = r.y;
+            }
+        }
+    }
+    return static_cast<uint64_t>(pack_bf16x2(v0[0], v0[1])) | (static_cast<uint64_t>(pack_bf16x2(v1[0], v1[1])) << 32);
+}
+
+// word p (0..3) of the 16-byte chunk at roff_c of the slot at `slot_base`
+__device__ __forceinline__ uint32_t word_at(const uint8_t *slot_base, uint32_t roff_c, int p)
+{
+    return *reinterpret_cast<const uint32_t *>(slot_base + roff_c + 4 * p);
 }
 
 // Element values of the lane's block.  For the cast, the input itself; for
 // the gated ops, the fast element op on the NIN input slots and the midpoint
 // test of every value (near_mid2: a value within its window of a 0x60/0x61
-// rounding midpoint, where a scale byte could step); then, in the rare path,
-// the exact recomputation of every element that needs it: all 32 if a block
-// amax is huge or not finite, otherwise every pair holding a flagged value or
-// a gate outside the fast range (the exact path settles gates below it on its
-// wide-range route).  (Testing every value, rather than only the blocks whose
-// amax sits at that mantissa pair, also covers the other direction's blocks
-// in "both" mode, and measured cheaper than scanning the risky blocks.)
-// DIST (forward only): the test keeps a running minimum of the values'
-// distances instead of a bit per pair, and the flagged pairs are found again
-// in the rare path.  Returns the outputs' amax patterns.
+// rounding midpoint, where a scale byte could step); then, for the warps with
+// a lane whose block holds a flagged value, a gate outside the fast range or
+// a huge or non-finite amax, settle_pair on the flagged pairs (on every pair
+// of a block with such a gate or amax).  (Testing every value, rather than
+// only the blocks whose amax sits at that mantissa pair, also covers the
+// other direction's blocks in "both" mode, and measured cheaper than scanning
+// the risky blocks.)  DIST (forward only): the test keeps a running minimum
+// of the values' distances instead of a bit per pair, and the flagged pairs
+// are found again in the rare path.  Returns the outputs' amax patterns.
 template <int OP, int ACT, bool DIST = false>
 __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t *stage, int tile_bytes_,
                                              const uint32_t (&roff)[4], uint32_t (&out)[2][16],
@@ -161,7 +202,6 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
 {
     constexpr int NOUT = OpTraits<OP>::kOut;
     constexpr int NIN = OpTraits<OP>::kIn;
-    constexpr int kGate = OP == kFwd ? 0 : 1;
     uint32_t dmin = 0xFFFFFFFFu;
     uint32_t near = 0;     // bit j: pair j (elements 2j, 2j+1)
     bool gates_ok = true;
@@ -209,41 +249,26 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
 #pragma unroll
         for (int o = 0; o < NOUT; ++o) full |= amax[o] >= kHugeAmax;
         if (__any_sync(0xFFFFFFFFu, near != 0u || dmin == 0u || full || !gates_ok)) {
-            if (!gates_ok) {
-                // the pairs holding a gate outside the fast range
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const uint32_t gw =
-                        *reinterpret_cast<const uint32_t *>(stage + kGate * tile_bytes_ + roff[j >> 2] + 4 * (j & 3));
-                    near |= static_cast<uint32_t>(far_gate_pair<ACT>(gw)) << j;
-                }
-            }
             if constexpr (DIST && OP == kFwd) {
                 // which pairs: those near a midpoint (their fast values
-                // evaluated again), unless the block is recomputed whole
-                if (!full && dmin == 0u) {
+                // evaluated again), unless every pair is settled anyway
+                if (gates_ok && !full && dmin == 0u) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) near |= near_bits_chunk<OP, ACT>(stage, tile_bytes_, roff[c]) << (4 * c);
                 }
             }
-            if (full) near = 0xFFFFu;
+            if (full || !gates_ok) near = 0xFFFFu;
+            const void *ta = Gated<ACT>::table_a(a), *tb = Gated<ACT>::table_b(a);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 if ((near >> j) & 1u) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int e = 2 * j + h;
-                        const float x0 = elem_in(stage, roff, e);
-                        const float x1 = elem_in(stage + tile_bytes_, roff, e);
-                        if constexpr (OP == kFwd) {
-                            set_half16(out[0][j], h, bf16_bits(Gated<ACT>::h_exact(a, x0, x1)));
-                        } else {
-                            const float x2 = elem_in(stage + 2 * tile_bytes_, roff, e);
-                            const float2 r = Gated<ACT>::grads_exact(a, x0, x1, x2);
-                            set_half16(out[0][j], h, bf16_bits(r.x));
-                            set_half16(out[1][j], h, bf16_bits(r.y));
-                        }
-                    }
+                    const uint32_t cj = roff[j >> 2];
+                    const uint64_t r = settle_pair<OP, ACT>(ta, tb, word_at(stage, cj, j & 3),
+                                                            word_at(stage + tile_bytes_, cj, j & 3),
+                                                            NIN > 2 ? word_at(stage + 2 * tile_bytes_, cj, j & 3) : 0u,
+                                                            full);
+                    out[0][j] = static_cast<uint32_t>(r);
+                    if constexpr (NOUT > 1) out[1][j] = static_cast<uint32_t>(r >> 32);
                 }
             }
             count_fallbacks_warp(a.fallbacks, 2u * __popc(near));
@@ -254,18 +279,17 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
 }
 
 // The same for the row pass of "both" mode, chunk by chunk: each chunk's
-// values are settled (exact recomputation of its pairs holding a flagged
-// value or a gate outside the fast range, or of all 8 if a value is huge or
-// not finite -- the per-element form of the block rules, which is all they
-// need) and written at once over the chunk's inputs in the value slots, so
-// only one chunk of outputs lives in registers.  Returns the outputs' amax.
+// values are settled (settle_pair on its flagged pairs, or on all four if a
+// gate is outside the fast range or a value is huge or not finite -- the
+// per-chunk form of the block rules, which is all they need) and written at
+// once over the chunk's inputs in the value slots, so only one chunk of
+// outputs lives in registers.  Returns the outputs' amax.
 template <int OP, int ACT>
 __device__ __forceinline__ void block_values_split(const KernelArgs &a, uint8_t *stage, int tile_bytes_,
                                                    const uint32_t (&roff)[4], uint32_t (&amax)[2])
 {
     constexpr int NOUT = OpTraits<OP>::kOut;
     constexpr int NIN = OpTraits<OP>::kIn;
-    constexpr int kGate = OP == kFwd ? 0 : 1;
     uint32_t acc[2] = {0u, 0u};   // running max of magnitudes (sign bits ignored)
     uint32_t nfb = 0;
 #pragma unroll
@@ -309,28 +333,14 @@ __device__ __forceinline__ void block_values_split(const KernelArgs &a, uint8_t 
             full |= (hmax_abs2(cm[o], __byte_perm(cm[o], 0, 0x1032)) & 0x7FFFu) >= kHugeAmax;
         }
         if (__any_sync(0xFFFFFFFFu, near != 0u || far || full)) {
-            if (far) {
-#pragma unroll
-                for (int p = 0; p < 4; ++p) near |= static_cast<uint32_t>(far_gate_pair<ACT>(in[kGate][p])) << p;
-            }
-            if (full) near = 0xFu;
+            if (full || far) near = 0xFu;
+            const void *ta = Gated<ACT>::table_a(a), *tb = Gated<ACT>::table_b(a);
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
                 if ((near >> p) & 1u) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int e = 8 * c + 2 * p + h;
-                        const float x0 = elem_in(stage, roff, e);
-                        const float x1 = elem_in(stage + tile_bytes_, roff, e);
-                        if constexpr (OP == kFwd) {
-                            set_half16(o4[0][p], h, bf16_bits(Gated<ACT>::h_exact(a, x0, x1)));
-                        } else {
-                            const float x2 = elem_in(stage + 2 * tile_bytes_, roff, e);
-                            const float2 r = Gated<ACT>::grads_exact(a, x0, x1, x2);
-                            set_half16(o4[0][p], h, bf16_bits(r.x));
-                            set_half16(o4[1][p], h, bf16_bits(r.y));
-                        }
-                    }
+                    const uint64_t r = settle_pair<OP, ACT>(ta, tb, in[0][p], in[1][p], NIN > 2 ? in[2][p] : 0u, full);
+                    o4[0][p] = static_cast<uint32_t>(r);
+                    if constexpr (NOUT > 1) o4[1][p] = static_cast<uint32_t>(r >> 32);
                 }
             }
             nfb += 2u * __popc(near);
