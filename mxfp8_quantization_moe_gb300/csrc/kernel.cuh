@@ -189,7 +189,7 @@ __device__ __forceinline__ uint32_t word_at(const uint8_t *slot_base, uint32_t r
 // rounding midpoint, where a scale byte could step); then, for the warps with
 // a lane whose block holds a flagged value, a gate outside the fast range or
 // a huge or non-finite amax, settle_pair on the flagged pairs (on every pair
-// of a block with such a gate or amax).  (Testing every value, rather than
+// of a chunk holding such a gate, of a block with such an amax).  (Testing every value, rather than
 // only the blocks whose amax sits at that mantissa pair, also covers the
 // other direction's blocks in "both" mode, and measured cheaper than scanning
 // the risky blocks.)  DIST (forward only): the test keeps a running minimum
@@ -204,7 +204,7 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
     constexpr int NIN = OpTraits<OP>::kIn;
     uint32_t dmin = 0xFFFFFFFFu;
     uint32_t near = 0;     // bit j: pair j (elements 2j, 2j+1)
-    bool gates_ok = true;
+    uint32_t farc = 0;     // bit c: chunk c holds a gate outside the fast range
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         uint32_t in[3][4];
@@ -220,7 +220,7 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
 #pragma unroll
             for (int p = 0; p < 4; ++p) out[0][4 * c + p] = in[0][p];
         } else if constexpr (OP == kFwd) {
-            gates_ok &= gates_fast8(in[0], Gated<ACT>::kMinGate2);
+            farc |= gates_fast8(in[0], Gated<ACT>::kMinGate2) ? 0u : 1u << c;
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
                 const uint64_t H = Gated<ACT>::h2(in[0][p], in[1][p]);
@@ -231,7 +231,7 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
                     near |= static_cast<uint32_t>(near_mid2(H, Gated<ACT>::kWinH)) << (4 * c + p);
             }
         } else {
-            gates_ok &= gates_fast8(in[1], Gated<ACT>::kMinGate2);
+            farc |= gates_fast8(in[1], Gated<ACT>::kMinGate2) ? 0u : 1u << c;
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
                 uint64_t DG, DU;
@@ -248,16 +248,20 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
         bool full = false;
 #pragma unroll
         for (int o = 0; o < NOUT; ++o) full |= amax[o] >= kHugeAmax;
-        if (__any_sync(0xFFFFFFFFu, near != 0u || dmin == 0u || full || !gates_ok)) {
+        if (__any_sync(0xFFFFFFFFu, near != 0u || dmin == 0u || full || farc != 0u)) {
             if constexpr (DIST && OP == kFwd) {
                 // which pairs: those near a midpoint (their fast values
                 // evaluated again), unless every pair is settled anyway
-                if (gates_ok && !full && dmin == 0u) {
+                if (!full && dmin == 0u) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) near |= near_bits_chunk<OP, ACT>(stage, tile_bytes_, roff[c]) << (4 * c);
                 }
             }
-            if (full || !gates_ok) near = 0xFFFFu;
+            // every pair of a chunk holding a gate outside the fast range, of
+            // the whole block if a value is huge or not finite
+#pragma unroll
+            for (int c = 0; c < 4; ++c) near |= ((farc >> c) & 1u) ? 0xFu << (4 * c) : 0u;
+            if (full) near = 0xFFFFu;
             const void *ta = Gated<ACT>::table_a(a), *tb = Gated<ACT>::table_b(a);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
