@@ -342,7 +342,12 @@ __device__ __forceinline__ void block_values_split(const KernelArgs &a, uint8_t 
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
                 if ((near >> p) & 1u) {
-                    const uint64_t r = settle_pair<OP, ACT>(ta, tb, in[0][p], in[1][p], NIN > 2 ? in[2][p] : 0u, full);
+                    // the pair's inputs read again from the stage (still there),
+                    // so that the chunk's input registers are free here
+                    const uint32_t cj = roff[c];
+                    const uint64_t r = settle_pair<OP, ACT>(ta, tb, word_at(stage, cj, p),
+                                                            word_at(stage + tile_bytes_, cj, p),
+                                                            NIN > 2 ? word_at(stage + 2 * tile_bytes_, cj, p) : 0u, full);
                     o4[0][p] = static_cast<uint32_t>(r);
                     if constexpr (NOUT > 1) o4[1][p] = static_cast<uint32_t>(r >> 32);
                 }
