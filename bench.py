@@ -296,7 +296,15 @@ def measure_configs(mx, synthetic, peak: float, steps: int, warmup: int):
     before each launch.  Keys: workload/cell."""
     import torch
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    flush = flush_buf.zero_
+    clean_buf = torch.zeros(L2_FLUSH_BYTES // 2, dtype=torch.int32, device="cuda")
+    clean_out = torch.empty((), dtype=torch.int64, device="cuda")
+
+    def flush():
+        # write a buffer larger than L2, then read another one, so that the
+        # written lines are written back here and not inside the timed launch
+        flush_buf.zero_()
+        torch.sum(clean_buf, dim=0, dtype=torch.int64, out=clean_out)
+
     rows = {}
 
     def record(key, fn, nbytes):
@@ -333,7 +341,7 @@ def measure_configs(mx, synthetic, peak: float, steps: int, warmup: int):
         record("experts_E%d/quant3d_col" % E, lambda xe=xe, q=q, sc=sc: mx.quant_3d_colwise(xe, q, sc),
                quant3d_bytes(E, N, K))
         del q, sc
-    del x, flush_buf
+    del x, flush_buf, clean_buf
     torch.cuda.empty_cache()
     return rows
 
@@ -500,8 +508,9 @@ def main():
     if configs:
         line["configs"] = configs
         line["configs_note"] = ("each workload of the pages' shape list, one cell at a time: median of %d "
-                                "CUDA-event launch times, inputs resident, L2 flushed (512 MB write) "
-                                "before each launch; 3D = the first E experts of the seed-4 draw"
+                                "CUDA-event launch times, inputs resident, L2 flushed before each launch "
+                                "(a 512 MB write, then a 1 GB read so the written lines leave L2 outside "
+                                "the timed launch); 3D = the first E experts of the seed-4 draw"
                                 % args.config_steps)
     if cpu:
         line["cpu_baseline"] = cpu

@@ -315,7 +315,7 @@ mxfp8_status mxfp8_device_status(uint32_t *flags, uint64_t *fallbacks, int reset
  * (index g), the fp32 factors the kernels compute -- out[k*65536 + g] for
  * k = 0 sigmoid(g), 1 2^60 silu(g) (the forward's scaled form), 2 1 -
  * sigmoid(g), 3 1 + g(1 - sigmoid(g)), 4 silu'(g), 5 2^120 e^g (the factor of
- * the wide-range values the kernels use for gates below -64).  `out` is a
+ * the wide-range values the kernels use for gates below -16).  `out` is a
  * device buffer of 6 * 65536 floats, 16-byte aligned.  The tests compare these with the
  * exact factors: the error bounds they establish are the ones the fused
  * kernels' recomputation windows are sized for.
