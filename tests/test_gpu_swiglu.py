@@ -357,3 +357,31 @@ def test_fwd_with_h_writes_the_encoded_activation(mode):
     # the rowwise codes are the standalone cast of the h written
     q = O.quant_2d(h, O.ROWWISE)
     assert np.array_equal(u8(got.q_row), q["q_row"]) and np.array_equal(u8(got.s_row), q["s_row"])
+
+
+def test_fwd_with_h_ragged_rows_and_strided_h():
+    """h leaves through TMA tensor stores of whole tiles: ragged rows (M not a
+    multiple of the tile height), a ragged last column tile and an h row
+    pitch wider than N -- h equals the oracle's within the fast-path
+    tolerance, and nothing outside the (M, N) window of h is written."""
+    M, N, LD = 1000, 320, 384
+    gate, up, _ = rand_inputs(M, N, 37)
+    hbuf = torch.full((M * LD + 2 * 4096,), 0x5A5A, dtype=torch.int16, device="cuda")
+    hview = hbuf[4096:4096 + M * LD].view(M, LD)
+    q = torch.empty((M, N), dtype=torch.uint8, device="cuda")
+    s = torch.empty((M, N // 32), dtype=torch.uint8, device="cuda")
+    st = capi.mxfp8_swiglu_fwd_with_h(gate.data_ptr(), up.data_ptr(), gate.stride(0), M, N, 1,
+                                      hview.data_ptr(), LD, q.data_ptr(), N, s.data_ptr(), N // 32,
+                                      None, 0, None, 0, _stream())
+    assert st == 0, capi.STATUS_NAMES[st]
+    torch.cuda.synchronize()
+    hb = hbuf.cpu().numpy().view(np.uint16)
+    assert np.all(hb[:4096] == 0x5A5A) and np.all(hb[4096 + M * LD:] == 0x5A5A), "h written outside its buffer"
+    h = hb[4096:4096 + M * LD].reshape(M, LD)
+    assert np.all(h[:, N:] == 0x5A5A), "h written beyond column N"
+    want, h_want = O.swiglu_fwd(bits(gate), bits(up), 1)
+    diff = h[:, :N] != h_want
+    assert diff.sum() <= 1e-3 * M * N, diff.sum()
+    steps = np.abs(h[:, :N].astype(np.int32) - h_want.astype(np.int32))[diff]
+    assert np.all(steps == 1)
+    compare({"q_row": u8(q), "s_row": u8(s)}, want, what="fwd-with-h-ragged")
