@@ -137,7 +137,7 @@ static __device__ __noinline__ uint32_t near_bits_chunk(const uint8_t *stage, in
 // 64-bit result, so that calling it costs the common path nothing): the
 // pair's fast values evaluated again, then, element by element, the exact
 // (correctly rounded) value where the block is recomputed whole (`whole`: a
-// huge or non-finite value), where the gate lies outside the fast range (the
+// huge or infinite value), where the gate lies outside the fast range (the
 // exact path settles gates below it on its wide-range route) or where a fast
 // value lies near a 0x60/0x61 rounding midpoint; the fast value elsewhere.
 // w0, w1, w2: the pair's input words in the op's order (gate, up or dh,
@@ -188,7 +188,7 @@ __device__ __forceinline__ uint32_t word_at(const uint8_t *slot_base, uint32_t r
 // test of every value (near_mid2: a value within its window of a 0x60/0x61
 // rounding midpoint, where a scale byte could step); then, for the warps with
 // a lane whose block holds a flagged value, a gate outside the fast range or
-// a huge or non-finite amax, settle_pair on the flagged pairs (on every pair
+// a huge or infinite amax, settle_pair on the flagged pairs (on every pair
 // of a chunk holding such a gate, of a block with such an amax).  (Testing every value, rather than
 // only the blocks whose amax sits at that mantissa pair, also covers the
 // other direction's blocks in "both" mode, and measured cheaper than scanning
@@ -247,7 +247,7 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
     if constexpr (OP != kQuant) {
         bool full = false;
 #pragma unroll
-        for (int o = 0; o < NOUT; ++o) full |= amax[o] >= kHugeAmax;
+        for (int o = 0; o < NOUT; ++o) full |= huge_amax(amax[o]);
         if (__any_sync(0xFFFFFFFFu, near != 0u || dmin == 0u || full || farc != 0u)) {
             if constexpr (DIST && OP == kFwd) {
                 // which pairs: those near a midpoint (their fast values
@@ -258,7 +258,7 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
                 }
             }
             // every pair of a chunk holding a gate outside the fast range, of
-            // the whole block if a value is huge or not finite
+            // the whole block if a value is huge or infinite
 #pragma unroll
             for (int c = 0; c < 4; ++c) near |= ((farc >> c) & 1u) ? 0xFu << (4 * c) : 0u;
             if (full) near = 0xFFFFu;
@@ -284,7 +284,7 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
 
 // The same for the row pass of "both" mode, chunk by chunk: each chunk's
 // values are settled (settle_pair on its flagged pairs, or on all four if a
-// gate is outside the fast range or a value is huge or not finite -- the
+// gate is outside the fast range or a value is huge or infinite -- the
 // per-chunk form of the block rules, which is all they need) and written at
 // once over the chunk's inputs in the value slots, so only one chunk of
 // outputs lives in registers.  Returns the outputs' amax.
@@ -334,7 +334,7 @@ __device__ __forceinline__ void block_values_split(const KernelArgs &a, uint8_t 
 #pragma unroll
         for (int o = 0; o < NOUT; ++o) {
             cm[o] = hmax_abs2(hmax_abs2(o4[o][0], o4[o][1]), hmax_abs2(o4[o][2], o4[o][3]));
-            full |= (hmax_abs2(cm[o], __byte_perm(cm[o], 0, 0x1032)) & 0x7FFFu) >= kHugeAmax;
+            full |= huge_amax(hmax_abs2(cm[o], __byte_perm(cm[o], 0, 0x1032)) & 0x7FFFu);
         }
         if (__any_sync(0xFFFFFFFFu, near != 0u || far || full)) {
             if (full || far) near = 0xFu;
