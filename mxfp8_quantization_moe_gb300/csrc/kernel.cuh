@@ -138,8 +138,9 @@ static __device__ __noinline__ uint32_t near_bits_chunk(const uint8_t *stage, in
 // pair's fast values evaluated again, then, element by element, the exact
 // (correctly rounded) value where the block is recomputed whole (`whole`: a
 // huge or infinite value), where the gate lies outside the fast range (the
-// exact path settles gates below it on its wide-range route) or where a fast
-// value lies near a 0x60/0x61 rounding midpoint; the fast value elsewhere.
+// exact path settles gates below it on its wide-range route), where a fast
+// value is not finite or where it lies near a 0x60/0x61 rounding midpoint;
+// the fast value elsewhere.
 // w0, w1, w2: the pair's input words in the op's order (gate, up or dh,
 // gate, up); ta, tb: the activation's exact-path tables.  Returns the output
 // words (the second output's in the high half).
@@ -158,11 +159,11 @@ static __device__ __noinline__ uint64_t settle_pair(const void *ta, const void *
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const uint32_t gb = h ? gw >> 16 : gw & 0xFFFFu;
-        bool need = whole || far_gate<ACT>(gb);
+        bool need = whole || far_gate<ACT>(gb) || !isfinite(v0[h]);
         if constexpr (OP == kFwd)
             need |= near_mid1(v0[h], Gated<ACT>::kWinH);
         else
-            need |= near_mid1(v0[h], Gated<ACT>::kWinDgate) || near_mid1(v1[h], Gated<ACT>::kWinDup);
+            need |= !isfinite(v1[h]) || near_mid1(v0[h], Gated<ACT>::kWinDgate) || near_mid1(v1[h], Gated<ACT>::kWinDup);
         if (need) {
             const float x0 = h ? bf16hi(w0) : bf16lo(w0), x1 = h ? bf16hi(w1) : bf16lo(w1);
             if constexpr (OP == kFwd) {
@@ -188,8 +189,8 @@ __device__ __forceinline__ uint32_t word_at(const uint8_t *slot_base, uint32_t r
 // test of every value (near_mid2: a value within its window of a 0x60/0x61
 // rounding midpoint, where a scale byte could step); then, for the warps with
 // a lane whose block holds a flagged value, a gate outside the fast range or
-// a huge or infinite amax, settle_pair on the flagged pairs (on every pair
-// of a chunk holding such a gate, of a block with such an amax).  (Testing every value, rather than
+// a huge, infinite or NaN amax, settle_pair on the flagged pairs (on every
+// pair of a chunk holding such a gate, of a block with such an amax).  (Testing every value, rather than
 // only the blocks whose amax sits at that mantissa pair, also covers the
 // other direction's blocks in "both" mode, and measured cheaper than scanning
 // the risky blocks.)  DIST (forward only): the test keeps a running minimum
@@ -245,10 +246,13 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
 #pragma unroll
     for (int o = 0; o < NOUT; ++o) amax[o] = amax32_lane(out[o]);
     if constexpr (OP != kQuant) {
-        bool full = false;
+        bool full = false, nanb = false;
 #pragma unroll
-        for (int o = 0; o < NOUT; ++o) full |= huge_amax(amax[o]);
-        if (__any_sync(0xFFFFFFFFu, near != 0u || dmin == 0u || full || farc != 0u)) {
+        for (int o = 0; o < NOUT; ++o) {
+            full |= huge_amax(amax[o]);
+            nanb |= nan_amax(amax[o]);
+        }
+        if (__any_sync(0xFFFFFFFFu, near != 0u || dmin == 0u || full || nanb || farc != 0u)) {
             if constexpr (DIST && OP == kFwd) {
                 // which pairs: those near a midpoint (their fast values
                 // evaluated again), unless every pair is settled anyway
@@ -261,7 +265,7 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
             // the whole block if a value is huge or infinite
 #pragma unroll
             for (int c = 0; c < 4; ++c) near |= ((farc >> c) & 1u) ? 0xFu << (4 * c) : 0u;
-            if (full) near = 0xFFFFu;
+            if (full || nanb) near = 0xFFFFu;
             const void *ta = Gated<ACT>::table_a(a), *tb = Gated<ACT>::table_b(a);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -330,14 +334,16 @@ __device__ __forceinline__ void block_values_split(const KernelArgs &a, uint8_t 
             }
         }
         uint32_t cm[2];
-        bool full = false;
+        bool full = false, nanc = false;
 #pragma unroll
         for (int o = 0; o < NOUT; ++o) {
             cm[o] = hmax_abs2(hmax_abs2(o4[o][0], o4[o][1]), hmax_abs2(o4[o][2], o4[o][3]));
-            full |= huge_amax(hmax_abs2(cm[o], __byte_perm(cm[o], 0, 0x1032)) & 0x7FFFu);
+            const uint32_t m = hmax_abs2(cm[o], __byte_perm(cm[o], 0, 0x1032)) & 0x7FFFu;
+            full |= huge_amax(m);
+            nanc |= nan_amax(m);
         }
-        if (__any_sync(0xFFFFFFFFu, near != 0u || far || full)) {
-            if (full || far) near = 0xFu;
+        if (__any_sync(0xFFFFFFFFu, near != 0u || far || full || nanc)) {
+            if (full || far || nanc) near = 0xFu;
             const void *ta = Gated<ACT>::table_a(a), *tb = Gated<ACT>::table_b(a);
 #pragma unroll
             for (int p = 0; p < 4; ++p) {

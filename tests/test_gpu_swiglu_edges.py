@@ -250,3 +250,31 @@ def test_special_values_mixed_in(act):
         compare(du, wu, what="dup-specials")
     flags, _ = device_status()
     assert flags == 0
+
+
+@pytest.mark.parametrize("act", ACTS)
+def test_both_mode_overflowing_fast_value_in_a_nan_row_block(act):
+    """In "both" mode the column blocks are encoded from the row pass's
+    settled values.  A row block holding a genuine NaN (a NaN up) and a
+    value whose fast form overflows while the exact one is finite (the
+    largest bf16 gate times up = 1: about 3.4e38) is a NaN block either way,
+    but the finite value must still reach its column block exactly."""
+    rng = np.random.default_rng(21)
+    g = (rng.standard_normal((M, N)) * 2).astype(np.float32)
+    u = rng.standard_normal((M, N)).astype(np.float32)
+    dh = (rng.standard_normal((M, N)) * 0.05).astype(np.float32)
+    to16 = lambda x: torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    gv, uv, dv = to16(g), to16(u), to16(dh)
+    for k in range(8):
+        r, c = 32 * k + 5, 32 * k + 7           # one per row block and column block
+        gv[r, c], uv[r, c] = 0x7F7F, 0x3F80     # g = bf16 max, u = 1
+        gv[r, c + 9], uv[r, c + 9] = 0x0000, 0x7FC0   # same row block: 0 * NaN
+        dv[r, c] = 0x3F00                        # dh = 0.5
+    gate, up, dhd = to_dev(gv), to_dev(uv), to_dev(dv)
+    compare(fwd_gpu(gate, up, 3, act=act), oracle_fwd(gate, up, 3, act=act), what="fwd-both-overflow")
+    dg, du = bwd_gpu(dhd, gate, up, 3, act=act)
+    wg, wu = oracle_bwd(dhd, gate, up, 3, act=act)
+    compare(dg, wg, what="dgate-both-overflow")
+    compare(du, wu, what="dup-both-overflow")
+    flags, _ = device_status()
+    assert flags == 0
