@@ -407,16 +407,11 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     const int mode = s.mode & 3;
     const mx::LaunchShape shape = mx::launch_shape(s.op, mode);
     const int tm = shape.tile_rows;
-    CUtensorMap maps[4];   // the inputs (unused ones repeat the first), then h (or the first input again)
+    CUtensorMap maps[3];
     std::memset(maps, 0, sizeof(maps));
     for (int i = 0; i < 3; ++i) {
         const int src = i < nin ? i : 0;
         if (!make_bf16_map(&maps[i], s.in[src], s.M, s.N, s.ld_in[src], tm)) return MXFP8_ERR_ALIGN;
-    }
-    if (s.with_h) {
-        if (!make_bf16_map(&maps[3], s.h, s.M, s.N, s.ld_h, tm)) return MXFP8_ERR_ALIGN;
-    } else {
-        maps[3] = maps[0];
     }
     KernelArgs a;
     std::memset(&a, 0, sizeof(a));
@@ -441,6 +436,7 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     a.blocked = (s.mode & MXFP8_BLOCKED_SCALES) != 0;
     a.h_out = s.with_h ? s.h : nullptr;
     a.ld_h = s.ld_h;
+    a.wide_h = s.with_h && (reinterpret_cast<uintptr_t>(s.h) & 31u) == 0 && (s.ld_h * 2) % 32 == 0;
     a.srow_tiles_c = (s.N / 32 + 3) / 4;
     a.scol_tiles_c = (s.M / 32 + 3) / 4;
     if (a.blocked && s.group_end) {           // M-groups row scales, K-groups column scales

@@ -411,6 +411,22 @@ __device__ __forceinline__ void transpose_subtile(uint32_t slot, const uint32_t 
     __syncwarp();
 }
 
+// the lane's 32 bf16 values (16 words) to row `row`, columns c0..c0+31 of h
+__device__ __forceinline__ void store_h(const KernelArgs &a, const uint32_t (&v)[16], int64_t row, int64_t c0)
+{
+    uint16_t *dst = a.h_out + row * a.ld_h + c0;
+    if (a.wide_h) {
+        const uint32_t lo[8] = {v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]};
+        const uint32_t hi[8] = {v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15]};
+        st_global_v8(dst, lo);
+        st_global_v8(dst + 16, hi);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            __stcs(reinterpret_cast<uint4 *>(dst) + j, make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+    }
+}
+
 // encode the lane's block(s) and store the 32 codes at `q` (16-byte aligned;
 // one 256-bit store -- a whole sector -- when `wide` says 32-byte aligned);
 // returns the scale bytes in b[o]
@@ -585,8 +601,7 @@ template <int OP, int MODE, int TM, int STAGES, int CTAS, int G, int ACT, bool G
 __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
     mxfp8_tile_kernel(const __grid_constant__ CUtensorMap tm0,
                       const __grid_constant__ CUtensorMap tm1,
-                      const __grid_constant__ CUtensorMap tm2,
-                      const __grid_constant__ CUtensorMap tmh, const KernelArgs a)
+                      const __grid_constant__ CUtensorMap tm2, const KernelArgs a)
 {
     constexpr int NIN = OpTraits<OP>::kIn;
     constexpr int NOUT = OpTraits<OP>::kOut;
@@ -646,15 +661,10 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
     // warp writes the row scales of the tile that occupied it out of their
     // buffer (and those of the last tiles at the end).
     if (warp == kWarps) {
-        // the forward that also writes h: the consumers leave each tile's h
-        // in its stage's gate slot, and this warp stores it with TMA before
-        // the stage is refilled
-        const bool store_h = OP == kFwd && a.h_out != nullptr;
         if (lane == 0) {
             prefetch_tensormap(&tm0);
             if (NIN > 1) prefetch_tensormap(&tm1);
             if (NIN > 2) prefetch_tensormap(&tm2);
-            if (store_h) prefetch_tensormap(&tmh);
         }
         int it = 0;
         int ghint = 0;     // group of this lane's last row-scale lookup
@@ -679,19 +689,6 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
                     }
                 }
                 if (lane == 0) {
-                    if (store_h && it >= STAGES) {
-                        // the finished tile's h boxes of this part, out of the
-                        // gate slot before it is refilled
-#pragma unroll
-                        for (int x = 0; x < kBoxesPerPart; ++x) {
-                            const int box = h * kBoxesPerPart + x;
-                            tma_store_2d(&tmh, smem_base + static_cast<uint32_t>(s * NIN) * kTileBytes + box * kBoxBytes,
-                                         static_cast<int32_t>(done.tc() * kTileN) + box * kBoxN,
-                                         static_cast<int32_t>(done.tr * kTileM));
-                        }
-                        bulk_commit();
-                        bulk_wait_read();
-                    }
                     const int32_t r0 = static_cast<int32_t>(w.tr * kTileM);
                     const uint32_t bar = full0 + 8 * (2 * s + h);
                     mbar_expect_tx(bar, NIN * kBoxesPerPart * kBoxBytes);
@@ -743,14 +740,6 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
                 if (lane == 0) atomicOr(a.status, kStatusProducerWait);
                 break;
             }
-            if (store_h && lane == 0) {
-#pragma unroll
-                for (int box = 0; box < 2; ++box)
-                    tma_store_2d(&tmh, smem_base + static_cast<uint32_t>(s * NIN) * kTileBytes + box * kBoxBytes,
-                                 static_cast<int32_t>(done.tc() * kTileN) + box * kBoxN,
-                                 static_cast<int32_t>(done.tr * kTileM));
-                bulk_commit();
-            }
             if constexpr (MODE & kRow) {
                 if (done.last_in_group() || j + 1 == it)
                     flush_row_scales<NOUT, TM, G, GRP>(a, sbuf0 + done.gslot * NOUT * scale_group_bytes<TM, G>(), done.tr,
@@ -758,8 +747,6 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             }
             done.next();
         }
-        // every h store issued has completed before the CTA leaves
-        if (store_h && lane == 0) bulk_wait_all();
         return;
     }
 
@@ -823,15 +810,10 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
                 uint32_t out[2][16], amax[2];
                 block_values<OP, ACT, OP == kFwd && MODE == kBoth>(a, stage_ptr, kTileBytes, roff, out, amax);
                 if constexpr (OP == kFwd) {
-                    // the activation itself, for callers that keep it in bf16:
-                    // over the gate slot (no longer read), stored by the
-                    // producer warp with TMA
-                    if (a.h_out != nullptr) {
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            *reinterpret_cast<uint4 *>(const_cast<uint8_t *>(stage_ptr) + roff[c]) =
-                                make_uint4(out[0][4 * c], out[0][4 * c + 1], out[0][4 * c + 2], out[0][4 * c + 3]);
-                    }
+                    // the activation itself, for callers that keep it in bf16
+                    // (per-lane stores: staging it for a TMA store measured
+                    // slower, 1269 against 1253 us at 131072 x 8192)
+                    if (a.h_out != nullptr && live) store_h(a, out[0], grow, c0);
                 }
                 uint8_t *q[2];
 #pragma unroll
@@ -896,11 +878,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             }
         }
 
-        if constexpr (kWrites) {
-            fence_proxy_async_smem();
-        } else if constexpr (OP == kFwd) {
-            if (a.h_out != nullptr) fence_proxy_async_smem();   // h, read next by a TMA store
-        }
+        if constexpr (kWrites) fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * (2 * s + part));
     }

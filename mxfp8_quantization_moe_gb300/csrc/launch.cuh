@@ -10,7 +10,7 @@ namespace mx {
 // Launch mxfp8_tile_kernel<OP, MODE> on `grid` CTAs.  The dynamic shared
 // memory limit of the instantiation is raised once per device.
 template <int OP, int MODE, int ACT, bool GRP>
-cudaError_t launch_tiles(const CUtensorMap (&maps)[4], const KernelArgs &a, int grid,
+cudaError_t launch_tiles(const CUtensorMap (&maps)[3], const KernelArgs &a, int grid,
                          cudaStream_t stream, int device)
 {
     constexpr int kTM = Tuning<OP, MODE>::kTM;
@@ -30,8 +30,7 @@ cudaError_t launch_tiles(const CUtensorMap (&maps)[4], const KernelArgs &a, int 
         attr_done.fetch_or(bit, std::memory_order_acq_rel);
     }
     void *args[] = {const_cast<CUtensorMap *>(&maps[0]), const_cast<CUtensorMap *>(&maps[1]),
-                    const_cast<CUtensorMap *>(&maps[2]), const_cast<CUtensorMap *>(&maps[3]),
-                    const_cast<KernelArgs *>(&a)};
+                    const_cast<CUtensorMap *>(&maps[2]), const_cast<KernelArgs *>(&a)};
     return cudaLaunchKernel(reinterpret_cast<const void *>(kern), dim3(grid),
                             dim3((warps_of<kTM>() + 1) * 32), args, kSmem, stream);
 }
@@ -64,9 +63,9 @@ inline LaunchShape launch_shape(int op, int mode)
 // per-op (and activation) dispatch over the scale mode, one translation unit
 // each
 #define MX_DECLARE_LAUNCH(NAME)                                                                  \
-    cudaError_t NAME(int mode, const CUtensorMap (&maps)[4], const KernelArgs &a, int grid,      \
+    cudaError_t NAME(int mode, const CUtensorMap (&maps)[3], const KernelArgs &a, int grid,      \
                      cudaStream_t stream, int device);                                           \
-    cudaError_t NAME##_grouped(int mode, const CUtensorMap (&maps)[4], const KernelArgs &a,      \
+    cudaError_t NAME##_grouped(int mode, const CUtensorMap (&maps)[3], const KernelArgs &a,      \
                                int grid, cudaStream_t stream, int device);
 MX_DECLARE_LAUNCH(launch_quant)
 MX_DECLARE_LAUNCH(launch_fwd)
@@ -77,7 +76,7 @@ MX_DECLARE_LAUNCH(launch_bwd_gelu)
 
 // one translation unit per (op, activation) and per plain / grouped scales
 #define MX_DEFINE_LAUNCH(NAME, OP, ACT, GRP)                                                     \
-    cudaError_t NAME(int mode, const CUtensorMap (&maps)[4], const KernelArgs &a, int grid,      \
+    cudaError_t NAME(int mode, const CUtensorMap (&maps)[3], const KernelArgs &a, int grid,      \
                      cudaStream_t stream, int device)                                            \
     {                                                                                            \
         switch (mode) {                                                                          \
