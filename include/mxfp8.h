@@ -302,9 +302,11 @@ mxfp8_status mxfp8_geglu_bwd(const uint16_t *dh, int64_t ld_dh, const uint16_t *
  * pipeline wait that exceeds its limit (about a second) makes the kernel set
  * a flag bit and return.  flags: bit 0 consumer wait, bit 1 producer wait,
  * bit 2 drain wait, bit 3 self-test wait, bit 4 invalid group ends.
- * fallbacks: number of SwiGLU or GEGLU elements the fused kernels
- * recomputed exactly (values near a scale boundary, gates outside the fast
- * range, huge or non-finite blocks).
+ * fallbacks: number of SwiGLU or GEGLU elements the fused kernels sent
+ * through their rare path (both elements of every pair settled there: pairs
+ * holding a value near a scale boundary, a gate outside the fast range or a
+ * non-finite value, and every pair of a block with a huge amax); the rare
+ * path recomputes exactly the elements among them that need it.
  * Synchronizes `stream`; with reset != 0 clears both afterwards.
  * Either output pointer (host memory) may be NULL.
  */
