@@ -3,7 +3,7 @@ kernels, device.cuh): for t >= 0,
 
     Phi(-t) = exp(-t^2 / 2) * z * Q(z),   z = 1 / (1 + p t),
 
-with Q a polynomial of degree 6 whose coefficients minimise the largest
+with Q a polynomial of degree 7 whose coefficients minimise the largest
 relative error of z Q(z) against Phi(-t) exp(t^2 / 2) (the Mills ratio over
 sqrt(2 pi)) on t in [0, 8], on a dense grid: a least-squares start, then the
 minimax correction as a linear program (scaled so that the solver's
@@ -15,7 +15,7 @@ import numpy as np
 from scipy.optimize import linprog
 from scipy.special import log_ndtr
 
-DEGREE = 6
+DEGREE = 7
 T_MAX = 8.0
 
 
@@ -43,7 +43,7 @@ def fit(p, n=DEGREE):
 
 def main():
     best = None
-    for p in np.round(np.arange(0.22, 0.5, 0.005), 4):
+    for p in np.round(np.arange(0.22, 0.42, 0.005), 4):
         c, e = fit(float(np.float32(p)))
         if best is None or e < best[1]:
             best = (float(np.float32(p)), e, c)
