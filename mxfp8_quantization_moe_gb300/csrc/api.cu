@@ -32,6 +32,7 @@ __device__ double g_sig_table[65536];
 __device__ float2 g_sig2_table[65536];
 __device__ float4 g_gelu_table[65536];
 __device__ double2 g_gelu_dtable[65536];
+__device__ float2 g_gelu_tail[mx::kGeluTabN];
 __device__ unsigned g_status;
 __device__ unsigned long long g_fallbacks;
 
@@ -41,10 +42,19 @@ __device__ __forceinline__ float2 float_pair(double v)
     return make_float2(hi, __double2float_rn(__dadd_rn(v, -static_cast<double>(hi))));
 }
 
-__global__ void init_sigmoid_table_kernel(double *table, float2 *table2, float4 *gelu_table, double2 *gelu_dtable)
+__global__ void init_sigmoid_table_kernel(double *table, float2 *table2, float4 *gelu_table, double2 *gelu_dtable,
+                                          float2 *gelu_tail)
 {
     const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= 65536u) return;
+    if (i < static_cast<uint32_t>(mx::kGeluTabN)) {
+        // the GEGLU fast path's entry i: t = |g| of pattern kGeluTabLo + i - 1
+        // (entry 0: every t below the first, taken as 0)
+        const double t = i == 0 ? 0.0 : static_cast<double>(__uint_as_float((mx::kGeluTabLo + i - 1u) << 16));
+        const double q = t * exp(-0.5 * t * t) * 0.39894228040143267794;   // t phi(t)
+        gelu_tail[i] = make_float2(__double2float_rn(i == 0 ? 0.5 : mx::normal_cdf_double(-t)),
+                                   __double2float_rn(q));
+    }
     const float gf = __uint_as_float(i << 16);
     const double g = static_cast<double>(gf);
     const double s = mx::sigmoid_double(gf);  // 1 / (1 + e^-g)
@@ -90,19 +100,25 @@ __global__ void selftest_activation_kernel(float *out)
     }
 }
 
-// The GEGLU fast path's gate-only factors for every bf16 pattern g (pairs of
-// consecutive patterns per thread): Phi(g), gelu(g) = g Phi(g) as the forward
-// forms it (the product (g * 1) Phi), gelu'(g) = Phi(g) + g phi(g).
-__global__ void selftest_activation_gelu_kernel(float *out)
+// The GEGLU fast paths' gate-only factors for every bf16 pattern g (pairs of
+// consecutive patterns per thread), computed by the device functions the
+// tile kernels inline: out[k * 65536 + g] for k = 0 Phi(g), 1 gelu(g) =
+// g Phi(g) as the forward forms it (the product (g * 1) Phi), 2 gelu'(g) =
+// Phi(g) + g phi(g), from the tail table; 3 Phi(g) and 4 gelu'(g) from the
+// rational tail.
+__global__ void selftest_activation_gelu_kernel(float *out, const float2 *gelu_tail)
 {
+    mx::gelu_tail_fill<true>(gelu_tail);
+    mx::gelu_tail_fill<false>(gelu_tail);
+    __syncthreads();
     const uint32_t i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
     if (i >= 65536u) return;
     const uint32_t gw = i | ((i + 1) << 16);
-    uint64_t E, DG, DU;
-    const uint64_t P = mx::normal_cdf2(gw, E);
+    uint64_t E, DG, DU, DGP, DUP;
     mx::geglu_grads2(0x3F803F80u, gw, 0x3F803F80u, DG, DU);     // dh = u = 1: DG = gelu'(g)
-    const uint64_t V[3] = {P, mx::geglu_h2(gw, 0x3F803F80u), DG};
-    for (int k = 0; k < 3; ++k) {
+    mx::geglu_grads2_poly(0x3F803F80u, gw, 0x3F803F80u, DGP, DUP);
+    const uint64_t V[5] = {mx::normal_cdf2(gw), mx::geglu_h2(gw, 0x3F803F80u), DG, mx::normal_cdf2_poly(gw, E), DGP};
+    for (int k = 0; k < 5; ++k) {
         out[k * 65536 + i] = mx::f2lo(V[k]);
         out[k * 65536 + i + 1] = mx::f2hi(V[k]);
     }
@@ -116,6 +132,7 @@ struct DeviceState {
     float2 *table2 = nullptr;
     float4 *gelu_table = nullptr;
     double2 *gelu_dtable = nullptr;
+    float2 *gelu_tail = nullptr;
     unsigned *status = nullptr;
     unsigned long long *fallbacks = nullptr;
     int sms = 0;
@@ -155,11 +172,13 @@ mxfp8_status ensure_device(cudaStream_t stream, int *dev_out, DeviceState **stat
     d.gelu_table = static_cast<float4 *>(p);
     if (cudaGetSymbolAddress(&p, g_gelu_dtable) != cudaSuccess) return MXFP8_ERR_DEVICE;
     d.gelu_dtable = static_cast<double2 *>(p);
+    if (cudaGetSymbolAddress(&p, g_gelu_tail) != cudaSuccess) return MXFP8_ERR_DEVICE;
+    d.gelu_tail = static_cast<float2 *>(p);
     if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return MXFP8_ERR_DEVICE;
     d.status = static_cast<unsigned *>(p);
     if (cudaGetSymbolAddress(&p, g_fallbacks) != cudaSuccess) return MXFP8_ERR_DEVICE;
     d.fallbacks = static_cast<unsigned long long *>(p);
-    init_sigmoid_table_kernel<<<256, 256, 0, stream>>>(d.table, d.table2, d.gelu_table, d.gelu_dtable);
+    init_sigmoid_table_kernel<<<256, 256, 0, stream>>>(d.table, d.table2, d.gelu_table, d.gelu_dtable, d.gelu_tail);
     if (cudaGetLastError() != cudaSuccess) return MXFP8_ERR_DEVICE;
     if (cudaMemsetAsync(d.status, 0, sizeof(unsigned), stream) != cudaSuccess ||
         cudaMemsetAsync(d.fallbacks, 0, sizeof(unsigned long long), stream) != cudaSuccess)
@@ -468,6 +487,7 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     a.sig2_table = d->table2;
     a.gelu_table = d->gelu_table;
     a.gelu_dtable = d->gelu_dtable;
+    a.gelu_tail = d->gelu_tail;
     a.status = d->status;
     a.fallbacks = d->fallbacks;
     a.wait_limit = d->wait_limit;
@@ -815,7 +835,7 @@ mxfp8_status mxfp8_selftest_activation_gelu(float *out, void *stream)
     DeviceState *d;
     mxfp8_status r = ensure_device(st, &dev, &d);
     if (r != MXFP8_OK) return r;
-    selftest_activation_gelu_kernel<<<128, 256, 0, st>>>(out);
+    selftest_activation_gelu_kernel<<<128, 256, 0, st>>>(out, d->gelu_tail);
     return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
 }
 
@@ -947,6 +967,7 @@ extern "C" mxfp8_status mxfp8_swiglu_fwd_noalloc(const uint16_t *gate, const uin
     a.sig2_table = d->table2;
     a.gelu_table = d->gelu_table;
     a.gelu_dtable = d->gelu_dtable;
+    a.gelu_tail = d->gelu_tail;
     a.fallbacks = d->fallbacks;
     a.status = d->status;
     const int64_t chunks = M * ((N + 7) / 8);

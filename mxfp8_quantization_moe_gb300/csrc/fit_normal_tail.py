@@ -1,10 +1,11 @@
-"""Fit of the normal tail used by the GEGLU fast path (gated-activation
-kernels, device.cuh): for t >= 0,
+"""Fit of the rational normal tail used by GEGLU's second fast path (the
+backward's row and column modes of the gated-activation kernels,
+device.cuh): for t >= 0,
 
-    Phi(-t) = exp(-t^2 / 2) * z * Q(z),   z = 1 / (1 + p t),
+    Phi(-t) = exp(-t^2 / 2) * z * R(z),   z = 1 / (1 + p t),
 
-with Q a polynomial of degree 7 whose coefficients minimise the largest
-relative error of z Q(z) against Phi(-t) exp(t^2 / 2) (the Mills ratio over
+with R a polynomial of degree 7 whose coefficients minimise the largest
+relative error of z R(z) against Phi(-t) exp(t^2 / 2) (the Mills ratio over
 sqrt(2 pi)) on t in [0, 8], on a dense grid: a least-squares start, then the
 minimax correction as a linear program (scaled so that the solver's
 tolerances sit far below the error), p chosen by a scan.  Prints the constants for device.cuh (rounded to fp32).
@@ -48,10 +49,10 @@ def main():
         if best is None or e < best[1]:
             best = (float(np.float32(p)), e, c)
     p, e, c = best
-    print("// p = %.9g, max relative error of z Q(z) on [0, %g]: %.3g (%.2f units of 2^-24)"
+    print("// p = %.9g, max relative error of z R(z) on [0, %g]: %.3g (%.2f units of 2^-24)"
           % (p, T_MAX, e, e / 2.0 ** -24))
     print("constexpr float kTailP = %.9gf;" % p)
-    print("constexpr float kTailQ[%d] = {%s};" % (len(c), ", ".join("%.9gf" % np.float32(v) for v in c)))
+    print("constexpr float kTailR[%d] = {%s};" % (len(c), ", ".join("%.9gf" % np.float32(v) for v in c)))
 
 
 if __name__ == "__main__":

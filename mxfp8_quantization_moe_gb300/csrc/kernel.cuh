@@ -74,6 +74,24 @@ MX_TUNE(kBwd, kCol, 96, 3, 1, 1)
 MX_TUNE(kBwd, kBoth, 128, 2, 1, 2)
 #undef MX_TUNE
 
+// The activation policy a kernel evaluates: GEGLU's tail table for the
+// forward and the backward's "both" mode, its rational tail for the
+// backward's row and column modes (three stages of 96-row tiles leave no
+// room for the table there; two stages measured 11-14 % slower).
+template <int OP, int MODE, int ACT>
+constexpr int policy_of()
+{
+    return (ACT == kGelu && OP == kBwd && MODE != kBoth) ? kGeluPoly : ACT;
+}
+
+// static shared memory of the policy's kernels: the tail table (L alone for
+// the forward, (L, Q) pairs for the backward)
+template <int OP, int POL>
+constexpr size_t static_smem_bytes()
+{
+    return POL != kGelu ? 0 : (OP == kFwd ? sizeof(float) : sizeof(float2)) * kGeluTabN;
+}
+
 template <int TM>
 __host__ __device__ constexpr int warps_of() { return (TM / kSub) * (kTileN / kSub); }
 
@@ -651,6 +669,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             }
         }
     }
+    if constexpr (ACT == kGelu && OP != kQuant) gelu_tail_fill<OP == kFwd>(a.gelu_tail);
     __syncthreads();
 
     const int64_t tiles_n = a.tiles_n;

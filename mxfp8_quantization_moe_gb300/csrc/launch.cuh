@@ -7,8 +7,9 @@
 
 namespace mx {
 
-// Launch mxfp8_tile_kernel<OP, MODE> on `grid` CTAs.  The dynamic shared
-// memory limit of the instantiation is raised once per device.
+// Launch mxfp8_tile_kernel<OP, MODE> (activation ACT, evaluated by the
+// policy policy_of picks) on `grid` CTAs.  The dynamic shared memory limit of
+// the instantiation is raised once per device.
 template <int OP, int MODE, int ACT, bool GRP>
 cudaError_t launch_tiles(const CUtensorMap (&maps)[3], const KernelArgs &a, int grid,
                          cudaStream_t stream, int device)
@@ -17,10 +18,12 @@ cudaError_t launch_tiles(const CUtensorMap (&maps)[3], const KernelArgs &a, int 
     constexpr int kStages = Tuning<OP, MODE>::kStages;
     constexpr int kCtas = Tuning<OP, MODE>::kCtas;
     constexpr int kGroup = Tuning<OP, MODE>::kGroup;
+    constexpr int kPol = policy_of<OP, MODE, ACT>();
     constexpr size_t kSmem = smem_bytes<OP, kTM, kStages, kGroup, GRP>();
-    static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
-    static_assert(kCtas * (kSmem + 1024) <= 228 * 1024, "shared memory per SM");
-    auto kern = mxfp8_tile_kernel<OP, MODE, kTM, kStages, kCtas, kGroup, ACT, GRP>;
+    constexpr size_t kStatic = static_smem_bytes<OP, kPol>();
+    static_assert(kSmem + kStatic <= 227 * 1024, "shared memory per CTA");
+    static_assert(kCtas * (kSmem + kStatic + 1024) <= 228 * 1024, "shared memory per SM");
+    auto kern = mxfp8_tile_kernel<OP, MODE, kTM, kStages, kCtas, kGroup, kPol, GRP>;
     static std::atomic<unsigned long long> attr_done{0};
     const unsigned long long bit = 1ull << (device & 63);
     if (!(attr_done.load(std::memory_order_acquire) & bit)) {

@@ -19,30 +19,35 @@ pytestmark = pytest.mark.gpu
 
 
 def test_gelu_fast_path_error_bounds_for_every_gate():
+    """Both fast paths: the tail table (forward, backward "both"; fast range
+    g >= -6) and the rational tail (backward row and column; g >= -8)."""
     init()
-    out = torch.empty(3 * 65536, dtype=torch.float32, device="cuda")
+    out = torch.empty(5 * 65536, dtype=torch.float32, device="cuda")
     assert capi.mxfp8_selftest_activation_gelu(out.data_ptr(), torch.cuda.current_stream().cuda_stream) == 0
     torch.cuda.synchronize()
-    v = out.view(3, 65536).cpu().numpy().astype(np.float64)
+    v = out.view(5, 65536).cpu().numpy().astype(np.float64)
     g = (np.arange(65536, dtype=np.uint64) << 16).astype(np.uint32).view(np.float32).astype(np.float64)
-    fast = np.isfinite(g) & (g >= -8.0) & (np.abs(g) < 2.0 ** 100)
-    gf = g[fast]
-    p = np.array([O.normal_cdf(float(x)) for x in gf])
-    d = np.array([O.geglu_grads_f64(1.0, float(x), 1.0)[0] for x in gf])
-    gelu = gf * p
+    sane = np.isfinite(g) & (np.abs(g) < 2.0 ** 100)
+    p = np.full(65536, np.nan)
+    d = np.full(65536, np.nan)
+    p[sane] = [O.normal_cdf(float(x)) for x in g[sane]]
+    d[sane] = [O.geglu_grads_f64(1.0, float(x), 1.0)[0] for x in g[sane]]
 
     def rel(a, b):
         with np.errstate(divide="ignore", invalid="ignore"):
             r = np.abs(a - b) / np.abs(b)
         r[(a == b)] = 0.0
-        return r
+        return r / 2.0 ** -24
 
-    u = 2.0 ** -24
-    # the kernels' midpoint windows are 64, 64 and 1024 fp32 ulps: an error of
-    # e units of 2^-24 is e * 1.75 / 2 ulps at the 0x60|0x61 midpoint mantissa,
-    # plus half an ulp for the multiply by the exact product of inputs
-    errs = {"Phi": (rel(v[0][fast], p) / u, 32), "gelu": (rel(v[1][fast], gelu) / u, 32),
-            "gelu'": (rel(v[2][fast], d) / u, 768)}
+    # the kernels' midpoint windows: 64, 64 and 512 fp32 ulps (table), 64 and
+    # 1024 (rational tail); an error of e units of 2^-24 is e * 1.75 / 2 ulps
+    # at the 0x60|0x61 midpoint mantissa, plus half an ulp for the multiply by
+    # the exact product of inputs
+    tab = sane & (g >= -6.0)
+    poly = sane & (g >= -8.0)
+    errs = {"Phi": (rel(v[0][tab], p[tab]), 16), "gelu": (rel(v[1][tab], g[tab] * p[tab]), 16),
+            "gelu'": (rel(v[2][tab], d[tab]), 256),
+            "Phi (rational)": (rel(v[3][poly], p[poly]), 32), "gelu' (rational)": (rel(v[4][poly], d[poly]), 768)}
     print("max GELU fast-path relative error (units of 2^-24): " +
           ", ".join("%s %.2f" % (k, e.max()) for k, (e, _) in errs.items()))
     for k, (e, bound) in errs.items():
