@@ -467,94 +467,117 @@ __device__ __forceinline__ void store_codes(const uint32_t (&out)[2][16], const 
     }
 }
 
-// flush_row_scales (below) in the per-group blocked layouts: lane j finds the
-// row shift of the band's 32-row block j, handed round while the warp walks
-// the blocks.  Writes nothing if the group ends were found invalid.
-template <int NOUT, int TM, int G>
-__device__ __forceinline__ void flush_row_scales_grouped(const KernelArgs &a, const uint8_t *gbuf, int64_t row0,
-                                                      int64_t blk0, int gsize, int lane, const int32_t *gtab,
-                                                      int &hint)
+// The lane's row-scale words of one column tile (NB consecutive 32-row
+// blocks: rows r0 + lane + 32 j) in the blocked layout, where the rows of a
+// 128-row tile that share r % 32 fill one 16-byte chunk, word (r / 32) % 4:
+// the words of consecutive blocks inside one tile go out as one store.  K0 =
+// (r0 / 32) % 4; `chunk` is the lane's chunk in the first tile, `stride` the
+// bytes between vertically adjacent tiles.
+template <int K0, int NB>
+__device__ __forceinline__ void store_blocked_words(uint8_t *chunk, int64_t stride, const uint32_t (&w)[NB])
 {
-    constexpr int kBlocks = TM / 32;
-    if (a.group_end != nullptr && gtab[3 * kMaxGroups] == 0) return;
-    const int64_t brow0 = row0 + 32 * lane;
-    const int32_t mine =
-        (lane < kBlocks && brow0 < a.M) ? static_cast<int32_t>(group_shift(a, gtab, brow0, hint).r) : 0;
 #pragma unroll
-    for (int j = 0; j < kBlocks; ++j) {
-        const int32_t rsh = __shfl_sync(0xFFFFFFFFu, mine, j);
-        const int i = lane + 32 * j;
-        const int64_t row = row0 + i;
-        if (row >= a.M) continue;
+    for (int p0 = 0; p0 < K0 + NB; p0 += 4) {          // each 128-row tile the band touches
+        const int lo = p0 > K0 ? p0 : K0, hi = p0 + 4 < K0 + NB ? p0 + 4 : K0 + NB;
+        uint8_t *dst = chunk + (p0 >> 2) * stride + 4 * (lo - p0);
+        const uint32_t *v = w + (lo - K0);
+        if (hi - lo == 4) {
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(v[0], v[1], v[2], v[3]);
+        } else if (hi - lo == 2 && (lo & 1) == 0) {
+            *reinterpret_cast<uint2 *>(dst) = make_uint2(v[0], v[1]);
+        } else {
+            for (int q = 0; q < hi - lo; ++q) reinterpret_cast<uint32_t *>(dst)[q] = v[q];
+        }
+    }
+}
+
+// Row scales of a whole band (rows r0 .. r0 + TM - 1 after any group shift,
+// r0 a multiple of 32) in the blocked layout, for the group's gsize column
+// tiles: per tile and output, the lane reads its TM / 32 words from the
+// group's buffer and stores them chunk by chunk (s_row 16-byte aligned).
+template <int NOUT, int TM, int G>
+__device__ __forceinline__ void flush_blocked_band(const KernelArgs &a, const uint8_t *gbuf, int64_t r0,
+                                                   int64_t blk0, int gsize, int lane)
+{
+    constexpr int NB = TM / 32;
+    const int k0 = static_cast<int>((r0 >> 5) & 3);
+    const int64_t stride = a.srow_tiles_c * 512;
+    for (int t = 0; t < gsize; ++t) {
 #pragma unroll
         for (int o = 0; o < NOUT; ++o) {
-            const uint8_t *src = gbuf + o * scale_group_bytes<TM, G>() + 4 * G * i;
-            for (int t = 0; t < gsize; ++t)
-                *reinterpret_cast<uint32_t *>(a.s_row[o] + blocked_offset(row + rsh, blk0 + 4 * t, a.srow_tiles_c)) =
-                    *reinterpret_cast<const uint32_t *>(src + 4 * t);
+            const uint8_t *src = gbuf + o * scale_group_bytes<TM, G>() + 4 * G * lane + 4 * t;
+            uint32_t w[NB];
+#pragma unroll
+            for (int j = 0; j < NB; ++j) w[j] = *reinterpret_cast<const uint32_t *>(src + 4 * G * 32 * j);
+            uint8_t *chunk = a.s_row[o] + ((r0 >> 7) * a.srow_tiles_c + (blk0 >> 2) + t) * 512 + 16 * lane;
+            switch (k0) {
+            case 0: store_blocked_words<0, NB>(chunk, stride, w); break;
+            case 1: store_blocked_words<1, NB>(chunk, stride, w); break;
+            case 2: store_blocked_words<2, NB>(chunk, stride, w); break;
+            default: store_blocked_words<3, NB>(chunk, stride, w); break;
+            }
         }
     }
 }
 
 // Row scales of one finished group of column tiles (tiles 0..gsize-1 of group
 // ug in row band tr), from its shared-memory buffer (4 G bytes a row) to s_row,
-// by the whole producer warp: one 4G-byte store per row where the group is
-// whole and rows are aligned (`wide`), 4-byte stores or single bytes
-// otherwise.
+// by the whole producer warp.  Row-major: one 4G-byte store per row where the
+// group is whole and rows are aligned (`wide`), single bytes otherwise.
+// Blocked (plain, per group or per expert): whole bands whose 32-row blocks
+// share one group shift go out chunk by chunk (flush_blocked_band); a ragged
+// last band, or one that a group boundary with a new shift crosses, row by
+// row.  The per-group layouts write nothing if the group ends were found
+// invalid.  (The producer issues the next tile's loads only after this, so
+// its instruction count bounds how far it can run ahead.)
 template <int NOUT, int TM, int G, bool GRP>
 __device__ __forceinline__ void flush_row_scales(const KernelArgs &a, const uint8_t *gbuf, int64_t tr, int64_t ug,
                                                  int gsize, int lane, const int32_t *gtab, int &hint)
 {
+    constexpr int kBlocks = TM / 32;
     const int64_t row0 = tr * TM;
     const int64_t blk0 = ug * 4 * G;
     const int64_t nblk = a.N >> 5;
-    if constexpr (GRP) {
-        flush_row_scales_grouped<NOUT, TM, G>(a, gbuf, row0, blk0, gsize, lane, gtab, hint);
+    if (GRP || a.blocked) {
+        int32_t mine = 0;     // lane j < kBlocks: the row shift of the band's block j
+        bool band = row0 + TM <= a.M;
+#pragma unroll
+        for (int o = 0; o < NOUT; ++o) band &= (reinterpret_cast<uintptr_t>(a.s_row[o]) & 15u) == 0;
+        if constexpr (GRP) {
+            if (a.group_end != nullptr && gtab[3 * kMaxGroups] == 0) return;
+            const int64_t brow0 = row0 + 32 * lane;
+            mine = (lane < kBlocks && brow0 < a.M) ? static_cast<int32_t>(group_shift(a, gtab, brow0, hint).r) : 0;
+        }
+        const int32_t rsh0 = __shfl_sync(0xFFFFFFFFu, mine, 0);
+        if (__all_sync(0xFFFFFFFFu, band && (lane >= kBlocks || mine == rsh0))) {
+            flush_blocked_band<NOUT, TM, G>(a, gbuf, row0 + rsh0, blk0, gsize, lane);
+            return;
+        }
+#pragma unroll
+        for (int j = 0; j < kBlocks; ++j) {
+            const int32_t rsh = __shfl_sync(0xFFFFFFFFu, mine, j);
+            const int i = lane + 32 * j;
+            const int64_t row = row0 + i;
+            if (row >= a.M) continue;
+#pragma unroll
+            for (int o = 0; o < NOUT; ++o) {
+                const uint8_t *src = gbuf + o * scale_group_bytes<TM, G>() + 4 * G * i;
+                // a tile's four blocks of a row are contiguous in the blocked
+                // layout (padding blocks of the last tile come out as 0)
+                for (int t = 0; t < gsize; ++t)
+                    *reinterpret_cast<uint32_t *>(a.s_row[o] + blocked_offset(row + rsh, blk0 + 4 * t, a.srow_tiles_c)) =
+                        *reinterpret_cast<const uint32_t *>(src + 4 * t);
+            }
+        }
         return;
     }
     const bool whole = a.wide_srow != 0 && gsize == G && blk0 + 4 * G <= nblk;
-    if constexpr (TM % 128 == 0) {
-        // bands of whole 128-row tiles: a lane's rows r, r + 32, r + 64,
-        // r + 96 fill one 16-byte chunk of a 128 x 4 tile -- one store per
-        // tile, where every row is inside the matrix and the buffers are
-        // 16-byte aligned (the layout itself only needs 4)
-        bool al16 = true;
-#pragma unroll
-        for (int o = 0; o < NOUT; ++o) al16 &= (reinterpret_cast<uintptr_t>(a.s_row[o]) & 15u) == 0;
-        if (a.blocked && al16 && row0 + TM <= a.M) {
-#pragma unroll
-            for (int q = 0; q < TM / 128; ++q) {
-                const int i0 = 128 * q + lane;
-#pragma unroll
-                for (int o = 0; o < NOUT; ++o) {
-                    const uint8_t *src = gbuf + o * scale_group_bytes<TM, G>() + 4 * G * i0;
-                    for (int t = 0; t < gsize; ++t) {
-                        uint4 v;
-                        v.x = *reinterpret_cast<const uint32_t *>(src + 4 * t);
-                        v.y = *reinterpret_cast<const uint32_t *>(src + 4 * G * 32 + 4 * t);
-                        v.z = *reinterpret_cast<const uint32_t *>(src + 4 * G * 64 + 4 * t);
-                        v.w = *reinterpret_cast<const uint32_t *>(src + 4 * G * 96 + 4 * t);
-                        *reinterpret_cast<uint4 *>(a.s_row[o] + blocked_offset(row0 + i0, blk0 + 4 * t, a.srow_tiles_c)) = v;
-                    }
-                }
-            }
-            return;
-        }
-    }
     for (int i = lane; i < TM; i += 32) {
         const int64_t row = row0 + i;
         if (row >= a.M) break;
 #pragma unroll
         for (int o = 0; o < NOUT; ++o) {
             const uint8_t *src = gbuf + o * scale_group_bytes<TM, G>() + 4 * G * i;
-            if (a.blocked) {
-                // a tile's four blocks of a row are contiguous in the blocked
-                // layout (padding blocks of the last tile come out as 0)
-                for (int t = 0; t < gsize; ++t)
-                    *reinterpret_cast<uint32_t *>(a.s_row[o] + blocked_offset(row, blk0 + 4 * t, a.srow_tiles_c)) =
-                        *reinterpret_cast<const uint32_t *>(src + 4 * t);
-                continue;
-            }
             uint8_t *dst = a.s_row[o] + row * a.ld_srow + blk0;
             if (whole) {
                 if constexpr (G == 4)
