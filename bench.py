@@ -49,16 +49,17 @@ PAGES_US = {("fwd", 1): 904.19, ("fwd", 2): 1022.98, ("fwd", 3): 1216.08,
 # held in L2 when the captured kernel ends does not scale with the size, so the
 # full-size figure slightly understates the real traffic.
 TRAFFIC = {
-    "bwd_both": (10.5487e9, "8f4c355c349c31d3"),
-    "bwd_both_gelu": (10.5502e9, "8f4c355c349c31d3"),
-    "bwd_col": (8.4511e9, "8f4c355c349c31d3"),
-    "bwd_row": (8.4546e9, "8f4c355c349c31d3"),
-    "fwd_both": (6.24343e9, "8f4c355c349c31d3"),
-    "fwd_col": (5.25023e9, "8f4c355c349c31d3"),
-    "fwd_row": (5.24218e9, "8f4c355c349c31d3"),
-    "fwd_row_gelu": (5.24924e9, "8f4c355c349c31d3"),
-    "quant3d": (7.86352e9, "8f4c355c349c31d3"),
-    "quant_both": (3.98482e9, "8f4c355c349c31d3"),
+    "bwd_both": (10.5501e9, "7ff130f67ada9f06"),
+    "bwd_both_gelu": (10.5527e9, "7ff130f67ada9f06"),
+    "bwd_col": (8.44839e9, "7ff130f67ada9f06"),
+    "bwd_row": (8.45383e9, "7ff130f67ada9f06"),
+    "fwd_both": (6.24262e9, "7ff130f67ada9f06"),
+    "fwd_col": (5.24911e9, "7ff130f67ada9f06"),
+    "fwd_row": (5.24271e9, "7ff130f67ada9f06"),
+    "fwd_row_gelu": (5.24513e9, "7ff130f67ada9f06"),
+    "quant3d": (7.8657e9, "7ff130f67ada9f06"),
+    "quant_both": (3.98872e9, "7ff130f67ada9f06"),
+    "quant_row": (3.00036e9, "7ff130f67ada9f06"),
 }
 TRAFFIC_KIND = ("estimate: ncu dram__bytes_read.sum + dram__bytes_write.sum of a 16384-row launch "
                 "scaled x8 to the full size; L2-resident write-back at kernel end does not scale")
