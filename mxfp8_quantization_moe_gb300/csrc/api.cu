@@ -438,6 +438,9 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     a.N = s.N;
     a.tiles_n = (s.N + mx::kTileN - 1) / mx::kTileN;
     a.num_tiles = ((s.M + tm - 1) / tm) * a.tiles_n;
+    // the kernels walk tiles with 32-bit counters (and TMA takes 32-bit
+    // coordinates): a tile count past that is out of range
+    if (a.num_tiles > 0x7FFFFFFFLL - 4096) return MXFP8_ERR_SHAPE;
     for (int o = 0; o < 2; ++o) {
         a.q_row[o] = s.q_row[o];
         a.s_row[o] = s.s_row[o];

@@ -598,23 +598,25 @@ __device__ __forceinline__ void flush_row_scales(const KernelArgs &a, const uint
 // of a row band ("super-tiles" u = blockIdx.x, + gridDim.x, ...), tile by
 // tile; the walk keeps the row band tr, the group ug, the tile i within it,
 // the pipeline slot (stage, phase parity) and the group's row-scale buffer
-// slot (group ordinal % (STAGES + 1)), advanced without divisions.
+// slot (group ordinal % (STAGES + 1)), advanced without divisions.  32-bit
+// counters (the host rejects tile counts that do not fit): they are live
+// across the whole tile loop, so every register they save counts.
 template <int STAGES, int G>
 struct TileWalk {
-    int64_t u, tr, ug, step_r, step_c, tiles_g, tiles_n;
+    int32_t u, tr, ug, step_r, step_c, tiles_g, tiles_n;
     int i, gsize, s, gslot;
     uint32_t ph;
     __device__ __forceinline__ explicit TileWalk(int64_t n_tiles_n)
-        : u(blockIdx.x), tiles_n(n_tiles_n), i(0), s(0), gslot(0), ph(0)
+        : u(static_cast<int32_t>(blockIdx.x)), tiles_n(static_cast<int32_t>(n_tiles_n)), i(0), s(0), gslot(0), ph(0)
     {
         tiles_g = (tiles_n + G - 1) / G;
         tr = u / tiles_g;
         ug = u - tr * tiles_g;
-        step_r = static_cast<int64_t>(gridDim.x) / tiles_g;
-        step_c = static_cast<int64_t>(gridDim.x) - step_r * tiles_g;
-        gsize = static_cast<int>(min(static_cast<int64_t>(G), tiles_n - ug * G));
+        step_r = static_cast<int32_t>(gridDim.x) / tiles_g;
+        step_c = static_cast<int32_t>(gridDim.x) - step_r * tiles_g;
+        gsize = min(G, tiles_n - ug * G);
     }
-    __device__ __forceinline__ int64_t tc() const { return ug * G + i; }
+    __device__ __forceinline__ int64_t tc() const { return static_cast<int64_t>(ug) * G + i; }
     __device__ __forceinline__ bool last_in_group() const { return i + 1 == gsize; }
     __device__ __forceinline__ void next()
     {
@@ -627,7 +629,7 @@ struct TileWalk {
                 ug -= tiles_g;
                 ++tr;
             }
-            gsize = static_cast<int>(min(static_cast<int64_t>(G), tiles_n - ug * G));
+            gsize = min(G, tiles_n - ug * G);
             if (++gslot == STAGES + 1) gslot = 0;
         }
         if (++s == STAGES) {
@@ -684,6 +686,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
         fence_proxy_async_smem();
     }
     if constexpr (GRP) {
+        if (lane == 0) gtab[kGroupHintWord + warp] = 0;
         if (a.group_end != nullptr && warp == 0) {
             const bool ok = build_group_table(a.group_end, a.num_groups, a.M, gtab, lane);
             if (lane == 0) {
@@ -731,7 +734,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
                     }
                 }
                 if (lane == 0) {
-                    const int32_t r0 = static_cast<int32_t>(w.tr * kTileM);
+                    const int32_t r0 = w.tr * kTileM;
                     const uint32_t bar = full0 + 8 * (2 * s + h);
                     mbar_expect_tx(bar, NIN * kBoxesPerPart * kBoxBytes);
 #pragma unroll
@@ -811,8 +814,15 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
                                   chunk0 + (static_cast<uint32_t>(lane) >> 3));
 
     constexpr bool kSplit = (MODE == kBoth) && (OP != kQuant);  // values handed row -> col pass
+    // the forward's col mode evaluates h row by row (lanes own rows, as in
+    // the row pass) into the up slot and transposes that one slot, rather
+    // than transposing gate and up and evaluating column by column: fewer
+    // shared-memory round trips (measured faster for the forward, SwiGLU
+    // 825 -> 809 us and GEGLU 1002 -> 943 at 131072 x 8192, and slower for
+    // the backward, 1362 -> 1462 us, and for the per-group forward, 879 ->
+    // 934 us)
+    constexpr bool kVF = (MODE == kCol) && (OP == kFwd) && !GRP;
     constexpr bool kWrites = kSplit || (MODE & kCol);           // generic writes into the stage
-    int chint = 0;   // group of this warp's last column-scale lookup
     for (TileWalk<STAGES, G> w(tiles_n); w.u < num_super; w.next()) {
         const int s = w.s;
         const uint32_t part = kParts == 2 ? (scb >> 1) : 0u;     // the half this warp reads
@@ -821,7 +831,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             if (lane == 0) atomicOr(a.status, kStatusConsumerWait);
             return;
         }
-        const int64_t r0 = w.tr * kTileM + kSub * srb;   // sub-tile origin
+        const int64_t r0 = static_cast<int64_t>(w.tr) * kTileM + kSub * srb;   // sub-tile origin
         const int64_t c0 = w.tc() * kTileN + kSub * scb;
         const uint32_t stage = smem_base + static_cast<uint32_t>(s * NIN) * kTileBytes;
         const uint8_t *stage_ptr = smem + static_cast<size_t>(s * NIN) * kTileBytes;
@@ -881,16 +891,26 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
 
         if constexpr (MODE & kCol) {
             // transpose the slots the col pass reads: the cast's input, the
-            // row pass's values ("both"), or the inputs ("col")
-            constexpr int kFirst = kSplit ? NIN - NOUT : 0;
-            constexpr int kCount = kSplit ? NOUT : NIN;
+            // row pass's values ("both"), the forward's values evaluated just
+            // below ("col"), or the backward's inputs ("col")
+            if constexpr (kVF) {
+                uint32_t vo[2][16], am[2];
+                block_values<OP, ACT>(a, stage_ptr, kTileBytes, roff, vo, am);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<uint4 *>(const_cast<uint8_t *>(stage_ptr) + (NIN - NOUT) * kTileBytes + roff[c]) =
+                        make_uint4(vo[0][4 * c], vo[0][4 * c + 1], vo[0][4 * c + 2], vo[0][4 * c + 3]);
+                __syncwarp();
+            }
+            constexpr int kFirst = (kSplit || kVF) ? NIN - NOUT : 0;
+            constexpr int kCount = (kSplit || kVF) ? NOUT : NIN;
 #pragma unroll
             for (int k = 0; k < kCount; ++k)
                 transpose_subtile(stage + static_cast<uint32_t>((kFirst + k) * kTileBytes), roff, st_off);
             const int64_t gcol = c0 + lane;
             const bool live = r0 < a.M && gcol < a.N;
             uint32_t out[2][16], amax[2];
-            if constexpr (kSplit || OP == kQuant)
+            if constexpr (kSplit || kVF || OP == kQuant)
                 block_settled<NOUT>(stage_ptr + kFirst * kTileBytes, kTileBytes, roff, out, amax);
             else
                 block_values<OP, ACT>(a, stage_ptr, kTileBytes, roff, out, amax);
@@ -907,7 +927,14 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             if constexpr (GRP) {
                 // per-group layouts (the same shift for the whole warp)
                 const bool ok = a.group_end == nullptr || gtab[3 * kMaxGroups] != 0;
+                // the warp's hint (its last lookup's group) lives in shared
+                // memory: as a register carried round the tile loop it was
+                // spilled to local memory, which missed in L1 (8-9 % of the
+                // kernel's time); any hint gives the same result
+                volatile int *hint_slot = gtab + kGroupHintWord + warp;
+                int chint = *hint_slot;
                 const GroupShift gs = group_shift(a, gtab, r0, chint);
+                if (lane == 0) *hint_slot = chint;
                 if (live && ok) {
                     const int64_t off = blocked_offset(gcol + gs.crow, (r0 >> 5) + gs.c, a.scol_tiles_c);
 #pragma unroll
