@@ -686,7 +686,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
         fence_proxy_async_smem();
     }
     if constexpr (GRP) {
-        if (lane == 0) gtab[kGroupHintWord + warp] = 0;
+        static_assert(STAGES <= kMaxColStages && TM / 32 <= kMaxColBlocks, "column-shift slots");
         if (a.group_end != nullptr && warp == 0) {
             const bool ok = build_group_table(a.group_end, a.num_groups, a.M, gtab, lane);
             if (lane == 0) {
@@ -713,10 +713,23 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
         }
         int it = 0;
         int ghint = 0;     // group of this lane's last row-scale lookup
+        int chint = 0;     // the same for the column shifts
         bool failed = false;
         TileWalk<STAGES, G> done(tiles_n);   // the oldest tile not yet recycled
         for (TileWalk<STAGES, G> w(tiles_n); w.u < num_super; w.next(), ++it) {
             const int s = w.s;
+            // per-group column scales: lane j < TM / 32 finds the shift of the
+            // tile's 32-row block j, handed to the column pass through the
+            // stage's slots below
+            int32_t csh_c = 0, csh_r = 0;
+            if constexpr (GRP && (MODE & kCol)) {
+                const int64_t brow = static_cast<int64_t>(w.tr) * kTileM + 32 * lane;
+                if (lane < kTileM / 32 && brow < a.M) {
+                    const GroupShift gs = group_shift(a, gtab, brow, chint);
+                    csh_c = static_cast<int32_t>(gs.c);
+                    csh_r = static_cast<int32_t>(gs.crow);
+                }
+            }
 #pragma unroll
             for (int h = 0; h < kParts; ++h) {
                 if (it >= STAGES) {
@@ -732,6 +745,15 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
                         failed = true;
                         break;
                     }
+                }
+                if constexpr (GRP && (MODE & kCol)) {
+                    // the part's copy of the shifts, then the arrive below
+                    // releases them to the part's consumers
+                    if (lane < kTileM / 32) {
+                        gtab[col_shift_word(s, h, lane)] = csh_c;
+                        gtab[col_shift_word(s, h, lane) + 1] = csh_r;
+                    }
+                    __syncwarp();
                 }
                 if (lane == 0) {
                     const int32_t r0 = w.tr * kTileM;
@@ -927,16 +949,12 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             if constexpr (GRP) {
                 // per-group layouts (the same shift for the whole warp)
                 const bool ok = a.group_end == nullptr || gtab[3 * kMaxGroups] != 0;
-                // the warp's hint (its last lookup's group) lives in shared
-                // memory: as a register carried round the tile loop it was
-                // spilled to local memory, which missed in L1 (8-9 % of the
-                // kernel's time); any hint gives the same result
-                volatile int *hint_slot = gtab + kGroupHintWord + warp;
-                int chint = *hint_slot;
-                const GroupShift gs = group_shift(a, gtab, r0, chint);
-                if (lane == 0) *hint_slot = chint;
+                // the block's shifts, found by the producer when it loaded
+                // the tile (a lookup here, in every warp's tile loop, cost
+                // 4-8 % of the kernel)
+                const int32_t *csh = gtab + col_shift_word(s, part, static_cast<int>(srb));
                 if (live && ok) {
-                    const int64_t off = blocked_offset(gcol + gs.crow, (r0 >> 5) + gs.c, a.scol_tiles_c);
+                    const int64_t off = blocked_offset(gcol + csh[1], (r0 >> 5) + csh[0], a.scol_tiles_c);
 #pragma unroll
                     for (int o = 0; o < NOUT; ++o) a.s_col[o][off] = static_cast<uint8_t>(b[o]);
                 }
