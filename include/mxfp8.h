@@ -77,7 +77,9 @@ typedef enum {
     MXFP8_OK = 0,
     MXFP8_ERR_NULL = 1,     /* a required pointer is NULL                        */
     MXFP8_ERR_SHAPE = 2,    /* negative size, or N % 32 (rowwise) / M % 32
-                               (colwise, 3D N) not zero, or a size overflows      */
+                               (colwise, 3D N) not zero, or a size overflows
+                               (M or N above 2^31 - 256, more than about 2^31
+                               tiles of 96 x 128, a byte extent past int64)      */
     MXFP8_ERR_ALIGN = 3,    /* pointer or leading dimension misaligned           */
     MXFP8_ERR_LD = 4,       /* leading dimension smaller than the row it spans   */
     MXFP8_ERR_MODE = 5,     /* scale mode not 1, 2 or 3                          */

@@ -328,6 +328,9 @@ mxfp8_status validate(const Spec &s)
     }
     if (s.M == 0 || s.N == 0) return MXFP8_OK;
     if (s.M > kMaxDim || s.N > kMaxDim) return MXFP8_ERR_SHAPE;
+    // the kernels walk their tiles (at least 96 x 128 elements each) with
+    // 32-bit counters
+    if ((s.M + 95) / 96 * ((s.N + 127) / 128) > 0x7FFFFFFFLL - 4096) return MXFP8_ERR_SHAPE;
     const bool row = s.mode & 1, col = s.mode & 2;
     if (s.per_expert && blocked && s.group_rows % 32 != 0) return MXFP8_ERR_SHAPE;
     if (row && s.N % 32 != 0) return MXFP8_ERR_SHAPE;
@@ -438,9 +441,6 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     a.N = s.N;
     a.tiles_n = (s.N + mx::kTileN - 1) / mx::kTileN;
     a.num_tiles = ((s.M + tm - 1) / tm) * a.tiles_n;
-    // the kernels walk tiles with 32-bit counters (and TMA takes 32-bit
-    // coordinates): a tile count past that is out of range
-    if (a.num_tiles > 0x7FFFFFFFLL - 4096) return MXFP8_ERR_SHAPE;
     for (int o = 0; o < 2; ++o) {
         a.q_row[o] = s.q_row[o];
         a.s_row[o] = s.s_row[o];

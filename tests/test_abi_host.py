@@ -65,6 +65,8 @@ def q2d(x=X, ld_x=256, M=128, N=256, mode=3, q_row=Q, ld_qrow=256, s_row=S, ld_s
     (dict(N=48, ld_x=48, ld_qrow=48, mode=1), SHAPE),          # rowwise needs N % 32
     (dict(M=100, mode=2), SHAPE),                                # colwise needs M % 32
     (dict(M=2 ** 31, mode=1), SHAPE),
+    # more than 2^31 tiles of 96 x 128 (the kernels' 32-bit tile counters)
+    (dict(M=2 ** 30, N=2 ** 16, ld_x=2 ** 16, ld_qrow=2 ** 16, ld_srow=2 ** 11, mode=1), SHAPE),
     (dict(x=0), NULL), (dict(q_row=0), NULL), (dict(s_row=0), NULL),
     (dict(q_col=0), NULL), (dict(s_col=0), NULL),
     (dict(x=X + 2), ALIGN), (dict(ld_x=260), ALIGN), (dict(q_row=Q + 8), ALIGN),
