@@ -84,12 +84,12 @@ constexpr int policy_of()
     return (ACT == kGelu && OP == kBwd && MODE != kBoth) ? kGeluPoly : ACT;
 }
 
-// static shared memory of the policy's kernels: the tail table (L alone for
-// the forward, (L, Q) pairs for the backward)
+// static shared memory of the policy's kernels: the tail table (Phi by sign
+// for the forward, (L, Q) pairs for the backward)
 template <int OP, int POL>
 constexpr size_t static_smem_bytes()
 {
-    return POL != kGelu ? 0 : (OP == kFwd ? sizeof(float) : sizeof(float2)) * kGeluTabN;
+    return POL != kGelu ? 0 : sizeof(float2) * kGeluTabN;
 }
 
 template <int TM>
