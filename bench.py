@@ -511,7 +511,10 @@ def main():
         line["configs_note"] = ("each workload of the pages' shape list, one cell at a time: median of %d "
                                 "CUDA-event launch times, inputs resident, L2 flushed before each launch "
                                 "(a 512 MB write, then a 1 GB read so the written lines leave L2 outside "
-                                "the timed launch); 3D = the first E experts of the seed-4 draw"
+                                "the timed launch); 3D = the first E experts of the seed-4 draw; "
+                                "the mixed workload scales every 7th row by up to 2^20, so about 5 % of "
+                                "its 8-element chunks hold a gate below the fast range, settled pair by "
+                                "pair on the exact path; the (128, 128) forward is launch-bound"
                                 % args.config_steps)
     if cpu:
         line["cpu_baseline"] = cpu
