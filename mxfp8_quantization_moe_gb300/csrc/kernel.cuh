@@ -202,6 +202,64 @@ __device__ __forceinline__ uint32_t word_at(const uint8_t *slot_base, uint32_t r
     return *reinterpret_cast<const uint32_t *>(slot_base + roff_c + 4 * p);
 }
 
+// settle_pair on every flagged pair of the warp (bit j of `near`: pair j of
+// the lane's block, whose chunk j / 4 sits at r0..r3 in the slots), for
+// blocks whose flagged pairs span more than two pair numbers in the warp
+// (a row of far gates, whose lane owns all 16 pairs, in a row pass): the
+// warp's flagged pairs are numbered across the lanes and lane t of a round
+// takes pair base + t (its owner found by a search over the owners' first
+// numbers), so such a block costs about one settle_pair per round rather
+// than one per pair in turn.  Each result is left in the stage over the
+// pair's words of slot 0 (and of slot 1 for the second output), for the
+// lanes to read back.  Out of line, with scalar arguments, so that none of
+// this weighs on the callers' registers.  Used by the forward's row passes
+// but for "both" (mixed 4096 x 7168: row 102 -> 47 us, col 104 -> 49); the
+// backward's row pass gained as much on that workload but lost 1.8 % on
+// the large one (code placement), and "both" modes keep their own paths.
+template <int OP, int ACT>
+static __device__ __noinline__ void settle_flagged(const void *ta, const void *tb, uint8_t *stage, int tile_bytes_,
+                                                   uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3, uint32_t near,
+                                                   bool whole)
+{
+    constexpr int NIN = OpTraits<OP>::kIn;
+    constexpr int NOUT = OpTraits<OP>::kOut;
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t cnt = __popc(near);
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= static_cast<uint32_t>(d)) incl += v;
+    }
+    const uint32_t excl = incl - cnt;
+    const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    for (uint32_t base = 0; base < total; base += 32) {
+        const uint32_t k = base + lane;
+        int owner = 0;            // the last lane whose first number is <= k
+#pragma unroll
+        for (int step = 16; step >= 1; step >>= 1) {
+            const uint32_t e = __shfl_sync(0xFFFFFFFFu, excl, owner + step);
+            if (e <= k) owner += step;
+        }
+        const uint32_t nm = __shfl_sync(0xFFFFFFFFu, near, owner);
+        const uint32_t first = __shfl_sync(0xFFFFFFFFu, excl, owner);
+        const bool wh = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(whole), owner) != 0u;
+        const uint32_t o0 = __shfl_sync(0xFFFFFFFFu, r0, owner), o1 = __shfl_sync(0xFFFFFFFFu, r1, owner);
+        const uint32_t o2 = __shfl_sync(0xFFFFFFFFu, r2, owner), o3 = __shfl_sync(0xFFFFFFFFu, r3, owner);
+        if (k < total) {
+            const int j = static_cast<int>(__fns(nm, 0u, static_cast<int>(k - first) + 1));
+            const int p = j & 3;
+            const uint32_t rc = (j >> 2) == 0 ? o0 : (j >> 2) == 1 ? o1 : (j >> 2) == 2 ? o2 : o3;
+            const uint64_t r = settle_pair<OP, ACT>(ta, tb, word_at(stage, rc, p), word_at(stage + tile_bytes_, rc, p),
+                                                    NIN > 2 ? word_at(stage + 2 * tile_bytes_, rc, p) : 0u, wh);
+            *reinterpret_cast<uint32_t *>(stage + rc + 4 * p) = static_cast<uint32_t>(r);
+            if constexpr (NOUT > 1)
+                *reinterpret_cast<uint32_t *>(stage + tile_bytes_ + rc + 4 * p) = static_cast<uint32_t>(r >> 32);
+        }
+    }
+    __syncwarp();
+}
+
 // Element values of the lane's block.  For the cast, the input itself; for
 // the gated ops, the fast element op on the NIN input slots and the midpoint
 // test of every value (near_mid2: a value within its window of a 0x60/0x61
@@ -214,7 +272,7 @@ __device__ __forceinline__ uint32_t word_at(const uint8_t *slot_base, uint32_t r
 // the risky blocks.)  DIST (forward only): the test keeps a running minimum
 // of the values' distances instead of a bit per pair, and the flagged pairs
 // are found again in the rare path.  Returns the outputs' amax patterns.
-template <int OP, int ACT, bool DIST = false>
+template <int OP, int ACT, bool DIST = false, bool COOP = !DIST && OP == kFwd>
 __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t *stage, int tile_bytes_,
                                              const uint32_t (&roff)[4], uint32_t (&out)[2][16],
                                              uint32_t (&amax)[2])
@@ -284,17 +342,32 @@ __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t 
 #pragma unroll
             for (int c = 0; c < 4; ++c) near |= ((farc >> c) & 1u) ? 0xFu << (4 * c) : 0u;
             if (full || nanb) near = 0xFFFFu;
-            const void *ta = Gated<ACT>::table_a(a), *tb = Gated<ACT>::table_b(a);
+            bool coop = false;
+            if constexpr (COOP) coop = __popc(__reduce_or_sync(0xFFFFFFFFu, near)) > 2;
+            if (coop) {
+                settle_flagged<OP, ACT>(Gated<ACT>::table_a(a), Gated<ACT>::table_b(a), const_cast<uint8_t *>(stage),
+                                        tile_bytes_, roff[0], roff[1], roff[2], roff[3], near, full);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                if ((near >> j) & 1u) {
-                    const uint32_t cj = roff[j >> 2];
-                    const uint64_t r = settle_pair<OP, ACT>(ta, tb, word_at(stage, cj, j & 3),
-                                                            word_at(stage + tile_bytes_, cj, j & 3),
-                                                            NIN > 2 ? word_at(stage + 2 * tile_bytes_, cj, j & 3) : 0u,
-                                                            full);
-                    out[0][j] = static_cast<uint32_t>(r);
-                    if constexpr (NOUT > 1) out[1][j] = static_cast<uint32_t>(r >> 32);
+                for (int j = 0; j < 16; ++j) {
+                    if ((near >> j) & 1u) {
+                        out[0][j] = word_at(stage, roff[j >> 2], j & 3);
+                        if constexpr (NOUT > 1) out[1][j] = word_at(stage + tile_bytes_, roff[j >> 2], j & 3);
+                    }
+                }
+            } else {
+                // few pair numbers flagged: each lane settles its own
+                const void *ta = Gated<ACT>::table_a(a), *tb = Gated<ACT>::table_b(a);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    if ((near >> j) & 1u) {
+                        const uint32_t cj = roff[j >> 2];
+                        const uint64_t r = settle_pair<OP, ACT>(ta, tb, word_at(stage, cj, j & 3),
+                                                                word_at(stage + tile_bytes_, cj, j & 3),
+                                                                NIN > 2 ? word_at(stage + 2 * tile_bytes_, cj, j & 3) : 0u,
+                                                                full);
+                        out[0][j] = static_cast<uint32_t>(r);
+                        if constexpr (NOUT > 1) out[1][j] = static_cast<uint32_t>(r >> 32);
+                    }
                 }
             }
             count_fallbacks_warp(a.fallbacks, 2u * __popc(near));
@@ -844,7 +917,9 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
     // the backward, 1362 -> 1462 us, and for the per-group forward, 879 ->
     // 934 us)
     constexpr bool kVF = (MODE == kCol) && (OP == kFwd) && !GRP;
-    constexpr bool kWrites = kSplit || (MODE & kCol);           // generic writes into the stage
+    // generic writes into the stage (the values handed to the col pass, the
+    // transposes, the forward rare path's results)
+    constexpr bool kWrites = kSplit || (MODE & kCol) || OP == kFwd;
     for (TileWalk<STAGES, G> w(tiles_n); w.u < num_super; w.next()) {
         const int s = w.s;
         const uint32_t part = kParts == 2 ? (scb >> 1) : 0u;     // the half this warp reads
@@ -935,7 +1010,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             if constexpr (kSplit || kVF || OP == kQuant)
                 block_settled<NOUT>(stage_ptr + kFirst * kTileBytes, kTileBytes, roff, out, amax);
             else
-                block_values<OP, ACT>(a, stage_ptr, kTileBytes, roff, out, amax);
+                block_values<OP, ACT, false, false>(a, stage_ptr, kTileBytes, roff, out, amax);
             int64_t grp = 0, rin = r0;
             if (a.group_stride != 0) {  // 3D: per-expert column-major output
                 grp = r0 / a.group_rows;
