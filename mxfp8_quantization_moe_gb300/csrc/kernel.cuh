@@ -213,9 +213,9 @@ __device__ __forceinline__ uint32_t word_at(const uint8_t *slot_base, uint32_t r
 // pair's words of slot 0 (and of slot 1 for the second output), for the
 // lanes to read back.  Out of line, with scalar arguments, so that none of
 // this weighs on the callers' registers.  Used by the forward's row passes
-// but for "both" (mixed 4096 x 7168: row 102 -> 47 us, col 104 -> 49); the
-// backward's row pass gained as much on that workload but lost 1.8 % on
-// the large one (code placement), and "both" modes keep their own paths.
+// (mixed 4096 x 7168: row 102 -> 47 us, col 104 -> 49, both 119 -> 61); the
+// backward's row pass gained as much on that workload but lost 1.8 % on the
+// large one (code placement).
 template <int OP, int ACT>
 static __device__ __noinline__ void settle_flagged(const void *ta, const void *tb, uint8_t *stage, int tile_bytes_,
                                                    uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3, uint32_t near,
@@ -272,7 +272,7 @@ static __device__ __noinline__ void settle_flagged(const void *ta, const void *t
 // the risky blocks.)  DIST (forward only): the test keeps a running minimum
 // of the values' distances instead of a bit per pair, and the flagged pairs
 // are found again in the rare path.  Returns the outputs' amax patterns.
-template <int OP, int ACT, bool DIST = false, bool COOP = !DIST && OP == kFwd>
+template <int OP, int ACT, bool DIST = false, bool COOP = OP == kFwd>
 __device__ __forceinline__ void block_values(const KernelArgs &a, const uint8_t *stage, int tile_bytes_,
                                              const uint32_t (&roff)[4], uint32_t (&out)[2][16],
                                              uint32_t (&amax)[2])
