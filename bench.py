@@ -85,6 +85,17 @@ def traffic_for(cell: str):
     return t[0]
 
 
+def configs_note(steps: int) -> str:
+    """How the per-workload lines of the bench line were measured."""
+    return ("each workload of the pages' shape list, one cell at a time: median of %d "
+            "CUDA-event launch times, inputs resident, L2 flushed before each launch "
+            "(a 512 MB write, then a 1 GB read so the written lines leave L2 outside "
+            "the timed launch); 3D = the first E experts of the seed-4 draw; "
+            "the mixed workload scales every 7th row by up to 2^20, so about 5 %% of "
+            "its 8-element chunks hold a gate below the fast range, settled pair by "
+            "pair on the exact path; the (128, 128) forward is launch-bound" % steps)
+
+
 def cell_bytes(kind: str, mode: int, M: int, N: int) -> int:
     k = 2 if mode == 3 else 1
     mn = M * N
@@ -508,14 +519,7 @@ def main():
         line["e2e"] = e2e
     if configs:
         line["configs"] = configs
-        line["configs_note"] = ("each workload of the pages' shape list, one cell at a time: median of %d "
-                                "CUDA-event launch times, inputs resident, L2 flushed before each launch "
-                                "(a 512 MB write, then a 1 GB read so the written lines leave L2 outside "
-                                "the timed launch); 3D = the first E experts of the seed-4 draw; "
-                                "the mixed workload scales every 7th row by up to 2^20, so about 5 % of "
-                                "its 8-element chunks hold a gate below the fast range, settled pair by "
-                                "pair on the exact path; the (128, 128) forward is launch-bound"
-                                % args.config_steps)
+        line["configs_note"] = configs_note(args.config_steps)
     if cpu:
         line["cpu_baseline"] = cpu
     if rank == 0:
