@@ -42,27 +42,27 @@ PAGES_US = {("fwd", 1): 904.19, ("fwd", 2): 1022.98, ("fwd", 3): 1216.08,
             ("bwd", 1): 1321.98, ("bwd", 2): 1710.08, ("bwd", 3): 1859.09}
 
 
-# DRAM traffic (read + write bytes) of one full-size launch, estimated from
-# an ncu capture of a smaller launch of the same kernel (16384 rows, or 8
-# experts for the 3D cast) scaled by the units processed; keyed to the hash of
-# the kernel sources it was taken on (None once they change).  Write-back still
-# held in L2 when the captured kernel ends does not scale with the size, so the
-# full-size figure slightly understates the real traffic.
+# DRAM traffic (read + write bytes) of one full-size launch of each kernel,
+# measured by ncu on that launch alone (dram__bytes_read.sum +
+# dram__bytes_write.sum, a one-pass capture, in a separate run of this
+# script's --cell mode: a number taken under a profiler is not timed here);
+# keyed to the hash of the kernel sources it was taken on (None once they
+# change).
 TRAFFIC = {
-    "bwd_both": (10.5501e9, "7ff130f67ada9f06"),
-    "bwd_both_gelu": (10.5527e9, "7ff130f67ada9f06"),
-    "bwd_col": (8.44839e9, "7ff130f67ada9f06"),
-    "bwd_row": (8.45383e9, "7ff130f67ada9f06"),
-    "fwd_both": (6.24262e9, "7ff130f67ada9f06"),
-    "fwd_col": (5.24911e9, "7ff130f67ada9f06"),
-    "fwd_row": (5.24271e9, "7ff130f67ada9f06"),
-    "fwd_row_gelu": (5.24513e9, "7ff130f67ada9f06"),
-    "quant3d": (7.8657e9, "7ff130f67ada9f06"),
-    "quant_both": (3.98872e9, "7ff130f67ada9f06"),
-    "quant_row": (3.00036e9, "7ff130f67ada9f06"),
+    "bwd_both": (10.8325e9, "9e115d450b4f5c05"),
+    "bwd_both_gelu": (10.8331e9, "9e115d450b4f5c05"),
+    "bwd_col": (8.632e9, "9e115d450b4f5c05"),
+    "bwd_row": (8.6309e9, "9e115d450b4f5c05"),
+    "fwd_both": (6.47706e9, "9e115d450b4f5c05"),
+    "fwd_col": (5.38256e9, "9e115d450b4f5c05"),
+    "fwd_row": (5.38188e9, "9e115d450b4f5c05"),
+    "fwd_row_gelu": (5.38289e9, "9e115d450b4f5c05"),
+    "quant3d": (8.10438e9, "9e115d450b4f5c05"),
+    "quant_both": (4.31613e9, "9e115d450b4f5c05"),
+    "quant_row": (3.22308e9, "9e115d450b4f5c05"),
 }
-TRAFFIC_KIND = ("estimate: ncu dram__bytes_read.sum + dram__bytes_write.sum of a 16384-row launch "
-                "scaled x8 to the full size; L2-resident write-back at kernel end does not scale")
+TRAFFIC_KIND = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch of the kernel, "
+                "captured alone in a separate run (bench.py --cell <cell> --steps 1 --warmup 0)")
 
 
 def kernel_source_hash() -> str:
