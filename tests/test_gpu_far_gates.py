@@ -123,6 +123,32 @@ def test_far_gates_next_to_huge_partners(act):
     print("differing codes:", n)
 
 
+
+
+@pytest.mark.parametrize("act", ["silu", "gelu"])
+def test_far_gate_rows_of_every_density(act):
+    """Rows whose share of gates below the fast range runs from none to all
+    (row r of each 32-row block: share (r % 8) / 7), next to rows of isolated
+    far gates: in a row pass the lanes then flag from 0 to all 16 pairs of
+    their blocks, the case the warp settles cooperatively, with every count
+    of flagged pairs across the lanes.  Forward and backward, every mode."""
+    rng = np.random.default_rng(21 if act == "silu" else 22)
+    share = (np.arange(M) % 8) / 7.0
+    far = rng.random((M, N)) < share[:, None]
+    far |= rng.random((M, N)) < 0.002
+    g = np.where(far, -rng.uniform(16.1, 90, (M, N)), rng.normal(0.0, 2.0, (M, N)))
+    u = rng.choice([-1.0, 1.0], (M, N)) * rng.uniform(1, 2, (M, N)) * 2.0 ** rng.integers(-10, 30, (M, N))
+    dh = rng.normal(0.0, 1.0, (M, N))
+    gate, up, dh = to_dev(bits_of(g)), to_dev(bits_of(u)), to_dev(bits_of(dh))
+    n = 0
+    for mode in (1, 2, 3):
+        n += compare(fwd_gpu(gate, up, mode, act=act), oracle_fwd(gate, up, mode, act=act), what="fwd-far-rows")
+        dg, du = bwd_gpu(dh, gate, up, mode, act=act)
+        wg, wu = oracle_bwd(dh, gate, up, mode, act=act)
+        n += compare(dg, wg, what="dgate-far-rows") + compare(du, wu, what="dup-far-rows")
+    print("differing codes:", n)
+
+
 def test_status_clean_after_far_gates():
     flags, _ = device_status()
     assert flags == 0
