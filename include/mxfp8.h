@@ -97,10 +97,12 @@ int mxfp8_version(void);
 
 /*
  * One-time set-up of the current device: fills the library's read-only
- * tables, one entry per bf16 pattern g -- sigmoid(g) in double and as a
- * (hi, lo) float pair, and (hi, lo) pairs of Phi(g) and gelu'(g) (2 MB in
- * all; used by the exact-rounding paths of the SwiGLU and GEGLU kernels) --
- * and waits for them on `stream`.  Every entry point calls it
+ * tables -- one entry per bf16 pattern g of sigmoid(g) in double and as a
+ * (hi, lo) float pair, and of Phi(g) and gelu'(g) as (hi, lo) pairs and in
+ * double (used by the exact-rounding paths of the SwiGLU and GEGLU
+ * kernels), and the GEGLU fast path's table of (Phi(-t), t phi(t)) over
+ * the bf16 magnitudes t from 2^-20 to 6 (3 MB in all) -- and waits for them
+ * on `stream`.  Every entry point calls it
  * on its first use on a device; call it yourself before capturing a graph.
  * Returns MXFP8_ERR_CAPTURE if it would have to run inside a capture.
  */
