@@ -232,7 +232,12 @@ def run_reference(args, world, rank):
     if rank != 0:
         return 0
     threads = os.cpu_count() or 1
-    rows = 32 * max(1, args.ref_blocks)
+    if args.ref_blocks > 0:
+        rows = 32 * args.ref_blocks
+    else:
+        # a sample per step sized so that all the steps take about
+        # --ref-seconds (tiny samples measure the thread pool, not the oracle)
+        rows, _ = time_oracle(args.ref_seconds / max(1, args.steps + args.warmup), threads)
     gate, up, dh = cpu_sample(rows)
     for _ in range(args.warmup):
         oracle_step(gate, up, dh, threads=threads)
@@ -372,7 +377,10 @@ def main():
                     help="row slabs the end-to-end step is pipelined over")
     ap.add_argument("--e2e-copy-streams", type=int, default=1,
                     help="streams per copy direction in the end-to-end step")
-    ap.add_argument("--ref-blocks", type=int, default=2)
+    ap.add_argument("--ref-blocks", type=int, default=0,
+                    help="reference arm: 32-row blocks per step (0: sized by --ref-seconds)")
+    ap.add_argument("--ref-seconds", type=float, default=90.0,
+                    help="reference arm: about how long all its steps take")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-config cell timings (every workload of the pages' shape list)")
     ap.add_argument("--config-steps", type=int, default=20)
