@@ -114,13 +114,6 @@ constexpr size_t smem_bytes()
 }
 
 // ------------------------------------------------------------ block values
-__device__ __forceinline__ uint32_t bf16_bits(float v) { return pack_bf16x2(v, 0.0f) & 0xFFFFu; }
-
-__device__ __forceinline__ void set_half16(uint32_t &w, int hi, uint32_t b)
-{
-    w = hi ? ((w & 0xFFFFu) | (b << 16)) : ((w & 0xFFFF0000u) | b);
-}
-
 // Bit p: pair p of chunk c (in the slot, 16-byte offset roff_c) has a fast
 // value near a rounding midpoint -- the block_values test again, for the
 // rare blocks where some value is.
@@ -266,7 +259,10 @@ static __device__ __noinline__ void settle_flagged(const void *ta, const void *t
 // rounding midpoint, where a scale byte could step); then, for the warps with
 // a lane whose block holds a flagged value, a gate outside the fast range or
 // a huge, infinite or NaN amax, settle_pair on the flagged pairs (on every
-// pair of a chunk holding such a gate, of a block with such an amax).  (Testing every value, rather than
+// pair of a chunk holding such a gate, of a block with such an amax): lane
+// by lane, or (COOP, the forward's row passes) across the warp's lanes
+// where the flagged pairs span more than two pair numbers (settle_flagged).
+// (Testing every value, rather than
 // only the blocks whose amax sits at that mantissa pair, also covers the
 // other direction's blocks in "both" mode, and measured cheaper than scanning
 // the risky blocks.)  DIST (forward only): the test keeps a running minimum
