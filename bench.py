@@ -49,17 +49,17 @@ PAGES_US = {("fwd", 1): 904.19, ("fwd", 2): 1022.98, ("fwd", 3): 1216.08,
 # keyed to the hash of the kernel sources it was taken on (None once they
 # change).
 TRAFFIC = {
-    "bwd_both": (10.8327e9, "4bce5a200f0fc5ad"),
-    "bwd_both_gelu": (10.8338e9, "4bce5a200f0fc5ad"),
-    "bwd_col": (8.63227e9, "4bce5a200f0fc5ad"),
-    "bwd_row": (8.63077e9, "4bce5a200f0fc5ad"),
-    "fwd_both": (6.47844e9, "4bce5a200f0fc5ad"),
-    "fwd_col": (5.3827e9, "4bce5a200f0fc5ad"),
-    "fwd_row": (5.38161e9, "4bce5a200f0fc5ad"),
-    "fwd_row_gelu": (5.38275e9, "4bce5a200f0fc5ad"),
-    "quant3d": (8.10412e9, "4bce5a200f0fc5ad"),
-    "quant_both": (4.31613e9, "4bce5a200f0fc5ad"),
-    "quant_row": (3.22171e9, "4bce5a200f0fc5ad"),
+    "bwd_both": (10.8331e9, "90c40141ab957ba1"),
+    "bwd_both_gelu": (10.8338e9, "90c40141ab957ba1"),
+    "bwd_col": (8.6316e9, "90c40141ab957ba1"),
+    "bwd_row": (8.63051e9, "90c40141ab957ba1"),
+    "fwd_both": (6.47753e9, "90c40141ab957ba1"),
+    "fwd_col": (5.38239e9, "90c40141ab957ba1"),
+    "fwd_row": (5.38169e9, "90c40141ab957ba1"),
+    "fwd_row_gelu": (5.3823e9, "90c40141ab957ba1"),
+    "quant3d": (8.10344e9, "90c40141ab957ba1"),
+    "quant_both": (4.31566e9, "90c40141ab957ba1"),
+    "quant_row": (3.22211e9, "90c40141ab957ba1"),
 }
 TRAFFIC_KIND = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch of the kernel, "
                 "captured alone in a separate run (bench.py --cell <cell> --steps 1 --warmup 0)")
