@@ -427,7 +427,7 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     if (!get_encoder()) return MXFP8_ERR_DEVICE;
     const int nin = s.op == mx::kQuant ? 1 : (s.op == mx::kFwd ? 2 : 3);
     const int mode = s.mode & 3;
-    const mx::LaunchShape shape = mx::launch_shape(s.op, mode);
+    const mx::LaunchShape shape = mx::launch_shape(s.op, mode, s.op == mx::kQuant ? mx::kSilu : s.act);
     const int tm = shape.tile_rows;
     CUtensorMap maps[3];
     std::memset(maps, 0, sizeof(maps));

@@ -14,10 +14,10 @@ template <int OP, int MODE, int ACT, bool GRP>
 cudaError_t launch_tiles(const CUtensorMap (&maps)[3], const KernelArgs &a, int grid,
                          cudaStream_t stream, int device)
 {
-    constexpr int kTM = Tuning<OP, MODE>::kTM;
-    constexpr int kStages = Tuning<OP, MODE>::kStages;
-    constexpr int kCtas = Tuning<OP, MODE>::kCtas;
-    constexpr int kGroup = Tuning<OP, MODE>::kGroup;
+    constexpr int kTM = TuningFor<OP, MODE, ACT>::kTM;
+    constexpr int kStages = TuningFor<OP, MODE, ACT>::kStages;
+    constexpr int kCtas = TuningFor<OP, MODE, ACT>::kCtas;
+    constexpr int kGroup = TuningFor<OP, MODE, ACT>::kGroup;
     constexpr int kPol = policy_of<OP, MODE, ACT>();
     constexpr size_t kSmem = smem_bytes<OP, kTM, kStages, kGroup, GRP>();
     constexpr size_t kStatic = static_smem_bytes<OP, kPol>();
@@ -39,27 +39,28 @@ cudaError_t launch_tiles(const CUtensorMap (&maps)[3], const KernelArgs &a, int 
 }
 
 // tile rows, resident CTAs per SM and row-scale group of the instantiation
-// the host will launch
+// the host will launch (GEGLU's backward "both" has its own)
 struct LaunchShape {
     int tile_rows, ctas_per_sm, group;
 };
-template <int OP, int MODE>
+template <int OP, int MODE, int ACT>
 constexpr LaunchShape shape_of()
 {
-    return {Tuning<OP, MODE>::kTM, Tuning<OP, MODE>::kCtas, Tuning<OP, MODE>::kGroup};
+    return {TuningFor<OP, MODE, ACT>::kTM, TuningFor<OP, MODE, ACT>::kCtas, TuningFor<OP, MODE, ACT>::kGroup};
 }
-inline LaunchShape launch_shape(int op, int mode)
+inline LaunchShape launch_shape(int op, int mode, int act)
 {
+    if (act == kGelu && op == kBwd && mode == kBoth) return shape_of<kBwd, kBoth, kGelu>();
     switch (op * 4 + mode) {
-    case kQuant * 4 + kRow: return shape_of<kQuant, kRow>();
-    case kQuant * 4 + kCol: return shape_of<kQuant, kCol>();
-    case kQuant * 4 + kBoth: return shape_of<kQuant, kBoth>();
-    case kFwd * 4 + kRow: return shape_of<kFwd, kRow>();
-    case kFwd * 4 + kCol: return shape_of<kFwd, kCol>();
-    case kFwd * 4 + kBoth: return shape_of<kFwd, kBoth>();
-    case kBwd * 4 + kRow: return shape_of<kBwd, kRow>();
-    case kBwd * 4 + kCol: return shape_of<kBwd, kCol>();
-    default: return shape_of<kBwd, kBoth>();
+    case kQuant * 4 + kRow: return shape_of<kQuant, kRow, kSilu>();
+    case kQuant * 4 + kCol: return shape_of<kQuant, kCol, kSilu>();
+    case kQuant * 4 + kBoth: return shape_of<kQuant, kBoth, kSilu>();
+    case kFwd * 4 + kRow: return shape_of<kFwd, kRow, kSilu>();
+    case kFwd * 4 + kCol: return shape_of<kFwd, kCol, kSilu>();
+    case kFwd * 4 + kBoth: return shape_of<kFwd, kBoth, kSilu>();
+    case kBwd * 4 + kRow: return shape_of<kBwd, kRow, kSilu>();
+    case kBwd * 4 + kCol: return shape_of<kBwd, kCol, kSilu>();
+    default: return shape_of<kBwd, kBoth, kSilu>();
     }
 }
 
