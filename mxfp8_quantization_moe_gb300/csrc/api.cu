@@ -427,7 +427,10 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     if (!get_encoder()) return MXFP8_ERR_DEVICE;
     const int nin = s.op == mx::kQuant ? 1 : (s.op == mx::kFwd ? 2 : 3);
     const int mode = s.mode & 3;
-    const mx::LaunchShape shape = mx::launch_shape(s.op, mode, s.op == mx::kQuant ? mx::kSilu : s.act);
+    // per-group blocked scales run their own instantiations
+    const bool grouped = (s.mode & MXFP8_BLOCKED_SCALES) != 0 &&
+                         (s.group_end != nullptr || (s.per_expert && s.group_rows / 32 > 0));
+    const mx::LaunchShape shape = mx::launch_shape(s.op, mode, s.op == mx::kQuant ? mx::kSilu : s.act, grouped);
     const int tm = shape.tile_rows;
     CUtensorMap maps[3];
     std::memset(maps, 0, sizeof(maps));
@@ -498,8 +501,6 @@ mxfp8_status run(const Spec &s, void *stream_ptr)
     const int64_t supers = ((s.M + tm - 1) / tm) * ((a.tiles_n + shape.group - 1) / shape.group);
     const int64_t slots = static_cast<int64_t>(d->sms) * shape.ctas_per_sm;
     const int grid = static_cast<int>(supers < slots ? supers : slots);
-    // per-group blocked scales run their own instantiations
-    const bool grouped = a.blocked && (a.group_end != nullptr || a.uni_blocks > 0);
     cudaError_t e;
     switch (s.op) {
     case mx::kQuant:

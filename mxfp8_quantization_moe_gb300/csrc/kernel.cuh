@@ -74,27 +74,29 @@ MX_TUNE(kBwd, kCol, 96, 3, 1, 1)
 MX_TUNE(kBwd, kBoth, 128, 2, 1, 2)
 #undef MX_TUNE
 
-// The same per activation: GEGLU's backward "both" takes 96-row tiles with
-// three stages and keeps its values in registers (its policy then is the
-// rational tail, the tail table having no room there): 2223 -> 2160 us at
-// 131072 x 8192, where SwiGLU's measured no gain from that shape.
-template <int OP, int MODE, int ACT>
+// The same per activation and scale kind: GEGLU's backward "both" with
+// plain scales takes 96-row tiles with three stages and keeps its values in
+// registers (its policy then is the rational tail, the tail table having no
+// room there): 2223 -> 2160 us at 131072 x 8192, where SwiGLU's measured no
+// gain from that shape, and the per-group one lost 12 % (2282 -> 2551).
+template <int OP, int MODE, int ACT, bool GRP>
 struct TuningFor : Tuning<OP, MODE> {
 };
 template <>
-struct TuningFor<kBwd, kBoth, kGelu> {
+struct TuningFor<kBwd, kBoth, kGelu, false> {
     static constexpr int kTM = 96, kStages = 3, kCtas = 1, kGroup = 2;
 };
 
 // The activation policy a kernel evaluates: GEGLU's tail table for the
-// forward, its rational tail for the backward (three stages of 96-row tiles
-// leave no room for the table there; two stages measured 11-14 % slower in
+// forward and the per-group backward "both" (two stages of 128-row tiles),
+// its rational tail for the rest of the backward (three stages of 96-row
+// tiles leave no room for the table; two stages measured 11-14 % slower in
 // the row and column modes, and the table with two stages of 128 rows 3 %
 // slower in "both").
-template <int OP, int MODE, int ACT>
+template <int OP, int MODE, int ACT, bool GRP>
 constexpr int policy_of()
 {
-    return (ACT == kGelu && OP == kBwd) ? kGeluPoly : ACT;
+    return (ACT == kGelu && OP == kBwd && (MODE != kBoth || !GRP)) ? kGeluPoly : ACT;
 }
 
 // static shared memory of the policy's kernels: the tail table (Phi by sign
@@ -950,7 +952,7 @@ __global__ void __launch_bounds__((warps_of<TM>() + 1) * 32, CTAS)
             const int64_t grow = r0 + lane;
             const bool live = grow < a.M && c0 < a.N;
             uint32_t b[2];
-            if constexpr (kSplit && OP == kBwd && ACT == kSilu) {
+            if constexpr (kSplit && OP == kBwd && ACT != kGeluPoly) {
                 // values settled chunk by chunk into the value slots (which
                 // the col pass then transposes), encoded from there: only one
                 // chunk of the two outputs lives in registers (measured: a

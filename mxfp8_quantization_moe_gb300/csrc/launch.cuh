@@ -14,11 +14,11 @@ template <int OP, int MODE, int ACT, bool GRP>
 cudaError_t launch_tiles(const CUtensorMap (&maps)[3], const KernelArgs &a, int grid,
                          cudaStream_t stream, int device)
 {
-    constexpr int kTM = TuningFor<OP, MODE, ACT>::kTM;
-    constexpr int kStages = TuningFor<OP, MODE, ACT>::kStages;
-    constexpr int kCtas = TuningFor<OP, MODE, ACT>::kCtas;
-    constexpr int kGroup = TuningFor<OP, MODE, ACT>::kGroup;
-    constexpr int kPol = policy_of<OP, MODE, ACT>();
+    constexpr int kTM = TuningFor<OP, MODE, ACT, GRP>::kTM;
+    constexpr int kStages = TuningFor<OP, MODE, ACT, GRP>::kStages;
+    constexpr int kCtas = TuningFor<OP, MODE, ACT, GRP>::kCtas;
+    constexpr int kGroup = TuningFor<OP, MODE, ACT, GRP>::kGroup;
+    constexpr int kPol = policy_of<OP, MODE, ACT, GRP>();
     constexpr size_t kSmem = smem_bytes<OP, kTM, kStages, kGroup, GRP>();
     constexpr size_t kStatic = static_smem_bytes<OP, kPol>();
     static_assert(kSmem + kStatic <= 227 * 1024, "shared memory per CTA");
@@ -39,28 +39,30 @@ cudaError_t launch_tiles(const CUtensorMap (&maps)[3], const KernelArgs &a, int 
 }
 
 // tile rows, resident CTAs per SM and row-scale group of the instantiation
-// the host will launch (GEGLU's backward "both" has its own)
+// the host will launch (GEGLU's backward "both" with plain scales has its
+// own)
 struct LaunchShape {
     int tile_rows, ctas_per_sm, group;
 };
-template <int OP, int MODE, int ACT>
+template <int OP, int MODE, int ACT, bool GRP>
 constexpr LaunchShape shape_of()
 {
-    return {TuningFor<OP, MODE, ACT>::kTM, TuningFor<OP, MODE, ACT>::kCtas, TuningFor<OP, MODE, ACT>::kGroup};
+    using T = TuningFor<OP, MODE, ACT, GRP>;
+    return {T::kTM, T::kCtas, T::kGroup};
 }
-inline LaunchShape launch_shape(int op, int mode, int act)
+inline LaunchShape launch_shape(int op, int mode, int act, bool grouped)
 {
-    if (act == kGelu && op == kBwd && mode == kBoth) return shape_of<kBwd, kBoth, kGelu>();
+    if (act == kGelu && op == kBwd && mode == kBoth && !grouped) return shape_of<kBwd, kBoth, kGelu, false>();
     switch (op * 4 + mode) {
-    case kQuant * 4 + kRow: return shape_of<kQuant, kRow, kSilu>();
-    case kQuant * 4 + kCol: return shape_of<kQuant, kCol, kSilu>();
-    case kQuant * 4 + kBoth: return shape_of<kQuant, kBoth, kSilu>();
-    case kFwd * 4 + kRow: return shape_of<kFwd, kRow, kSilu>();
-    case kFwd * 4 + kCol: return shape_of<kFwd, kCol, kSilu>();
-    case kFwd * 4 + kBoth: return shape_of<kFwd, kBoth, kSilu>();
-    case kBwd * 4 + kRow: return shape_of<kBwd, kRow, kSilu>();
-    case kBwd * 4 + kCol: return shape_of<kBwd, kCol, kSilu>();
-    default: return shape_of<kBwd, kBoth, kSilu>();
+    case kQuant * 4 + kRow: return shape_of<kQuant, kRow, kSilu, false>();
+    case kQuant * 4 + kCol: return shape_of<kQuant, kCol, kSilu, false>();
+    case kQuant * 4 + kBoth: return shape_of<kQuant, kBoth, kSilu, false>();
+    case kFwd * 4 + kRow: return shape_of<kFwd, kRow, kSilu, false>();
+    case kFwd * 4 + kCol: return shape_of<kFwd, kCol, kSilu, false>();
+    case kFwd * 4 + kBoth: return shape_of<kFwd, kBoth, kSilu, false>();
+    case kBwd * 4 + kRow: return shape_of<kBwd, kRow, kSilu, false>();
+    case kBwd * 4 + kCol: return shape_of<kBwd, kCol, kSilu, false>();
+    default: return shape_of<kBwd, kBoth, kSilu, false>();
     }
 }
 
