@@ -331,9 +331,9 @@ mxfp8_status mxfp8_selftest_activation(float *out, void *stream);
 /*
  * Self-test of the GEGLU fast paths, like mxfp8_selftest_activation: for
  * every bf16 pattern g, out[k*65536 + g] for k = 0 Phi(g), 1 gelu(g), 2
- * gelu'(g) = Phi(g) + g phi(g) as the forward and the backward's "both" mode
- * compute them (tail table), 3 Phi(g) and 4 gelu'(g) as the backward's row
- * and column modes compute them (rational tail).  `out` is a device buffer of
+ * gelu'(g) = Phi(g) + g phi(g) from the tail table (the forward, and the
+ * backward's "both" mode with per-group scales), 3 Phi(g) and 4 gelu'(g)
+ * from the rational tail (the rest of the backward).  `out` is a device buffer of
  * 5 * 65536 floats, 16-byte aligned.
  */
 mxfp8_status mxfp8_selftest_activation_gelu(float *out, void *stream);

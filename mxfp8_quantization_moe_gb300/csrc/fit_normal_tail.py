@@ -1,6 +1,6 @@
 """Fit of the rational normal tail used by GEGLU's second fast path (the
-backward's row and column modes of the gated-activation kernels,
-device.cuh): for t >= 0,
+backward of the gated-activation kernels but for "both" with per-group
+scales, device.cuh): for t >= 0,
 
     Phi(-t) = exp(-t^2 / 2) * z * R(z),   z = 1 / (1 + p t),
 

@@ -2,7 +2,7 @@
 
 SwiGLU gates below -16 take the wide-range evaluation (silu(g) = g e^g,
 silu'(g) = (1 + g) e^g to a relative 2^-23, e^g formed with a 2^120 offset);
-GEGLU gates below -6 (-8 in the backward's row and column modes) take the
+GEGLU gates below -6 (-8 in the backward but for per-group "both") take the
 exact path.  Same tolerance as the other
 gated tests (scales bit-exact, codes within one, at most 1e-4 of them):
 

@@ -19,8 +19,8 @@ pytestmark = pytest.mark.gpu
 
 
 def test_gelu_fast_path_error_bounds_for_every_gate():
-    """Both fast paths: the tail table (forward, backward "both"; fast range
-    g >= -6) and the rational tail (backward row and column; g >= -8)."""
+    """Both fast paths: the tail table (forward, per-group backward "both"; fast range
+    g >= -6) and the rational tail (the rest of the backward; g >= -8)."""
     init()
     out = torch.empty(5 * 65536, dtype=torch.float32, device="cuda")
     assert capi.mxfp8_selftest_activation_gelu(out.data_ptr(), torch.cuda.current_stream().cuda_stream) == 0
