@@ -49,17 +49,17 @@ PAGES_US = {("fwd", 1): 904.19, ("fwd", 2): 1022.98, ("fwd", 3): 1216.08,
 # keyed to the hash of the kernel sources it was taken on (None once they
 # change).
 TRAFFIC = {
-    "bwd_both": (10.8327e9, "ae0eb05429c3916e"),
-    "bwd_both_gelu": (10.8439e9, "ae0eb05429c3916e"),
-    "bwd_col": (8.63173e9, "ae0eb05429c3916e"),
-    "bwd_row": (8.63082e9, "ae0eb05429c3916e"),
-    "fwd_both": (6.47807e9, "ae0eb05429c3916e"),
-    "fwd_col": (5.38286e9, "ae0eb05429c3916e"),
-    "fwd_row": (5.38204e9, "ae0eb05429c3916e"),
-    "fwd_row_gelu": (5.38284e9, "ae0eb05429c3916e"),
-    "quant3d": (8.10395e9, "ae0eb05429c3916e"),
-    "quant_both": (4.31582e9, "ae0eb05429c3916e"),
-    "quant_row": (3.22215e9, "ae0eb05429c3916e"),
+    "bwd_both": (10.8328e9, "4a518d3dad333b0d"),
+    "bwd_both_gelu": (10.845e9, "4a518d3dad333b0d"),
+    "bwd_col": (8.63175e9, "4a518d3dad333b0d"),
+    "bwd_row": (8.63187e9, "4a518d3dad333b0d"),
+    "fwd_both": (6.47681e9, "4a518d3dad333b0d"),
+    "fwd_col": (5.38253e9, "4a518d3dad333b0d"),
+    "fwd_row": (5.38212e9, "4a518d3dad333b0d"),
+    "fwd_row_gelu": (5.38247e9, "4a518d3dad333b0d"),
+    "quant3d": (8.105e9, "4a518d3dad333b0d"),
+    "quant_both": (4.31589e9, "4a518d3dad333b0d"),
+    "quant_row": (3.22182e9, "4a518d3dad333b0d"),
 }
 TRAFFIC_KIND = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch of the kernel, "
                 "captured alone in a separate run (bench.py --cell <cell> --steps 1 --warmup 0)")
